@@ -1,0 +1,254 @@
+"""CPU oracle for the tile-wise mixed-precision CG hot path (test infrastructure).
+
+Only the test-suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this package. It wraps ``oracle.c`` (plain, single-threaded C, FP64) with
+ctypes and numpy; it shares no code with the GPU library and never imports it.
+
+The method is the one of "EvoCG: Self-Evolving Precision Control for Faster Conjugate
+Gradient" (arXiv 2611.04469); each C function cites the section it restates.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FP64, FP32, BF16 = 0, 1, 2
+OK, EINVAL, ENOMEM, ENOTCONV, EBREAKDOWN = 0, 1, 2, 4, 5
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (-O2, no fused multiply-add) into _build/liboracle.so."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = C.CDLL(_SO)
+            P = C.c_void_p
+            i64, i32, dbl = C.c_int64, C.c_int, C.c_double
+            lib.ora_round_to_format.restype = dbl
+            lib.ora_round_to_format.argtypes = [dbl, i32, i32, i32]
+            lib.ora_round_f32_array.argtypes = [i64, P, P]
+            lib.ora_round_bf16_array.argtypes = [i64, P, P]
+            lib.ora_csr_spmv.argtypes = [i64, P, P, P, P, P]
+            lib.ora_csr_check.argtypes = [i64, P, P, P]
+            lib.ora_csr_check.restype = i32
+            lib.ora_col_exp.argtypes = [i64, P, P, P, P]
+            lib.ora_tile_count.argtypes = [i64, P, P, i32, P, P]
+            lib.ora_tile_count.restype = i32
+            lib.ora_tile_build.argtypes = [i64, P, P, P, i32] + [P] * 9
+            lib.ora_tile_build.restype = i32
+            lib.ora_mixed_spmv.argtypes = [i64, P, P, P, i32, P, P, P, P, P, P]
+            lib.ora_ctrl_threshold.argtypes = [i64, i32, P, dbl, P]
+            lib.ora_ctrl_mlp.argtypes = [i64, i32, P, i32, i32, P, P, P, P, P, P, dbl, P, P]
+            lib.ora_true_residual.argtypes = [i64, P, P, P, P, P]
+            lib.ora_true_residual.restype = dbl
+            lib.ora_cg_flat.argtypes = ([i64, P, P, P, i32, P, P, P, P, P, dbl, i32, i32,
+                                         i32, P, dbl, i32, i32, i32] + [P] * 6 +
+                                        [dbl, i32, P, P, P, P])
+            lib.ora_cg_flat.restype = i32
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(C.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class CSR:
+    """A square CSR matrix: int64 row pointers, int32 sorted columns, FP64 values."""
+
+    def __init__(self, n, rp, ci, v):
+        self.n = int(n)
+        self.rp = _c(rp, np.int64)
+        self.ci = _c(ci, np.int32)
+        self.v = _c(v, np.float64)
+
+
+def round_to_format(x: float, frac_bits: int, emin: int, emax: int) -> float:
+    return _load().ora_round_to_format(float(x), frac_bits, emin, emax)
+
+
+def round_f32(x):
+    """FP64 -> FP32, round-to-nearest-even, as an FP32 array."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.float32)
+    _load().ora_round_f32_array(x.size, _p(x), _p(out))
+    return out
+
+
+def round_bf16_bits(x):
+    """FP64 -> BF16 (single rounding, nearest-even), as uint16 bit patterns."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, np.uint16)
+    _load().ora_round_bf16_array(x.size, _p(x), _p(out))
+    return out
+
+
+def csr_check(A: CSR) -> int:
+    return _load().ora_csr_check(A.n, _p(A.rp), _p(A.ci), _p(A.v))
+
+
+def csr_spmv(A: CSR, x):
+    x = _c(x, np.float64)
+    y = np.empty(A.n, np.float64)
+    _load().ora_csr_spmv(A.n, _p(A.rp), _p(A.ci), _p(A.v), _p(x), _p(y))
+    return y
+
+
+def col_exp(A: CSR):
+    e = np.empty(A.n, np.int8)
+    _load().ora_col_exp(A.n, _p(A.rp), _p(A.ci), _p(A.v), _p(e))
+    return e
+
+
+class Tiles:
+    """The oracle's own tile layout (arrays named as in the GPU library's export)."""
+
+    def __init__(self, A: CSR, T: int):
+        lib = _load()
+        nt, nz = C.c_int64(), C.c_int64()
+        st = lib.ora_tile_count(A.n, _p(A.rp), _p(A.ci), int(T), C.byref(nt), C.byref(nz))
+        if st != OK:
+            raise ValueError(f"tile count failed: status {st}")
+        self.n, self.T = A.n, int(T)
+        self.nrb = (A.n + T - 1) // T
+        self.ntiles, self.nnz = nt.value, nz.value
+        self.tileRowPtr = np.empty(self.nrb + 1, np.int64)
+        self.tileColIdx = np.empty(max(self.ntiles, 1), np.int32)
+        self.tileNnzOff = np.empty(self.ntiles + 1, np.int64)
+        self.rowEnd = np.empty(max(self.ntiles * T, 1), np.uint16)
+        self.colIdx = np.empty(max(self.nnz, 1), np.uint8)
+        self.v64 = np.empty(max(self.nnz, 1), np.float64)
+        self.v32 = np.empty(max(self.nnz, 1), np.float32)
+        self.v16 = np.empty(max(self.nnz, 1), np.uint16)
+        self.colExp = np.empty(max(A.n, 1), np.int8)
+        st = lib.ora_tile_build(A.n, _p(A.rp), _p(A.ci), _p(A.v), int(T), _p(self.tileRowPtr),
+                                _p(self.tileColIdx), _p(self.tileNnzOff), _p(self.rowEnd),
+                                _p(self.colIdx), _p(self.v64), _p(self.v32), _p(self.v16),
+                                _p(self.colExp))
+        if st != OK:
+            raise ValueError(f"tile build failed: status {st}")
+        self.tileColIdx = self.tileColIdx[: self.ntiles]
+        self.rowEnd = self.rowEnd[: self.ntiles * T]
+        self.colIdx, self.v64 = self.colIdx[: self.nnz], self.v64[: self.nnz]
+        self.v32, self.v16 = self.v32[: self.nnz], self.v16[: self.nnz]
+        self.colExp = self.colExp[: A.n]
+
+    def tile_rows(self):
+        """Row-block index of every tile."""
+        return np.repeat(np.arange(self.nrb, dtype=np.int64), np.diff(self.tileRowPtr))
+
+    def to_csr(self) -> CSR:
+        """Rebuild CSR (FP64 stream) from the layout: the round-trip check."""
+        T = self.T
+        rows, cols, vals = [], [], []
+        trow = self.tile_rows()
+        for t in range(self.ntiles):
+            off = int(self.tileNnzOff[t])
+            start = 0
+            for r in range(T):
+                end = int(self.rowEnd[t * T + r])
+                for k in range(off + start, off + end):
+                    rows.append(trow[t] * T + r)
+                    cols.append(int(self.tileColIdx[t]) * T + int(self.colIdx[k]))
+                    vals.append(self.v64[k])
+                start = end
+        rows, cols, vals = np.array(rows, np.int64), np.array(cols, np.int64), np.array(vals)
+        order = np.lexsort((cols, rows))
+        rows, cols, vals = rows[order], cols[order], vals[order]
+        rp = np.zeros(self.n + 1, np.int64)
+        np.add.at(rp, rows + 1, 1)
+        return CSR(self.n, np.cumsum(rp), cols.astype(np.int32), vals)
+
+
+def mixed_spmv(A: CSR, tiles: Tiles, tile_prec, x):
+    """Emulated mixed-precision SpMV (tile_prec None = every tile FP64)."""
+    x = _c(x, np.float64)
+    y = np.empty(A.n, np.float64)
+    tp = None if tile_prec is None else _c(tile_prec, np.uint8)
+    _load().ora_mixed_spmv(A.n, _p(A.rp), _p(A.ci), _p(A.v), tiles.T, _p(tiles.colExp),
+                           _p(tiles.tileRowPtr), _p(tiles.tileColIdx), _p(tp), _p(x), _p(y))
+    return y
+
+
+def ctrl_threshold(p, T: int, eps: float):
+    p = _c(p, np.float64)
+    ncb = (p.size + T - 1) // T
+    out = np.empty(ncb, np.uint8)
+    _load().ora_ctrl_threshold(p.size, T, _p(p), float(eps), _p(out))
+    return out
+
+
+def ctrl_mlp(p, T: int, weights, delta: float):
+    """weights = (W1, b1, W2, b2, W3, b3), FP32, W row-major (out, in). Returns (map, logits)."""
+    p = _c(p, np.float64)
+    W1, b1, W2, b2, W3, b3 = [_c(w, np.float32) for w in weights]
+    H1, H2 = b1.size, b2.size
+    ncb = (p.size + T - 1) // T
+    out = np.empty(ncb, np.uint8)
+    logits = np.empty(ncb * 3, np.float64)
+    _load().ora_ctrl_mlp(p.size, T, _p(p), H1, H2, _p(W1), _p(b1), _p(W2), _p(b2), _p(W3),
+                         _p(b3), float(delta), _p(out), _p(logits))
+    return out, logits.reshape(ncb, 3)
+
+
+def true_residual(A: CSR, b, x) -> float:
+    b, x = _c(b, np.float64), _c(x, np.float64)
+    return _load().ora_true_residual(A.n, _p(A.rp), _p(A.ci), _p(A.v), _p(b), _p(x))
+
+
+def cg(A: CSR, tiles: Tiles, b, rtol: float, maxit: int, jacobi: bool = False,
+       ctrl: str = "static", tile_map=None, eps: float = 0.0, kstar: int = 1,
+       weights=None, delta: float = 1e-30, finish_fp64: bool = False):
+    """CG / Jacobi-PCG with a static map or an in-loop controller ('threshold', 'mlp').
+
+    Returns a dict: status, x, iters, iters_rec, restarts, hist (iters+1 entries),
+    rel_res (recursive), true_res (FP64 recomputed), prec_nnz (entries per precision).
+    """
+    b = _c(b, np.float64)
+    x = np.zeros(A.n, np.float64)
+    hist = np.zeros(maxit + 1, np.float64)
+    out = np.zeros(3, np.int64)
+    fout = np.zeros(2, np.float64)
+    pn = np.zeros(3, np.int64)
+    kind = {"static": 0, "threshold": 1, "mlp": 2}[ctrl]
+    tm = None if tile_map is None else _c(tile_map, np.uint8)
+    if weights is not None:
+        W = [_c(w, np.float32) for w in weights]
+        H1, H2 = W[1].size, W[3].size
+    else:
+        W, H1, H2 = [None] * 6, 0, 0
+    st = _load().ora_cg_flat(A.n, _p(A.rp), _p(A.ci), _p(A.v), tiles.T, _p(tiles.tileRowPtr),
+                             _p(tiles.tileColIdx), _p(tiles.colExp), _p(b), _p(x), float(rtol),
+                             int(maxit), int(bool(jacobi)), kind, _p(tm), float(eps), int(kstar),
+                             H1, H2, *[_p(w) for w in W], float(delta), int(bool(finish_fp64)),
+                             _p(hist), _p(out), _p(fout), _p(pn))
+    it = int(out[0])
+    return dict(status=st, x=x, iters=it, iters_rec=int(out[1]), restarts=int(out[2]),
+                hist=hist[: it + 1].copy(), rel_res=float(fout[0]), true_res=float(fout[1]),
+                prec_nnz=pn.copy())
