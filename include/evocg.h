@@ -1,0 +1,207 @@
+/*
+ * evocg.h -- C ABI of the GB300 tile-wise mixed-precision CG library (libevocg.so).
+ *
+ * The method is the one of "EvoCG: Self-Evolving Precision Control for Faster Conjugate
+ * Gradient" (arXiv 2611.04469): a sparse matrix cut into square tiles, each tile holding
+ * its values in FP64, FP32 and BF16 and read in the precision a per-tile map selects
+ * (§3.3 EvoSpMV, Fig. 4), inside a CG / Jacobi-PCG loop (§2.1 Fig. 1, §4.6) whose map is
+ * rewritten in-loop by a controller (§3.2 Eq. 8-10, §4.7), run on the device without a
+ * host round trip per iteration (§3.4 EvoRun, Fig. 5).
+ *
+ * Conventions for every call:
+ *  - Return value: an evocg_status; EVOCG_OK (0) on success. No call throws, aborts or
+ *    prints. evocg_last_error() gives a message for the calling thread's last failure.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Device work is queued
+ *    on it; a call that must hand back a host-visible result synchronises that stream.
+ *  - Vector arguments marked "host or device" may point to either; the library checks
+ *    with cudaPointerGetAttributes and stages host data through its own device buffers.
+ *  - Indices are 0-based. Matrices are square, n x n, n < 2^31.
+ *  - The caller owns every pointer it passes; the library owns the tile structure and
+ *    its workspaces, which evocg_tiles_free releases. A handle may be used from one
+ *    thread at a time.
+ */
+#ifndef EVOCG_H
+#define EVOCG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct evocg_tiles *evocg_tiles_t;
+
+typedef enum {
+    EVOCG_OK = 0,
+    EVOCG_EINVAL = 1,      /* bad argument or input (message says which) */
+    EVOCG_ENOMEM = 2,      /* a device or host allocation failed */
+    EVOCG_ECUDA = 3,       /* a CUDA runtime call failed */
+    EVOCG_ENOTCONV = 4,    /* CG stopped at maxit; iterations and history are filled */
+    EVOCG_EBREAKDOWN = 5,  /* p.Ap <= 0 or not finite: the operator is not SPD */
+    EVOCG_ETIMEOUT = 6,    /* a bounded device wait ran out */
+    EVOCG_EDEVICE = 7      /* no usable CUDA device, or not an sm_103 device */
+} evocg_status;
+
+/* Precision codes of EvoCG Eq. 9. */
+enum { EVOCG_FP64 = 0, EVOCG_FP32 = 1, EVOCG_BF16 = 2 };
+
+/* Map layouts for evocg_set_tile_precision. */
+enum {
+    EVOCG_MAP_PER_TILE = 0,     /* one code per nonempty tile, in tile order */
+    EVOCG_MAP_PER_COLBLOCK = 1  /* one code per column block (EvoCG Eq. 10), every tile of
+                                   column block i takes code i */
+};
+
+/* Controllers (EvoCG §3.2, §4.7). */
+enum {
+    EVOCG_CTRL_STATIC = 0,     /* the matrix's current map is used for every iteration */
+    EVOCG_CTRL_THRESHOLD = 1,  /* residual-threshold rule on m_i = max |p_i| */
+    EVOCG_CTRL_MLP = 2         /* policy MLP on phi(p_i) = p_i / max(||p_i||, delta) */
+};
+
+typedef struct {
+    int64_t n;            /* matrix order */
+    int64_t nrb;          /* row blocks = column blocks = ceil(n / tile_size) */
+    int64_t ntiles;       /* nonempty tiles */
+    int64_t nnz;          /* stored entries */
+    int32_t tile_size;    /* T: tiles are T x T */
+    int32_t map_kind;     /* which map the SpMV reads (EVOCG_MAP_*) */
+    int64_t bytes_index;  /* tileRowPtr + tileColIdx + tileNnzOff + rowEnd + colIdx */
+    int64_t bytes_v64, bytes_v32, bytes_v16, bytes_colexp;
+} evocg_tiles_desc;
+
+typedef struct {
+    int kind;              /* EVOCG_CTRL_* */
+    int kstar;             /* the controller runs on iterations k with k % kstar == 0 (EvoCG
+                              §3.4 interval reuse); values < 1 mean 1 */
+    double eps;            /* THRESHOLD: BF16 if m_i < 0.1 eps, FP32 if m_i < eps, else FP64 */
+    int hidden1, hidden2;  /* MLP hidden widths (EvoCG §4.1: 64, 64); at most 64 each */
+    const float *weights;  /* MLP: host pointer to W1 (hidden1 x T), b1, W2 (hidden2 x
+                              hidden1), b2, W3 (3 x hidden2), b3, packed in that order, each
+                              W row-major (out, in), FP32 */
+    double delta;          /* MLP: the floor of the segment norm in phi (EvoCG Eq. 8) */
+} evocg_ctrl;
+
+typedef struct {
+    int status;            /* same value the solve returns */
+    int iters;             /* SpMVs performed in the loop, restarts included */
+    int iters_recursive;   /* iterations at the first recursive convergence, or -1 */
+    int restarts;          /* FP64-finish restarts taken */
+    double rel_res;        /* last recursively updated ||r_k|| / ||r_0|| */
+    double true_res;       /* ||b - A x|| / ||b|| recomputed in FP64 (all tiles FP64), or -1 */
+    int64_t prec_nnz[3];   /* stored entries processed per precision, summed over SpMVs */
+    int64_t ctrl_calls;    /* controller invocations */
+} evocg_solve_info;
+
+/*
+ * Build the tile structure (EvoCG §3.3.1 Fig. 4(a) and §3.3.2): row blocks of
+ * tile_size rows, the nonempty tile_size x tile_size tiles of each row block listed in
+ * ascending column block (tileRowPtr / tileColIdx), inside a tile the entries row by
+ * row with ascending column (one end offset per local row in rowEnd, one local column
+ * per entry in colIdx), and three value streams over the same entries: FP64 a_ij, FP32
+ * and BF16 of a_ij / s_j, where s_j = 2^e_j is the per-column factor of §3.3.2 with
+ * e_j = floor(log2 max_i |a_ij|) clamped to [-100, 100] (0 for an empty column). FP32 and
+ * BF16 values are rounded once from FP64, to nearest with ties to even.
+ *   n, row_ptr (n+1, int64), col_idx (row_ptr[n], int32, strictly ascending per row,
+ *   0 <= col < n), vals (FP64, finite): HOST pointers, read only.
+ *   tile_size: 16, 32 or 64.
+ *   *out receives the handle; the map starts all-FP64 (per tile).
+ * Errors: EINVAL (bad sizes, unsorted or out-of-range columns, non-finite values),
+ * ENOMEM, ECUDA, EDEVICE.
+ */
+int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                     const double *vals, int tile_size, evocg_tiles_t *out);
+
+/* Release the handle and all device memory it owns (synchronises the device first).
+ * NULL is accepted. */
+int evocg_tiles_free(evocg_tiles_t A);
+
+/* Sizes of the structure. d: host pointer. */
+int evocg_tiles_info(evocg_tiles_t A, evocg_tiles_desc *d);
+
+/*
+ * Copy the structure back to HOST arrays, for bit-exact layout checks. Sizes:
+ * tileRowPtr nrb+1, tileColIdx ntiles, tileNnzOff ntiles+1, rowEnd ntiles*T,
+ * colIdx / v64 / v32 / v16 nnz, colExp n. Any pointer may be NULL to skip that array.
+ * Synchronises the device.
+ */
+int evocg_tiles_export(evocg_tiles_t A, int64_t *tileRowPtr, int32_t *tileColIdx,
+                       int64_t *tileNnzOff, uint16_t *rowEnd, uint8_t *colIdx, double *v64,
+                       float *v32, uint16_t *v16, int8_t *colExp);
+
+/*
+ * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
+ *   map: host or device, len = ntiles (PER_TILE) or nrb (PER_COLBLOCK).
+ * The SpMV and static-map solves read the map set last. Errors: EINVAL on a wrong length
+ * or a code above 2 (the map is checked on the host; a device map is copied there).
+ */
+int evocg_set_tile_precision(evocg_tiles_t A, const uint8_t *map, int64_t len,
+                             int map_kind, void *stream);
+
+/* Copy the current per-tile map (the per-column-block map broadcast to tiles when that
+ * kind is set) to a HOST array of ntiles entries. Synchronises the stream. */
+int evocg_get_tile_precision(evocg_tiles_t A, uint8_t *map_out, int64_t len, void *stream);
+
+/*
+ * Mixed-precision SpMV y = (A + E(map)) x (EvoCG Eq. 2 / Eq. 5 and §3.3.2): a tile in
+ * FP64 multiplies its FP64 values by x; a tile in FP32 or BF16 multiplies its FP32/BF16
+ * values by the x entries rounded to the same format and scaled by s_j. Every product is
+ * exact or, for FP64 tiles, rounded once; each row is summed in FP64 (FP32/BF16 products
+ * through an error-free FP32 pair). x, y: host or device, n FP64 each, not overlapping.
+ * Asynchronous on `stream` for device pointers; with a host pointer the call returns once
+ * y is written.
+ */
+int evocg_spmv(evocg_tiles_t A, const double *x, double *y, void *stream);
+
+/*
+ * CG (jacobi = 0) or Jacobi-preconditioned CG (jacobi = 1) for A x = b from x0 = 0, in
+ * the order of EvoCG Algorithm 1 (the solver lines) and §4.6:
+ *   controller on p_k when k % kstar == 0; q = A~ p; sigma = p.q (breakdown unless
+ *   finite and > 0); alpha = rho / sigma; x += alpha p; r -= alpha q;
+ *   res_hist[k+1] = ||r|| / ||r_0||; stop when <= rtol (the recursively updated residual,
+ *   §4.1); z = D^-1 r (or r); rho' = r.z; beta = rho'/rho; p = z + beta p.
+ * All vector arithmetic is FP64; only the SpMV follows the precision map. The whole loop
+ * runs on the device as one CUDA graph with a conditional while node: no host round trip
+ * per iteration.
+ *   b: host or device, n FP64. x: host or device, n FP64 (output; x0 = 0).
+ *   rtol > 0 or 0 (run maxit iterations); maxit >= 0.
+ *   ctrl: NULL = static map (the map set last); otherwise a controller.
+ *   finish_fp64: after a recursive convergence, recompute ||b - A x|| in FP64; if above
+ *   rtol, continue from r = b - A x with every tile in FP64 (up to 8 restarts).
+ *   res_hist: host or device, maxit+1 FP64 entries, or NULL; entries past iters are
+ *   left untouched.
+ *   info: host pointer or NULL.
+ * Returns OK on convergence, ENOTCONV at maxit, EBREAKDOWN, or an error. Synchronises
+ * `stream` before returning. Jacobi needs every diagonal entry present and > 0 (EINVAL).
+ */
+int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, double rtol, int maxit,
+                   int jacobi, const evocg_ctrl *ctrl, int finish_fp64, double *res_hist,
+                   evocg_solve_info *info, void *stream);
+
+/*
+ * One controller decision (EvoCG Eq. 8-10, §4.7) on a given vector p, for controller
+ * parity checks: cb_prec[i] for each column block i of A. p: host or device, n FP64.
+ * cb_prec: host or device, nrb bytes. logits: NULL or host/device 3*nrb FP32 (MLP only).
+ * Synchronises the stream for host outputs.
+ */
+int evocg_ctrl_decide(evocg_tiles_t A, const evocg_ctrl *ctrl, const double *p,
+                      uint8_t *cb_prec, float *logits, void *stream);
+
+/*
+ * The device's FP64 -> FP32 and FP64 -> BF16 rounding (integer-pipe, round to nearest
+ * even, one rounding from FP64), exposed for rounding checks. x: host or device, n FP64;
+ * out32 (FP32) / out16 (BF16 bit patterns): host or device, may be NULL.
+ */
+int evocg_round(const double *x, int64_t n, float *out32, uint16_t *out16, void *stream);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char *evocg_last_error(void);
+
+/* Library ABI version (increases on incompatible changes). */
+int evocg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EVOCG_H */

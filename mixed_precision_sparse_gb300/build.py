@@ -1,0 +1,91 @@
+"""Build libevocg.so in-tree for sm_103a (GB300) with nvcc; no cmake, no torch extension.
+
+Objects go to mixed_precision_sparse_gb300/_build/, the library next to this file.
+Translation units compile in parallel; a unit is rebuilt when it or a header changed.
+"""
+from __future__ import annotations
+
+import glob
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INC = os.path.join(ROOT, "include")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB = os.path.join(HERE, "libevocg.so")
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _nvcc():
+    p = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(p):
+        raise RuntimeError("nvcc not found (CUDA 13 toolkit required)")
+    return p
+
+
+def _headers():
+    return glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
+        glob.glob(os.path.join(INC, "*.h"))
+
+
+def _stale(obj, src, deps):
+    if not os.path.exists(obj):
+        return True
+    t = os.path.getmtime(obj)
+    return any(os.path.getmtime(d) > t for d in [src, *deps])
+
+
+def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
+    os.makedirs(OUT_DIR, exist_ok=True)
+    nvcc = _nvcc()
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    deps = _headers()
+    common = ["-std=c++17", "-O3", "-I", INC, "-I", CSRC, "-Xcompiler", "-fPIC"]
+    jobs = []
+    objs = []
+    for s in srcs:
+        obj = os.path.join(OUT_DIR, os.path.basename(s) + ".o")
+        objs.append(obj)
+        if force or _stale(obj, s, deps):
+            cmd = [nvcc, *common, "-c", s, "-o", obj]
+            if s.endswith(".cu"):
+                cmd[1:1] = [*ARCH, "-lineinfo", "-rdc=true"]
+                if ptxas_verbose:
+                    cmd.insert(1, "-Xptxas=-v")
+            else:
+                cmd[1:1] = ["-x", "c++"]
+            jobs.append(cmd)
+
+    def run(cmd):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        return cmd, r
+
+    failed = []
+    with ThreadPoolExecutor(max_workers=min(8, max(1, len(jobs)))) as ex:
+        for cmd, r in ex.map(run, jobs):
+            if verbose or ptxas_verbose or r.returncode:
+                sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
+            if r.returncode:
+                failed.append(cmd[-3])
+    if failed:
+        raise RuntimeError(f"nvcc failed for {failed}")
+    if force or jobs or not os.path.exists(LIB):
+        tmp = LIB + f".tmp{os.getpid()}"
+        cudalib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "lib64")
+        link = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcudadevrt",
+                "-lpthread", "-Xlinker", "-rpath", "-Xlinker", cudalib]
+        r = subprocess.run(link, capture_output=True, text=True)
+        if r.returncode:
+            raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
+        os.replace(tmp, LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
+                ptxas_verbose="--ptxas" in sys.argv))

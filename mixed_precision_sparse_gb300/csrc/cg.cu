@@ -1,0 +1,389 @@
+// cg.cu -- fused CG / Jacobi-PCG vector kernels (EvoCG, "Self-Evolving Precision Control
+// for Faster Conjugate Gradient": the solver lines of Algorithm 1, §2.1 Fig. 1, §3.4
+// fused step, §4.6 Jacobi-PCG) for sm_103a.
+//
+// One iteration is three kernels in a CUDA graph: the SpMV with p.q fused into its
+// epilogue (its last block forms alpha), cg_update (x, r, z and the two dot products;
+// its last block forms beta, the history entry and the stop flag, and drives the graph's
+// while node), and cg_pupdate (p, the rounded copies of p that the next SpMV reads, and
+// the threshold controller's decisions). Reductions are per-thread FP64 partials in a
+// fixed order, a fixed shuffle tree per block, and a last-block sum over the blocks in
+// index order: bit-reproducible from run to run. FP64 instructions are only the method's
+// own (one per axpy or dot term); conversions and comparisons run on the integer pipe.
+#include <cuda_runtime.h>
+
+#include "evocg_internal.h"
+#include "fpconv.cuh"
+
+namespace evocg {
+
+__device__ __forceinline__ bool last_block_cg(DevState *st, int slot)
+{
+    __shared__ bool amLast;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned t = atomicAdd(&st->tickets[slot], 1u);
+        amLast = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (amLast) __threadfence();
+    return amLast;
+}
+
+__device__ __forceinline__ double block_sum_cg(double v)
+{
+    __shared__ double ws[32];
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) ws[w] = v;
+    __syncthreads();
+    double s = 0.0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += ws[i];
+    return s;
+}
+
+// Sum of gridDim.x partials in a fixed order; valid in thread 0 of the calling block.
+__device__ __forceinline__ double sum_partials(const double *part)
+{
+    double v = 0.0;
+    for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) v += __ldcg(part + i);
+    return block_sum_cg(v);
+}
+
+__device__ __forceinline__ uint64_t abs_bits(double v)
+{
+    return (uint64_t)__double_as_longlong(v) & 0x7FFFFFFFFFFFFFFFull;
+}
+
+// Threshold rule of EvoCG §4.7 on segments of T entries held by T/2 consecutive lanes
+// (two entries per lane): m = max |p| over the segment, compared through the bit
+// patterns of non-negative doubles (which order like the values; a NaN compares above
+// every threshold and keeps FP64). Every lane of the warp must call it.
+template <int T>
+__device__ __forceinline__ void threshold_segments(uint64_t m, int64_t pair, int64_t ncb,
+                                                   uint64_t lo_bits, uint64_t hi_bits,
+                                                   uint8_t *cbPrec)
+{
+    constexpr int W = T / 2;
+#pragma unroll
+    for (int o = W / 2; o; o >>= 1) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, m, o);
+        m = other > m ? other : m;
+    }
+    if ((threadIdx.x & (W - 1)) == 0) {
+        const int64_t seg = (2 * pair) / T;
+        if (seg < ncb) cbPrec[seg] = (m < lo_bits) ? EVOCG_BF16 : (m < hi_bits) ? EVOCG_FP32 : EVOCG_FP64;
+    }
+}
+
+// Rounded copies of p for the next SpMV's low-precision tiles (x32, x16) and its
+// threshold features; entries past n are zero.
+__device__ __forceinline__ void write_copies(const CgLaunch &L, int64_t j, double v)
+{
+    const float s = pow2f(L.A.colExp[j]);
+    L.x32[j] = __fmul_rn(f32_from_f64_rn(v), s);
+    L.x16[j] = (uint16_t)(__float_as_uint(__fmul_rn(f32_from_bf16(bf16_from_f64_rn(v)), s)) >> 16);
+}
+
+// Start (restart = 0) or FP64-finish restart (restart = 1, after q = A x in FP64):
+//   r = b (x = 0) or r = b - q; z = D^-1 r; p = z; rho = r.z; ||r||^2.
+template <int T>
+__global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int restart)
+{
+    DevState *st = L.st;
+    const int64_t n = L.n, npairs = (n + 1) / 2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const bool thr = (L.ctrl == EVOCG_CTRL_THRESHOLD) && !restart;
+    const uint64_t lo_bits = (uint64_t)__double_as_longlong(st->eps_lo);
+    const uint64_t hi_bits = (uint64_t)__double_as_longlong(st->eps_hi);
+    const int64_t ncb = (n + T - 1) / T;
+    double rz = 0.0, rr = 0.0;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < npairs;
+         base += stride) {
+        const int64_t pair = base + lane;
+        uint64_t m = 0;
+        if (pair < npairs) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t j = 2 * pair + h;
+                if (j >= n) break;
+                double r = L.b[j];
+                if (restart) r = r - L.q[j];
+                else L.x[j] = 0.0;
+                L.r[j] = r;
+                double z = r;
+                if (L.jacobi) { z = L.dinv[j] * r; L.z[j] = z; }
+                L.p[j] = z;
+                write_copies(L, j, z);
+                rz = fma(r, z, rz);
+                rr = fma(r, r, rr);
+                const uint64_t ab = abs_bits(z);
+                m = ab > m ? ab : m;
+            }
+        }
+        if (thr) threshold_segments<T>(m, pair, ncb, lo_bits, hi_bits, L.cbPrec);
+    }
+    const double s_rz = block_sum_cg(rz);
+    const double s_rr = block_sum_cg(rr);
+    if (threadIdx.x == 0) {
+        L.partials[blockIdx.x] = s_rz;
+        L.partials[kMaxBlocks + blockIdx.x] = s_rr;
+    }
+    if (last_block_cg(st, TK_INIT)) {
+        const double RZ = sum_partials(L.partials);
+        const double RR = sum_partials(L.partials + kMaxBlocks);
+        if (threadIdx.x == 0) {
+            st->tickets[TK_INIT] = 0;
+            st->rho = L.jacobi ? RZ : RR;
+            st->rr = RR;
+            if (!restart) {
+                st->nr0 = sqrt(RR);
+                st->k = 0;
+                L.hist[0] = 1.0;
+                st->status = EVOCG_OK;
+                st->converged = 0;
+                if (thr) st->ctrl_calls += 1;
+            }
+            st->done = 0;
+            if (RR == 0.0) {             // b = 0 (or an exact restart residual of zero)
+                st->done = 1;
+                st->converged = 1;
+                st->status = EVOCG_OK;
+            } else if (st->k >= st->maxit) {
+                st->done = 1;
+                st->status = EVOCG_ENOTCONV;
+            }
+            cudaGraphSetConditional(L.cond, st->done ? 0u : 1u);
+        }
+    }
+}
+
+// x += alpha p; r -= alpha q; z = D^-1 r; r.z and ||r||^2. The last block appends the
+// history entry, tests convergence and forms beta.
+__global__ void __launch_bounds__(kVecThreads) cg_update_kernel(CgLaunch L)
+{
+    DevState *st = L.st;
+    if (st->done) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) cudaGraphSetConditional(L.cond, 0u);
+        return;
+    }
+    const double alpha = st->alpha;
+    const int64_t n = L.n, npairs = (n + 1) / 2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    double rz = 0.0, rr = 0.0;
+    for (int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; pair < npairs; pair += stride) {
+        const int64_t j = 2 * pair;
+        if (j + 1 < n) {
+            const double2 p = *reinterpret_cast<const double2 *>(L.p + j);
+            const double2 q = *reinterpret_cast<const double2 *>(L.q + j);
+            double2 x = *reinterpret_cast<const double2 *>(L.x + j);
+            double2 r = *reinterpret_cast<const double2 *>(L.r + j);
+            x.x = fma(alpha, p.x, x.x);
+            x.y = fma(alpha, p.y, x.y);
+            r.x = fma(-alpha, q.x, r.x);
+            r.y = fma(-alpha, q.y, r.y);
+            *reinterpret_cast<double2 *>(L.x + j) = x;
+            *reinterpret_cast<double2 *>(L.r + j) = r;
+            rr = fma(r.x, r.x, rr);
+            rr = fma(r.y, r.y, rr);
+            if (L.jacobi) {
+                const double2 d = *reinterpret_cast<const double2 *>(L.dinv + j);
+                double2 z;
+                z.x = d.x * r.x;
+                z.y = d.y * r.y;
+                *reinterpret_cast<double2 *>(L.z + j) = z;
+                rz = fma(r.x, z.x, rz);
+                rz = fma(r.y, z.y, rz);
+            }
+        } else {
+            const double x = fma(alpha, L.p[j], L.x[j]);
+            const double r = fma(-alpha, L.q[j], L.r[j]);
+            L.x[j] = x;
+            L.r[j] = r;
+            rr = fma(r, r, rr);
+            if (L.jacobi) {
+                const double z = L.dinv[j] * r;
+                L.z[j] = z;
+                rz = fma(r, z, rz);
+            }
+        }
+    }
+    const double s_rz = block_sum_cg(rz);
+    const double s_rr = block_sum_cg(rr);
+    if (threadIdx.x == 0) {
+        L.partials[blockIdx.x] = s_rz;
+        L.partials[kMaxBlocks + blockIdx.x] = s_rr;
+    }
+    if (last_block_cg(st, TK_UPDATE)) {
+        const double RZ = sum_partials(L.partials);
+        const double RR = sum_partials(L.partials + kMaxBlocks);
+        if (threadIdx.x == 0) {
+            st->tickets[TK_UPDATE] = 0;
+            const int k = st->k + 1;
+            st->k = k;
+            st->rr = RR;
+            const double h = sqrt(RR) / st->nr0;
+            L.hist[k] = h;
+            if (h <= st->rtol) {
+                st->done = 1;
+                st->converged = 1;
+                st->status = EVOCG_OK;
+            } else if (k >= st->maxit) {
+                st->done = 1;
+                st->status = EVOCG_ENOTCONV;
+            } else {
+                const double rho_new = L.jacobi ? RZ : RR;
+                st->beta = rho_new / st->rho;
+                st->rho = rho_new;
+            }
+            cudaGraphSetConditional(L.cond, st->done ? 0u : 1u);
+        }
+    }
+}
+
+// p = z + beta p, its rounded copies, and the threshold rule when it is due.
+template <int T>
+__global__ void __launch_bounds__(kVecThreads) cg_pupdate_kernel(CgLaunch L)
+{
+    DevState *st = L.st;
+    if (st->done) return;
+    const double beta = st->beta;
+    const int64_t n = L.n, npairs = (n + 1) / 2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int lane = threadIdx.x & 31;
+    const bool thr = (L.ctrl == EVOCG_CTRL_THRESHOLD) && (st->k % st->kstar == 0);
+    const uint64_t lo_bits = (uint64_t)__double_as_longlong(st->eps_lo);
+    const uint64_t hi_bits = (uint64_t)__double_as_longlong(st->eps_hi);
+    const int64_t ncb = (n + T - 1) / T;
+    const double *zsrc = L.jacobi ? L.z : L.r;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < npairs;
+         base += stride) {
+        const int64_t pair = base + lane;
+        uint64_t m = 0;
+        if (pair < npairs) {
+            const int64_t j = 2 * pair;
+            if (j + 1 < n) {
+                const double2 z = *reinterpret_cast<const double2 *>(zsrc + j);
+                double2 p = *reinterpret_cast<const double2 *>(L.p + j);
+                p.x = fma(beta, p.x, z.x);
+                p.y = fma(beta, p.y, z.y);
+                *reinterpret_cast<double2 *>(L.p + j) = p;
+                write_copies(L, j, p.x);
+                write_copies(L, j + 1, p.y);
+                const uint64_t a0 = abs_bits(p.x), a1 = abs_bits(p.y);
+                m = a0 > a1 ? a0 : a1;
+            } else {
+                const double p = fma(beta, L.p[j], zsrc[j]);
+                L.p[j] = p;
+                write_copies(L, j, p);
+                m = abs_bits(p);
+            }
+        }
+        if (thr) threshold_segments<T>(m, pair, ncb, lo_bits, hi_bits, L.cbPrec);
+    }
+    if (thr && blockIdx.x == 0 && threadIdx.x == 0) st->ctrl_calls += 1;
+}
+
+// FP64 true residual ||b - q||^2 and ||b||^2 with q = A x from an all-FP64 SpMV.
+__global__ void __launch_bounds__(kVecThreads) true_residual_kernel(CgLaunch L)
+{
+    DevState *st = L.st;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    double num = 0.0, den = 0.0;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < L.n; j += stride) {
+        const double b = L.b[j];
+        const double d = b - L.q[j];
+        num = fma(d, d, num);
+        den = fma(b, b, den);
+    }
+    const double s_n = block_sum_cg(num);
+    const double s_d = block_sum_cg(den);
+    if (threadIdx.x == 0) {
+        L.partials[blockIdx.x] = s_n;
+        L.partials[kMaxBlocks + blockIdx.x] = s_d;
+    }
+    if (last_block_cg(st, TK_TRUE)) {
+        const double N = sum_partials(L.partials);
+        const double D = sum_partials(L.partials + kMaxBlocks);
+        if (threadIdx.x == 0) {
+            st->tickets[TK_TRUE] = 0;
+            st->tr_num = N;
+            st->tr_den = D;
+        }
+    }
+}
+
+template <int T>
+static cudaError_t init_T(const CgLaunch &L, int restart, cudaStream_t s)
+{
+    cg_init_kernel<T><<<L.vec_grid, kVecThreads, 0, s>>>(L, restart);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_cg_init(const CgLaunch &L, int restart, cudaStream_t s)
+{
+    switch (L.T) {
+    case 16: return init_T<16>(L, restart, s);
+    case 32: return init_T<32>(L, restart, s);
+    case 64: return init_T<64>(L, restart, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// One loop body: [MLP controller] -> SpMV (+ p.q, alpha) -> update -> p-update.
+cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
+{
+    cudaError_t e;
+    if (!force64 && L.ctrl == EVOCG_CTRL_MLP) {
+        e = launch_ctrl_mlp(L.A, L.p, L.mlpW, L.H1, L.H2, L.delta, L.cbPrec, nullptr, L.st, s);
+        if (e != cudaSuccess) return e;
+    }
+    SpmvLaunch S{};
+    S.A = L.A;
+    S.x64 = L.p;
+    S.x32 = L.x32;
+    S.x16 = L.x16;
+    S.y = L.q;
+    S.prec = (L.ctrl == EVOCG_CTRL_STATIC) ? L.prec : L.cbPrec;
+    S.map_kind = (L.ctrl == EVOCG_CTRL_STATIC) ? L.map_kind : EVOCG_MAP_PER_COLBLOCK;
+    S.force64 = force64;
+    S.dot = 1;
+    S.partials = L.partials;
+    S.st = L.st;
+    S.census = 1;
+    S.grid = L.spmv_grid;
+    e = launch_spmv(S, s);
+    if (e != cudaSuccess) return e;
+    cg_update_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    switch (L.T) {
+    case 16: cg_pupdate_kernel<16><<<L.vec_grid, kVecThreads, 0, s>>>(L); break;
+    case 32: cg_pupdate_kernel<32><<<L.vec_grid, kVecThreads, 0, s>>>(L); break;
+    default: cg_pupdate_kernel<64><<<L.vec_grid, kVecThreads, 0, s>>>(L); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_true_residual(const CgLaunch &L, cudaStream_t s)
+{
+    SpmvLaunch S{};
+    S.A = L.A;
+    S.x64 = L.x;
+    S.y = L.q;
+    S.force64 = 1;
+    S.dot = 0;
+    S.st = L.st;
+    S.census = 0;
+    S.grid = L.spmv_grid;
+    cudaError_t e = launch_spmv(S, s);
+    if (e != cudaSuccess) return e;
+    true_residual_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L);
+    return cudaGetLastError();
+}
+
+}  // namespace evocg

@@ -1,0 +1,195 @@
+// evocg_internal.h -- structures shared by the host driver and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "evocg.h"
+
+namespace evocg {
+
+constexpr int kMaxBlocks = 2048;      // upper bound of any grid here (partials buffers)
+constexpr int kVecThreads = 256;      // threads per block of the vector kernels
+constexpr int kSpmvThreads = 256;     // threads per block of the SpMV
+constexpr int kMlpHiddenMax = 64;
+
+// Device-resident solver state; one per handle. Written by the last block of each
+// reducing kernel, read by every block of the next kernel.
+struct DevState {
+    double rho;        // r.z of the current iterate
+    double alpha, beta, sigma;
+    double nr0;        // ||r_0|| = ||b||
+    double rr;         // ||r_k||^2
+    double rtol;
+    double eps_lo, eps_hi;  // threshold rule cut points (0.1 eps, eps)
+    double tr_num, tr_den;  // true-residual check
+    int k;             // iterations done
+    int maxit;
+    int kstar;
+    int done;          // 1: the loop stops
+    int status;        // EVOCG_OK / ENOTCONV / EBREAKDOWN while running or done
+    int converged;
+    unsigned int tickets[8];
+    unsigned long long census[3];
+    unsigned long long ctrl_calls;
+};
+
+// ticket slots
+enum { TK_SPMV = 0, TK_UPDATE = 1, TK_INIT = 2, TK_TRUE = 3 };
+
+// Everything the SpMV reads from the tile structure.
+struct TilesView {
+    int64_t n, nrb, ntiles;
+    int T;
+    const int64_t *tileRowPtr;
+    const int32_t *tileColIdx;
+    const int64_t *tileNnzOff;
+    const uint16_t *rowEnd;
+    const uint8_t *colIdx;
+    const double *v64;
+    const float *v32;
+    const uint16_t *v16;
+    const int8_t *colExp;
+};
+
+struct SolveWS {
+    int64_t cap_n = 0, cap_ncb = 0;
+    int cap_hist = 0;
+    double *b = nullptr, *x = nullptr, *r = nullptr, *p = nullptr, *q = nullptr, *z = nullptr;
+    double *hist = nullptr;
+    double *partials = nullptr;       // 4 * kMaxBlocks
+    uint8_t *cbPrec = nullptr;        // controller decisions per column block
+    float *mlpW = nullptr;            // packed MLP weights on the device
+    int64_t cap_mlp = 0;
+    DevState *st = nullptr;
+    DevState *st_host = nullptr;      // pinned mirror
+    // cached graphs
+    cudaGraphExec_t exec = nullptr;
+    cudaGraph_t graph = nullptr;
+    uint64_t exec_key = 0;
+    cudaGraphExec_t exec_rs = nullptr;
+    cudaGraph_t graph_rs = nullptr;
+    uint64_t exec_rs_key = 0;
+};
+
+}  // namespace evocg
+
+struct evocg_tiles {
+    int device = 0;
+    int sms = 0;
+    int64_t n = 0, nrb = 0, ntiles = 0, nnz = 0;
+    int T = 0;
+    int64_t *tileRowPtr = nullptr;
+    int32_t *tileColIdx = nullptr;
+    int64_t *tileNnzOff = nullptr;
+    uint16_t *rowEnd = nullptr;
+    uint8_t *colIdx = nullptr;
+    double *v64 = nullptr;
+    float *v32 = nullptr;
+    uint16_t *v16 = nullptr;
+    int8_t *colExp = nullptr;
+    uint8_t *tilePrec = nullptr;   // per-tile map
+    uint8_t *cbPrec = nullptr;     // per-column-block map
+    int map_kind = EVOCG_MAP_PER_TILE;
+    double *dinv = nullptr;        // 1 / a_ii (Jacobi)
+    int diag_ok = 0;               // every diagonal entry present and > 0
+    // SpMV scratch: rounded x copies and host staging
+    float *x32 = nullptr;
+    uint16_t *x16 = nullptr;
+    double *xstage = nullptr, *ystage = nullptr;
+    int spmv_grid = 0, vec_grid = 0;
+    evocg::SolveWS ws;
+
+    evocg::TilesView view() const
+    {
+        return evocg::TilesView{n, nrb, ntiles, T, tileRowPtr, tileColIdx, tileNnzOff, rowEnd,
+                                colIdx, v64, v32, v16, colExp};
+    }
+};
+
+namespace evocg {
+
+// ---- host helpers (api.cpp) ----
+void set_error(const std::string &msg);
+int fail(int code, const std::string &msg);
+int cuda_fail(cudaError_t e, const char *what);
+
+// ---- tile builder (tile_build.cpp) ----
+struct HostTiles {
+    int64_t n = 0, nrb = 0, ntiles = 0, nnz = 0;
+    int T = 0;
+    int64_t *tileRowPtr = nullptr;
+    int32_t *tileColIdx = nullptr;
+    int64_t *tileNnzOff = nullptr;
+    uint16_t *rowEnd = nullptr;
+    uint8_t *colIdx = nullptr;
+    double *v64 = nullptr;
+    float *v32 = nullptr;
+    uint16_t *v16 = nullptr;
+    int8_t *colExp = nullptr;
+    double *dinv = nullptr;
+    int diag_ok = 0;
+    void release();
+};
+int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int T,
+                     HostTiles *out, std::string *err);
+
+// ---- kernels (spmv.cu, cg.cu, ctrl.cu) ----
+struct SpmvLaunch {
+    TilesView A;
+    const double *x64;
+    const float *x32;
+    const uint16_t *x16;
+    double *y;
+    const uint8_t *prec;   // tilePrec (map_kind 0) or cbPrec (map_kind 1); ignored if force64
+    int map_kind;
+    int force64;
+    // fused p.q for CG (dot != 0): partial sums, then the last block computes alpha
+    int dot;
+    double *partials;
+    DevState *st;
+    int census;            // accumulate per-precision entry counts into st->census
+    int grid;
+};
+cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
+cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, uint16_t *x16,
+                           int grid, cudaStream_t s);
+cudaError_t launch_round(const double *x, int64_t n, float *o32, uint16_t *o16, cudaStream_t s);
+int spmv_grid_for(int T, int sms);
+
+struct CgLaunch {
+    TilesView A;
+    int64_t n;
+    int T;
+    int jacobi;
+    int ctrl;              // EVOCG_CTRL_*
+    const double *dinv;
+    double *b, *x, *r, *p, *q, *z;
+    float *x32;
+    uint16_t *x16;
+    double *hist;
+    double *partials;
+    uint8_t *cbPrec;       // controller output (map_kind 1 for the SpMV)
+    const uint8_t *prec;   // static map
+    int map_kind;
+    const float *mlpW;
+    int H1, H2;
+    double delta;
+    DevState *st;
+    int vec_grid, spmv_grid;
+    cudaGraphConditionalHandle cond;
+};
+cudaError_t launch_cg_init(const CgLaunch &L, int restart, cudaStream_t s);
+cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s);
+cudaError_t launch_true_residual(const CgLaunch &L, cudaStream_t s);
+cudaError_t launch_ctrl_threshold(const TilesView &A, const double *p, double eps_lo,
+                                  double eps_hi, uint8_t *cbPrec, cudaStream_t s);
+cudaError_t launch_ctrl_mlp(const TilesView &A, const double *p, const float *W, int H1,
+                            int H2, double delta, uint8_t *cbPrec, float *logits,
+                            const DevState *gate, cudaStream_t s);
+cudaError_t launch_broadcast_map(const TilesView &A, const uint8_t *cbPrec, uint8_t *tilePrec,
+                                 cudaStream_t s);
+
+}  // namespace evocg

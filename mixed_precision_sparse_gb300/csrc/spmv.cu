@@ -1,0 +1,274 @@
+// spmv.cu -- the tile-wise mixed-precision SpMV (EvoCG, "Self-Evolving Precision Control
+// for Faster Conjugate Gradient", §3.3 EvoSpMV, Eq. 2 / Eq. 5) for sm_103a.
+//
+// Work mapping. A warp owns a row block (T rows) at a time and walks its tiles in
+// ascending column block, so every row is summed in column order. Lane l owns local row
+// l (T = 32), rows l and l+32 (T = 64), or, for T = 16, the two half-warps take
+// alternate tiles of the row block and are merged at the end. Each lane keeps its rows'
+// sums in registers for the whole row block: no cross-lane reduction at all.
+//
+// Arithmetic. An FP64 tile costs exactly one FP64 fused multiply-add per entry, the
+// floor for FP64 data. FP32 and BF16 tiles never touch the FP64 unit: their products
+// are exact in an FP32 pair (BF16 x BF16 fits in FP32; FP32 x FP32 is split by one
+// fused multiply-add), summed error-free (TwoSum) into an FP32 hi/lo pair, and merged
+// into the FP64 row sum once per row: about 48 bits of the sum are kept, so a
+// low-precision tile contributes its exactly rounded-operand products, as the paper's
+// model asks, and the row sum stays an FP64 sum. GB300 issues FP64 at about 1/58 of
+// the FP32 rate, so this split is what lets low-precision tiles run at memory speed.
+//
+// Operands. The x entries a low-precision tile reads are the FP32 / BF16 roundings of x
+// scaled by the column factor 2^e_j, made once per SpMV (xcopies_kernel, or the CG
+// p-update) with integer instructions.
+#include <cuda_runtime.h>
+
+#include "evocg_internal.h"
+#include "fpconv.cuh"
+
+namespace evocg {
+
+template <int T>
+struct Geo {
+    static constexpr int G = T < 32 ? T : 32;  // lanes per row group
+    static constexpr int NG = 32 / G;          // row groups per warp
+    static constexpr int RPL = T / G;          // rows per lane
+};
+
+// Last block of a grid: sums per-block partials in a fixed order (deterministic) and
+// returns true in every thread of that block. `slot` selects the ticket counter.
+__device__ __forceinline__ bool last_block(DevState *st, int slot)
+{
+    __shared__ bool amLast;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned t = atomicAdd(&st->tickets[slot], 1u);
+        amLast = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (amLast) __threadfence();
+    return amLast;
+}
+
+// Deterministic block sum of one double per thread (fixed shuffle tree, fixed order).
+__device__ __forceinline__ double block_sum(double v)
+{
+    __shared__ double ws[32];
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) ws[w] = v;
+    __syncthreads();
+    double s = 0.0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += ws[i];
+    return s;  // valid in thread 0
+}
+
+template <int T, bool FORCE64, bool DOT>
+__global__ void __launch_bounds__(kSpmvThreads) spmv_kernel(SpmvLaunch L)
+{
+    using Gm = Geo<T>;
+    const TilesView A = L.A;
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / Gm::G;
+    const int gl = lane % Gm::G;
+    const int64_t wpb = blockDim.x >> 5;
+    const int64_t nwarps = (int64_t)gridDim.x * wpb;
+    const int64_t wid = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    double dotp = 0.0;
+    unsigned long long cnt0 = 0, cnt1 = 0, cnt2 = 0;
+
+    for (int64_t rb = wid; rb < A.nrb; rb += nwarps) {
+        const int64_t t0 = A.tileRowPtr[rb], t1 = A.tileRowPtr[rb + 1];
+        double acc64[Gm::RPL];
+        F32Pair accl[Gm::RPL];
+#pragma unroll
+        for (int rr = 0; rr < Gm::RPL; ++rr) acc64[rr] = 0.0;
+        bool any64 = false, anylow = false;
+        for (int64_t t = t0 + grp; t < t1; t += Gm::NG) {
+            const int64_t cb = A.tileColIdx[t];
+            const int64_t off = A.tileNnzOff[t];
+            const int prec = FORCE64 ? 0 : (int)__ldg(L.prec + (L.map_kind ? cb : t));
+            const uint8_t *ci = A.colIdx + off;
+            const int64_t xb = cb * T;
+            const uint16_t *re = A.rowEnd + t * T;
+#pragma unroll
+            for (int rr = 0; rr < Gm::RPL; ++rr) {
+                const int r = gl + rr * Gm::G;
+                const int end = __ldg(re + r);
+                const int start = r ? (int)__ldg(re + r - 1) : 0;
+                if (prec == EVOCG_FP64) {
+                    const double *vv = A.v64 + off;
+                    const double *xs = L.x64 + xb;
+                    double a = acc64[rr];
+#pragma unroll 4
+                    for (int k = start; k < end; ++k)
+                        a = fma(__ldg(vv + k), __ldg(xs + __ldg(ci + k)), a);
+                    acc64[rr] = a;
+                } else if (prec == EVOCG_FP32) {
+                    const float *vv = A.v32 + off;
+                    const float *xs = L.x32 + xb;
+#pragma unroll 4
+                    for (int k = start; k < end; ++k)
+                        accl[rr].add_prod(__ldg(vv + k), __ldg(xs + __ldg(ci + k)));
+                } else {
+                    const uint16_t *vv = A.v16 + off;
+                    const uint16_t *xs = L.x16 + xb;
+#pragma unroll 4
+                    for (int k = start; k < end; ++k)  // BF16 x BF16 is exact in FP32
+                        accl[rr].add(__fmul_rn(f32_from_bf16(__ldg(vv + k)),
+                                               f32_from_bf16(__ldg(xs + __ldg(ci + k)))));
+                }
+            }
+            any64 |= (prec == EVOCG_FP64);
+            anylow |= (prec != EVOCG_FP64);
+            if (L.census && gl == 0) {
+                const unsigned long long c = __ldg(re + T - 1);
+                if (prec == 0) cnt0 += c; else if (prec == 1) cnt1 += c; else cnt2 += c;
+            }
+        }
+        if (Gm::NG == 2) {  // T = 16: fold the odd-tile half-warp into the even one
+#pragma unroll
+            for (int rr = 0; rr < Gm::RPL; ++rr) {
+                acc64[rr] += __shfl_down_sync(0xffffffffu, acc64[rr], 16);
+                F32Pair o;
+                o.hi = __shfl_down_sync(0xffffffffu, accl[rr].hi, 16);
+                o.lo = __shfl_down_sync(0xffffffffu, accl[rr].lo, 16);
+                accl[rr].merge(o);
+            }
+        }
+        any64 = __any_sync(0xffffffffu, any64);
+        anylow = __any_sync(0xffffffffu, anylow);
+        if (grp == 0) {
+#pragma unroll
+            for (int rr = 0; rr < Gm::RPL; ++rr) {
+                const int64_t row = rb * T + gl + rr * Gm::G;
+                if (row < A.n) {
+                    double y = acc64[rr];
+                    if (anylow) {
+                        const double d = f64_from_f32(accl[rr].hi) + f64_from_f32(accl[rr].lo);
+                        y = any64 ? y + d : d;
+                    }
+                    L.y[row] = y;
+                    if (DOT) dotp = fma(__ldg(L.x64 + row), y, dotp);
+                }
+            }
+        }
+    }
+    if (L.census) {
+        for (int o = 16; o; o >>= 1) {
+            cnt0 += __shfl_xor_sync(0xffffffffu, cnt0, o);
+            cnt1 += __shfl_xor_sync(0xffffffffu, cnt1, o);
+            cnt2 += __shfl_xor_sync(0xffffffffu, cnt2, o);
+        }
+        if (lane == 0) {
+            if (cnt0) atomicAdd(&L.st->census[0], cnt0);
+            if (cnt1) atomicAdd(&L.st->census[1], cnt1);
+            if (cnt2) atomicAdd(&L.st->census[2], cnt2);
+        }
+    }
+    if (DOT) {
+        DevState *st = L.st;
+        const double s = block_sum(dotp);
+        if (threadIdx.x == 0) L.partials[blockIdx.x] = s;
+        if (last_block(st, TK_SPMV)) {
+            double v = 0.0;
+            for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) v += __ldcg(L.partials + i);
+            const double sigma = block_sum(v);
+            if (threadIdx.x == 0) {
+                st->tickets[TK_SPMV] = 0;
+                if (!st->done) {
+                    if (!(sigma > 0.0) || !isfinite(sigma)) {
+                        st->status = EVOCG_EBREAKDOWN;
+                        st->done = 1;
+                    } else {
+                        st->sigma = sigma;
+                        st->alpha = st->rho / sigma;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// x copies for the low-precision tiles: x32_j = RN32(x_j) 2^e_j, x16_j = RN16(x_j) 2^e_j.
+__global__ void __launch_bounds__(kVecThreads)
+    xcopies_kernel(int64_t n, const double *__restrict__ x, const int8_t *__restrict__ colExp,
+                   float *__restrict__ x32, uint16_t *__restrict__ x16)
+{
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const double v = x[j];
+        const float s = pow2f(colExp[j]);
+        x32[j] = __fmul_rn(f32_from_f64_rn(v), s);
+        x16[j] = (uint16_t)(__float_as_uint(__fmul_rn(f32_from_bf16(bf16_from_f64_rn(v)), s)) >> 16);
+    }
+}
+
+__global__ void __launch_bounds__(kVecThreads)
+    round_kernel(int64_t n, const double *__restrict__ x, float *o32, uint16_t *o16)
+{
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
+         j += (int64_t)gridDim.x * blockDim.x) {
+        const double v = x[j];
+        if (o32) o32[j] = f32_from_f64_rn(v);
+        if (o16) o16[j] = bf16_from_f64_rn(v);
+    }
+}
+
+template <int T>
+static cudaError_t launch_T(const SpmvLaunch &L, cudaStream_t s)
+{
+    const int grid = L.grid;
+    if (L.force64) {
+        if (L.dot) spmv_kernel<T, true, true><<<grid, kSpmvThreads, 0, s>>>(L);
+        else spmv_kernel<T, true, false><<<grid, kSpmvThreads, 0, s>>>(L);
+    } else {
+        if (L.dot) spmv_kernel<T, false, true><<<grid, kSpmvThreads, 0, s>>>(L);
+        else spmv_kernel<T, false, false><<<grid, kSpmvThreads, 0, s>>>(L);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
+{
+    switch (L.A.T) {
+    case 16: return launch_T<16>(L, s);
+    case 32: return launch_T<32>(L, s);
+    case 64: return launch_T<64>(L, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int spmv_grid_for(int T, int sms)
+{
+    int per = 0;
+    cudaError_t e;
+    switch (T) {
+    case 16: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_kernel<16, false, true>, kSpmvThreads, 0); break;
+    case 64: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_kernel<64, false, true>, kSpmvThreads, 0); break;
+    default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_kernel<32, false, true>, kSpmvThreads, 0); break;
+    }
+    if (e != cudaSuccess || per < 1) per = 2;
+    int g = sms * per;
+    return g > kMaxBlocks ? kMaxBlocks : g;
+}
+
+cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, uint16_t *x16,
+                           int grid, cudaStream_t s)
+{
+    if (A.n == 0) return cudaSuccess;
+    xcopies_kernel<<<grid, kVecThreads, 0, s>>>(A.n, x, A.colExp, x32, x16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_round(const double *x, int64_t n, float *o32, uint16_t *o16, cudaStream_t s)
+{
+    if (n == 0) return cudaSuccess;
+    int64_t g = (n + kVecThreads - 1) / kVecThreads;
+    if (g > 4096) g = 4096;
+    round_kernel<<<(int)g, kVecThreads, 0, s>>>(n, x, o32, o16);
+    return cudaGetLastError();
+}
+
+}  // namespace evocg

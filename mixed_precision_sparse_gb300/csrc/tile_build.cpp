@@ -1,0 +1,199 @@
+// tile_build.cpp -- host construction of the tile structure, multi-threaded over row
+// blocks.
+//
+// Layout (EvoCG, "Self-Evolving Precision Control for Faster Conjugate Gradient",
+// §3.3.1 Fig. 4(a) and §3.3.2): CSR over row blocks of nonempty T x T tiles; inside a
+// tile the entries row by row in ascending column, with the end offset of every local
+// row (rowEnd) and one local column byte per entry (colIdx); three value streams over the
+// same entries (FP64 a_ij; FP32 and BF16 of a_ij / 2^e_j with the per-column exponent
+// e_j = floor(log2 max_i |a_ij|) clamped to [-100, 100]).
+//
+// Row-major order inside the tile (the paper stores the tile column-major) lets the SpMV
+// give each row to one lane and accumulate it in registers: no cross-lane FP64
+// reduction, which GB300's FP64 rate would make the bottleneck.
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "evocg_internal.h"
+#include "fpconv.cuh"
+
+namespace evocg {
+
+void HostTiles::release()
+{
+    delete[] tileRowPtr; delete[] tileColIdx; delete[] tileNnzOff; delete[] rowEnd;
+    delete[] colIdx; delete[] v64; delete[] v32; delete[] v16; delete[] colExp; delete[] dinv;
+    tileRowPtr = nullptr; tileColIdx = nullptr; tileNnzOff = nullptr; rowEnd = nullptr;
+    colIdx = nullptr; v64 = nullptr; v32 = nullptr; v16 = nullptr; colExp = nullptr;
+    dinv = nullptr;
+}
+
+namespace {
+
+template <class F>
+void parallel_for(int64_t count, F &&fn)
+{
+    unsigned hw = std::thread::hardware_concurrency();
+    int64_t nt = std::max<int64_t>(1, std::min<int64_t>(hw ? hw : 4, 64));
+    nt = std::min<int64_t>(nt, std::max<int64_t>(1, count / 256));
+    if (nt <= 1) { fn(0, count); return; }
+    std::vector<std::thread> th;
+    th.reserve((size_t)nt);
+    for (int64_t t = 0; t < nt; ++t) {
+        int64_t a = count * t / nt, b = count * (t + 1) / nt;
+        th.emplace_back([&fn, a, b] { fn(a, b); });
+    }
+    for (auto &x : th) x.join();
+}
+
+// floor(log2 |v|) for a finite nonzero v
+int ilog2_abs(double v)
+{
+    uint64_t u;
+    std::memcpy(&u, &v, 8);
+    int ef = (int)((u >> 52) & 0x7FF);
+    if (ef != 0) return ef - 1023;
+    int e2;
+    std::frexp(v, &e2);  // FP64 subnormal
+    return e2 - 1;
+}
+
+}  // namespace
+
+int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int T,
+                     HostTiles *out, std::string *err)
+{
+    if (n < 0 || n >= (int64_t)INT32_MAX) { *err = "n out of range"; return EVOCG_EINVAL; }
+    if (T != 16 && T != 32 && T != 64) { *err = "tile_size must be 16, 32 or 64"; return EVOCG_EINVAL; }
+    if (!rp || (n > 0 && (!ci || !v)) || rp[0] != 0) { *err = "bad CSR pointers"; return EVOCG_EINVAL; }
+    const int64_t nnz = rp[n];
+    // --- validate rows
+    std::atomic<int64_t> bad_row{-1};
+    parallel_for(n, [&](int64_t a, int64_t b) {
+        for (int64_t i = a; i < b; ++i) {
+            if (rp[i + 1] < rp[i] || rp[i + 1] > nnz) { bad_row = i; return; }
+            for (int64_t k = rp[i]; k < rp[i + 1]; ++k) {
+                if (ci[k] < 0 || ci[k] >= n || (k > rp[i] && ci[k] <= ci[k - 1]) ||
+                    !std::isfinite(v[k])) { bad_row = i; return; }
+            }
+        }
+    });
+    if (bad_row.load() >= 0) {
+        *err = "invalid CSR at row " + std::to_string(bad_row.load()) +
+               " (row pointers must be monotone, columns in [0,n) strictly ascending, values finite)";
+        return EVOCG_EINVAL;
+    }
+    HostTiles H;
+    H.n = n; H.T = T; H.nnz = nnz; H.nrb = (n + T - 1) / T;
+    const int64_t nrb = H.nrb;
+    try {
+        // --- per-column exponent (max over the column of floor(log2 |a_ij|))
+        std::vector<std::atomic<int>> emax((size_t)std::max<int64_t>(n, 1));
+        for (auto &e : emax) e.store(INT_MIN, std::memory_order_relaxed);
+        parallel_for(n, [&](int64_t a, int64_t b) {
+            for (int64_t i = a; i < b; ++i)
+                for (int64_t k = rp[i]; k < rp[i + 1]; ++k) {
+                    if (v[k] == 0.0) continue;
+                    int e = ilog2_abs(v[k]);
+                    std::atomic<int> &slot = emax[(size_t)ci[k]];
+                    int cur = slot.load(std::memory_order_relaxed);
+                    while (e > cur && !slot.compare_exchange_weak(cur, e, std::memory_order_relaxed)) {}
+                }
+        });
+        H.colExp = new int8_t[(size_t)std::max<int64_t>(n, 1)];
+        for (int64_t j = 0; j < n; ++j) {
+            int e = emax[(size_t)j].load(std::memory_order_relaxed);
+            e = (e == INT_MIN) ? 0 : std::min(100, std::max(-100, e));
+            H.colExp[j] = (int8_t)e;
+        }
+        // --- diagonal
+        H.dinv = new double[(size_t)std::max<int64_t>(n, 1)];
+        std::atomic<int> diag_bad{0};
+        parallel_for(n, [&](int64_t a, int64_t b) {
+            for (int64_t i = a; i < b; ++i) {
+                const int32_t *lo = ci + rp[i], *hi = ci + rp[i + 1];
+                const int32_t *f = std::lower_bound(lo, hi, (int32_t)i);
+                double d = (f != hi && *f == i) ? v[rp[i] + (f - lo)] : 0.0;
+                if (!(d > 0.0)) { diag_bad = 1; H.dinv[i] = 0.0; }
+                else H.dinv[i] = 1.0 / d;
+            }
+        });
+        H.diag_ok = diag_bad.load() ? 0 : 1;
+        // --- pass 1: tiles per row block (distinct column blocks of its entries)
+        std::vector<int64_t> ntile_rb((size_t)nrb + 1, 0);
+        parallel_for(nrb, [&](int64_t a, int64_t b) {
+            std::vector<int32_t> cbs;
+            for (int64_t rb = a; rb < b; ++rb) {
+                int64_t r0 = rb * T, r1 = std::min<int64_t>(n, r0 + T);
+                cbs.clear();
+                for (int64_t k = rp[r0]; k < rp[r1]; ++k) cbs.push_back(ci[k] / T);
+                std::sort(cbs.begin(), cbs.end());
+                ntile_rb[(size_t)rb] = (int64_t)(std::unique(cbs.begin(), cbs.end()) - cbs.begin());
+            }
+        });
+        H.tileRowPtr = new int64_t[(size_t)nrb + 1];
+        H.tileRowPtr[0] = 0;
+        for (int64_t rb = 0; rb < nrb; ++rb) H.tileRowPtr[rb + 1] = H.tileRowPtr[rb] + ntile_rb[(size_t)rb];
+        H.ntiles = H.tileRowPtr[nrb];
+        const int64_t nt = H.ntiles;
+        H.tileColIdx = new int32_t[(size_t)std::max<int64_t>(nt, 1)];
+        H.tileNnzOff = new int64_t[(size_t)nt + 1];
+        H.rowEnd = new uint16_t[(size_t)std::max<int64_t>(nt * T, 1)];
+        H.colIdx = new uint8_t[(size_t)std::max<int64_t>(nnz, 1)];
+        H.v64 = new double[(size_t)std::max<int64_t>(nnz, 1)];
+        H.v32 = new float[(size_t)std::max<int64_t>(nnz, 1)];
+        H.v16 = new uint16_t[(size_t)std::max<int64_t>(nnz, 1)];
+        H.tileNnzOff[nt] = nnz;
+        // --- pass 2: fill. The entries of row block rb occupy [rp[r0], rp[r1]) in the
+        // streams too (tiles only reorder them inside the row block).
+        parallel_for(nrb, [&](int64_t a, int64_t b) {
+            std::vector<int64_t> cur((size_t)T);
+            for (int64_t rb = a; rb < b; ++rb) {
+                const int64_t r0 = rb * T, r1 = std::min<int64_t>(n, r0 + T);
+                const int nr = (int)(r1 - r0);
+                for (int r = 0; r < nr; ++r) cur[(size_t)r] = rp[r0 + r];
+                int64_t pos = rp[r0];
+                for (int64_t t = H.tileRowPtr[rb]; t < H.tileRowPtr[rb + 1]; ++t) {
+                    int32_t cb = INT32_MAX;  // smallest column block left in the row block
+                    for (int r = 0; r < nr; ++r)
+                        if (cur[(size_t)r] < rp[r0 + r + 1]) cb = std::min(cb, ci[cur[(size_t)r]] / T);
+                    H.tileColIdx[t] = cb;
+                    H.tileNnzOff[t] = pos;
+                    const int64_t base = pos;
+                    for (int r = 0; r < T; ++r) {
+                        if (r < nr) {
+                            int64_t k = cur[(size_t)r];
+                            const int64_t kend = rp[r0 + r + 1];
+                            for (; k < kend && ci[k] / T == cb; ++k, ++pos) {
+                                const int32_t j = ci[k];
+                                const double s = std::ldexp(v[k], -(int)H.colExp[j]);
+                                uint64_t sb;
+                                std::memcpy(&sb, &s, 8);
+                                H.colIdx[pos] = (uint8_t)(j - cb * T);
+                                H.v64[pos] = v[k];
+                                uint32_t b32 = rne_bits_from_f64<23>(sb);
+                                std::memcpy(&H.v32[pos], &b32, 4);
+                                H.v16[pos] = (uint16_t)rne_bits_from_f64<7>(sb);
+                            }
+                            cur[(size_t)r] = k;
+                        }
+                        H.rowEnd[t * T + r] = (uint16_t)(pos - base);
+                    }
+                }
+            }
+        });
+    } catch (const std::bad_alloc &) {
+        H.release();
+        *err = "host allocation failed while building tiles";
+        return EVOCG_ENOMEM;
+    }
+    *out = H;
+    return EVOCG_OK;
+}
+
+}  // namespace evocg

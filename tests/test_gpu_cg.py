@@ -1,0 +1,177 @@
+"""GPU parity of the CG / Jacobi-PCG solve and the controllers through the C ABI."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import Pair
+from mixed_precision_sparse_gb300 import evocg
+from mixed_precision_sparse_gb300 import workloads as W
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _solve(P, b, rtol, maxit, jacobi=False, ctrl=None, finish=False, dev=True):
+    if dev:
+        bd = torch.from_numpy(np.ascontiguousarray(b)).cuda()
+        xd = torch.empty(P.n, dtype=torch.float64, device="cuda")
+        hd = torch.zeros(maxit + 1, dtype=torch.float64, device="cuda")
+        info = evocg.cg_solve(P.G, bd, xd, rtol, maxit, jacobi, ctrl, finish, hd)
+        torch.cuda.synchronize()
+        return info, xd.cpu().numpy(), hd.cpu().numpy()[: info["iters"] + 1]
+    x = np.empty(P.n)
+    h = np.zeros(maxit + 1)
+    info = evocg.cg_solve(P.G, b, x, rtol, maxit, jacobi, ctrl, finish, h)
+    return info, x, h[: info["iters"] + 1]
+
+
+def _within(a, b, frac=0.03, slack=2):
+    return abs(a - b) <= max(slack, frac * b)
+
+
+def test_cg_fp64_matches_oracle_laplacian():
+    w = W.workload(1)
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    evocg.set_tile_precision(P.G, np.zeros(P.t.ntiles, np.uint8))
+    ref = oracle.cg(P.A, P.t, w.b, w.rtol, w.maxit)
+    info, x, h = _solve(P, w.b, w.rtol, w.maxit)
+    assert info["status"] == evocg.OK and ref["status"] == oracle.OK
+    assert abs(info["iters"] - ref["iters"]) <= 1
+    k = min(len(h), len(ref["hist"])) - 1
+    assert np.allclose(h[: min(k, 60)], ref["hist"][: min(k, 60)], rtol=1e-8, atol=0)
+    assert oracle.true_residual(P.A, w.b, x) <= 10 * w.rtol
+    assert np.linalg.norm(x - ref["x"]) <= 1e-8 * np.linalg.norm(ref["x"])
+
+
+def test_cg_mixed_static_map_laplacian():
+    w = W.workload(1)
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    mp = P.tile_map(w.map_seed)
+    evocg.set_tile_precision(P.G, mp)
+    ref = oracle.cg(P.A, P.t, w.b, w.rtol, w.maxit, tile_map=mp, finish_fp64=True)
+    info, x, h = _solve(P, w.b, w.rtol, w.maxit, finish=True)
+    assert info["status"] == evocg.OK and ref["status"] == oracle.OK
+    assert _within(info["iters_recursive"], ref["iters_rec"])
+    assert _within(info["iters"], ref["iters"])
+    assert oracle.true_residual(P.A, w.b, x) <= w.rtol
+    assert abs(info["true_res"] - oracle.true_residual(P.A, w.b, x)) <= 1e-3 * w.rtol
+    # precision census: every SpMV of the first pass reads the static map
+    per = np.bincount(mp, weights=np.diff(P.t.tileNnzOff), minlength=3).astype(np.int64)
+    rec = info["iters_recursive"]
+    rest = info["iters"] - rec
+    want = per * rec + np.array([P.t.nnz * rest, 0, 0])
+    assert list(info["prec_nnz"]) == list(want)
+
+
+@pytest.mark.parametrize("dev", [True, False])
+def test_pcg_threshold_controller_small_diffusion(dev):
+    w = W.workload(2, scale=0.25)  # 32^3, same coefficient law and settings
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    ref = oracle.cg(P.A, P.t, w.b, w.rtol, w.maxit, jacobi=True, ctrl="threshold", eps=w.eps,
+                    finish_fp64=True)
+    ctrl = evocg.Ctrl.threshold(w.eps)
+    info, x, h = _solve(P, w.b, w.rtol, w.maxit, True, ctrl, True, dev=dev)
+    assert info["status"] == evocg.OK and ref["status"] == oracle.OK
+    assert _within(info["iters"], ref["iters"])
+    assert info["ctrl_calls"] >= info["iters_recursive"]
+    assert oracle.true_residual(P.A, w.b, x) <= w.rtol
+    n0 = min(30, len(h), len(ref["hist"]))
+    assert np.allclose(h[:n0], ref["hist"][:n0], rtol=1e-6)
+    # the controller really switched precision near convergence
+    assert info["prec_nnz"][1] + info["prec_nnz"][2] > 0 or ref["prec_nnz"][1] + ref["prec_nnz"][2] == 0
+
+
+def test_pcg_mlp_controller_small_fe():
+    w = W.workload(3, scale=0.25)  # 24^3 interior nodes, D A D scaling, seeded policy
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    wts = W.mlp_weights(w.T, w.mlp_seed)
+    ref = oracle.cg(P.A, P.t, w.b, w.rtol, w.maxit, jacobi=True, ctrl="mlp", weights=wts,
+                    delta=w.delta, finish_fp64=True)
+    info, x, h = _solve(P, w.b, w.rtol, w.maxit, True, evocg.Ctrl.mlp(wts, 1, w.delta), True)
+    assert info["status"] == evocg.OK and ref["status"] == oracle.OK
+    assert _within(info["iters_recursive"], ref["iters_rec"], 0.05)
+    assert oracle.true_residual(P.A, w.b, x) <= w.rtol
+    assert info["ctrl_calls"] >= info["iters_recursive"]
+
+
+def test_threshold_decisions_match_oracle():
+    w = W.workload(2, scale=0.25)
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    for seed in range(3):
+        p = W.p_snapshot(P.n, w.T, seed, -12, 0)
+        want = oracle.ctrl_threshold(p, w.T, w.eps)
+        got = np.empty(P.t.nrb, np.uint8)
+        evocg.ctrl_decide(P.G, evocg.Ctrl.threshold(w.eps), p, got)
+        assert np.array_equal(got, want)
+        assert len(set(want.tolist())) == 3  # all three codes exercised
+
+
+@pytest.mark.parametrize("T", [16, 32, 64])
+def test_mlp_decisions_match_oracle(T):
+    n = T * 700 + 5                            # a ragged last segment
+    n2, rp, ci, v = W.laplace2d_5pt(n, 1)     # a 1 x n grid: n unknowns, tridiagonal
+    P = Pair((n2, rp, ci, v), T)
+    wts = W.mlp_weights(T, 10 + T)
+    for seed in range(2):
+        p = W.p_snapshot(n2, T, seed, -40, 5)
+        p[:T] = 0.0                              # a zero segment
+        p[T:2 * T] *= 1e-35                      # a segment below delta
+        want, lg = oracle.ctrl_mlp(p, T, wts, 1e-30)
+        got = np.empty(P.t.nrb, np.uint8)
+        glog = np.empty(3 * P.t.nrb, np.float32)
+        evocg.ctrl_decide(P.G, evocg.Ctrl.mlp(wts, 1, 1e-30), p, got, glog)
+        glog = glog.reshape(-1, 3)
+        srt = np.sort(lg, axis=1)
+        margin = srt[:, 2] - srt[:, 1]
+        clear = margin > 1e-4 * (1 + np.abs(srt[:, 2]))
+        assert np.array_equal(got[clear], want[clear])
+        assert np.allclose(glog, lg, atol=1e-4 * (1 + np.abs(lg).max()))
+        assert clear.mean() > 0.95
+
+
+def test_status_codes_and_edge_cases():
+    P = Pair(W.dense_to_csr(np.diag([1.0, -1.0, 2.0])), 16)
+    info, _, _ = _solve(P, np.array([0.0, 1.0, 0.0]), 1e-10, 10)
+    assert info["status"] == evocg.EBREAKDOWN
+    P = Pair(W.laplace2d_5pt(20), 16)
+    info, _, h = _solve(P, np.ones(P.n), 1e-12, 5)
+    assert info["status"] == evocg.ENOTCONV and info["iters"] == 5 and len(h) == 6
+    info, x, h = _solve(P, np.zeros(P.n), 1e-12, 5)
+    assert info["status"] == evocg.OK and info["iters"] == 0 and np.all(x == 0)
+    info, x, h = _solve(P, np.ones(P.n), 1e-12, 0)
+    assert info["status"] == evocg.ENOTCONV and info["iters"] == 0
+    Pz = Pair(W.dense_to_csr(np.array([[0.0, 1.0], [1.0, 2.0]])), 16)
+    with pytest.raises(evocg.EvocgError) as e:
+        _solve(Pz, np.ones(2), 1e-10, 10, jacobi=True)
+    assert e.value.code == evocg.EINVAL
+
+
+def test_solve_is_deterministic_and_graph_reuse():
+    w = W.workload(5, scale=0.05)
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    evocg.set_tile_precision(P.G, P.tile_map(5))
+    a = _solve(P, w.b, 1e-8, 400, jacobi=True)
+    b = _solve(P, w.b, 1e-8, 400, jacobi=True)
+    assert a[0]["iters"] == b[0]["iters"]
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    ref = oracle.cg(P.A, P.t, w.b, 1e-8, 400, jacobi=True, tile_map=P.tile_map(5))
+    assert _within(a[0]["iters"], ref["iters"])
+
+
+@pytest.mark.parametrize("cfg,iters", [(2, 20), (5, 10)])
+def test_cg_history_full_size_first_iterations(cfg, iters):
+    """Full-size workloads: the first iterations of the GPU solve against the oracle's
+    (the oracle cannot run the whole solve at this size in seconds)."""
+    w = W.workload(cfg)
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    if w.ctrl == "static":
+        mp = P.tile_map(w.map_seed)
+        evocg.set_tile_precision(P.G, mp)
+        ref = oracle.cg(P.A, P.t, w.b, 0.0, iters, jacobi=w.jacobi, tile_map=mp)
+        info, x, h = _solve(P, w.b, 0.0, iters, w.jacobi)
+    else:
+        ref = oracle.cg(P.A, P.t, w.b, 0.0, iters, jacobi=w.jacobi, ctrl="threshold", eps=w.eps)
+        info, x, h = _solve(P, w.b, 0.0, iters, w.jacobi, evocg.Ctrl.threshold(w.eps))
+    assert info["iters"] == ref["iters"] == iters
+    assert np.allclose(h, ref["hist"], rtol=1e-8)
+    assert np.linalg.norm(x - ref["x"]) <= 1e-8 * np.linalg.norm(ref["x"])
