@@ -1,0 +1,383 @@
+"""Benchmark: CG time-to-solution of the tile-wise mixed-precision solver on one GB300.
+
+Workload (default): 3D 7-point variable-coefficient diffusion on a 128^3 grid (n = 2,097,152,
+nnz = 14,581,760), face coefficients 10^U[-2,2], b ~ U[-1,1], 32 x 32 tiles, Jacobi-PCG,
+rtol 1e-8, in-loop threshold controller (eps = rtol), FP64 finish. A step is one full solve
+(every stage of the hot path: controller, mixed SpMV with fused p.q, fused updates, the
+graph-driven loop and the FP64 true-residual check), inputs resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs N independent replicas (one solve per rank per step, weak scaling); launch it
+with torch.distributed.run. `--impl reference` times the CPU oracle on the host cores on a
+bounded sample of the same workload and prints the same JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CG time-to-solution (s) and mixed-precision SpMV HBM GB/s vs GB300 peak"
+REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+           0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+           0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+           0x100: "display_clock_setting"}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock and throttle reasons, sampled every 200 ms in the background."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 3:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+                bits = int(parts[2], 16)
+            except ValueError:
+                continue
+            for b, name in REASONS.items():
+                if bits & b:
+                    reasons.add(name)
+        reasons.discard("gpu_idle")
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _workload(cfg):
+    from mixed_precision_sparse_gb300 import workloads as W
+    return W.workload(cfg)
+
+
+def _spmv_bytes(desc_n, ntiles, nrb, T, nnz_by_prec):
+    """Algorithmic bytes of one SpMV launch: the active value stream of every tile, one
+    local-column byte per entry, the tile's row ends (2T) and descriptor (column block 4,
+    entry offset 8, precision code 1), the row-block pointers, x read once, y written once."""
+    vals = 8 * nnz_by_prec[0] + 4 * nnz_by_prec[1] + 2 * nnz_by_prec[2]
+    nnz = sum(nnz_by_prec)
+    return vals + nnz + ntiles * (2 * T + 13) + 8 * (nrb + 1) + 16 * desc_n
+
+
+def _traffic_for(kernel_src_hash):
+    """Per-launch DRAM bytes of the SpMV from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "spmv_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_src_sha256") != kernel_src_hash:
+        return None
+    return d.get("bytes_per_launch_full_size")
+
+
+def _src_hash():
+    h = hashlib.sha256()
+    for name in ("spmv.cu", "fpconv.cuh", "evocg_internal.h"):
+        with open(os.path.join(ROOT, "mixed_precision_sparse_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------------------
+
+def _oracle_iterations(cfg):
+    p = os.path.join(ROOT, "tests", "golden", "oracle_iterations.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        v = d.get(str(cfg))
+        if v:
+            return int(v["iters"])
+    return None
+
+
+def oracle_sample(w, sample_iters):
+    """Time `sample_iters` iterations of the oracle's solve of workload w (single thread).
+    Returns seconds per iteration."""
+    import oracle
+    A = oracle.CSR(w.n, w.rp, w.ci, w.v)
+    t = oracle.Tiles(A, w.T)
+    kw = dict(jacobi=w.jacobi)
+    if w.ctrl == "threshold":
+        kw.update(ctrl="threshold", eps=w.eps)
+    t0 = time.perf_counter()
+    r = oracle.cg(A, t, w.b, 0.0, sample_iters, **kw)
+    el = time.perf_counter() - t0
+    return el / max(1, r["iters"]), r
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    w = _workload(args.workload)
+    iters_full = _oracle_iterations(args.workload)
+    sample = args.cpu_sample_iters
+    times = []
+    for _ in range(args.warmup):
+        oracle_sample(w, 1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sec_it, _ = oracle_sample(w, sample)
+        times.append(sec_it)
+    wall = time.perf_counter() - t0
+    sec_it = statistics.median(times)
+    value = sec_it * iters_full if iters_full else None
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * wall / max(1, args.steps), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "n": w.n, "nnz": w.nnz, "tile": w.T,
+                   "solver": "jacobi-pcg" if w.jacobi else "cg", "rtol": w.rtol,
+                   "controller": w.ctrl, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "s", "cores": 1, "kind": "oracle",
+                         "sample": f"{sample} iterations per step, seconds/iteration x "
+                                   f"{iters_full} iterations of the oracle's full solve"},
+        "e2e": {"value": value, "unit": "s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from mixed_precision_sparse_gb300 import evocg
+    from mixed_precision_sparse_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    w = _workload(args.workload)
+    t0 = time.perf_counter()
+    G = evocg.tile_build(w.n, w.rp, w.ci, w.v, w.T)
+    build_s = time.perf_counter() - t0
+    if w.ctrl == "threshold":
+        ctrl = evocg.Ctrl.threshold(w.eps, w.kstar)
+    elif w.ctrl == "mlp":
+        ctrl = evocg.Ctrl.mlp(W.mlp_weights(w.T, w.mlp_seed), w.kstar, w.delta)
+    else:
+        ctrl = None
+        trow, ex = G.tile_rows()
+        evocg.set_tile_precision(G, W.tile_map(trow, ex["tileColIdx"], G.nrb, w.map_seed))
+    b = torch.from_numpy(w.b).to(dev)
+    x = torch.empty_like(b)
+    hist = torch.empty(w.maxit + 1, dtype=torch.float64, device=dev)
+
+    def solve():
+        return evocg.cg_solve(G, b, x, w.rtol, w.maxit, w.jacobi, ctrl, True, hist)
+
+    for _ in range(max(3, args.warmup)):
+        info = solve()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    infos = []
+    with ClockSampler(local) as clk:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            infos.append(solve())
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    info = infos[-1]
+    value = ms / 1000.0 / world      # seconds per solve for the whole job
+    launches = 0
+    for inf in infos:
+        # init + 3 kernels per iteration (+1 policy kernel per iteration with the MLP),
+        # true-residual check 2 per check, each restart graph: SpMV + init
+        per_it = 3 + (1 if w.ctrl == "mlp" else 0)
+        launches += 1 + per_it * inf["iters"] + 2 * (1 + inf["restarts"]) + 2 * inf["restarts"]
+
+    # ---- end to end through the C ABI with pinned host buffers
+    bh = torch.from_numpy(w.b).pin_memory()
+    xh = torch.empty(w.n, dtype=torch.float64).pin_memory()
+    hh = torch.empty(w.maxit + 1, dtype=torch.float64).pin_memory()
+    evocg.cg_solve(G, bh, xh, w.rtol, w.maxit, w.jacobi, ctrl, True, hh)
+    e2e_steps = max(1, min(args.steps, 5))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    e2e_infos = [evocg.cg_solve(G, bh, xh, w.rtol, w.maxit, w.jacobi, ctrl, True, hh)
+                 for _ in range(e2e_steps)]
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    h2d = 8 * w.n
+    d2h = 8 * w.n + 8 * (e2e_infos[-1]["iters"] + 1)
+
+    # ---- the dominant kernel (the SpMV) timed alone on the same stream, CUDA events,
+    # back-to-back launches (inputs > L2), with the seeded 40/40/20 mixed map and all-FP64
+    trow, ex = G.tile_rows()
+    tnnz = np.diff(ex["tileNnzOff"])
+    peak, peak_kind = _peaks()
+    xs = torch.from_numpy(np.random.default_rng(7).uniform(-1, 1, w.n)).to(dev)
+    ys = torch.empty_like(xs)
+    spmv = {}
+    for label, mp in (("mixed_40_40_20", W.tile_map(trow, ex["tileColIdx"], G.nrb, 12345)),
+                      ("fp64", np.zeros(G.ntiles, np.uint8))):
+        evocg.set_tile_precision(G, mp)
+        evocg.spmv(G, xs, ys)
+        reps = 50
+        for _ in range(5):
+            evocg.spmv_ex(G, xs, ys, evocg.SPMV_REUSE_XCOPIES)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            evocg.spmv_ex(G, xs, ys, evocg.SPMV_REUSE_XCOPIES)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000.0 / reps
+        per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
+        B = _spmv_bytes(w.n, G.ntiles, G.nrb, w.T, per)
+        spmv[label] = {"us": us, "bytes": int(B), "gbs": B / us / 1e3,
+                       "frac_of_peak": B / us / 1e3 / peak, "frac_of_8tbs": B / us / 1e3 / 8000.0}
+    src_hash = _src_hash()
+    traffic = _traffic_for(src_hash)
+    mixed = spmv["mixed_40_40_20"]
+    roofline = {"bound": "hbm", "achieved": mixed["gbs"], "peak": peak, "unit": "GB/s",
+                "frac": mixed["frac_of_peak"], "traffic": traffic,
+                "kernel": "spmv_kernel<32> (mixed 40/40/20 map)", "peak_kind": peak_kind,
+                "frac_of_8tbs": mixed["frac_of_8tbs"], "bytes_per_launch": mixed["bytes"],
+                "us_per_launch": mixed["us"], "fp64_map": spmv["fp64"]}
+
+    # ---- CPU oracle on the host cores, a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sec_it, _ = oracle_sample(w, args.cpu_sample_iters)
+        cpu = {"value": sec_it * info["iters"], "unit": "s", "cores": 1, "kind": "oracle",
+               "sample": f"first {args.cpu_sample_iters} iterations of the same solve, "
+                         f"seconds/iteration x the GPU solve's {info['iters']} iterations"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64+f32+bf16 (tile-wise), f64 vectors", "data": "synthetic",
+            "config": {"workload": w.name, "n": w.n, "nnz": w.nnz, "tile": w.T,
+                       "solver": "jacobi-pcg" if w.jacobi else "cg", "rtol": w.rtol,
+                       "maxit": w.maxit, "controller": w.ctrl, "finish_fp64": True,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (matrix streams ~230 MB)"},
+            "solve": {"iters": info["iters"], "iters_recursive": info["iters_recursive"],
+                      "restarts": info["restarts"], "true_res": info["true_res"],
+                      "prec_nnz": info["prec_nnz"], "ctrl_calls": info["ctrl_calls"],
+                      "status": info["status"], "tile_build_s": build_s,
+                      "s_per_iter": value / max(1, info["iters"]) * world},
+            "clocks": clk.summary(),
+            "e2e": {"value": e2e_ms / 1000.0 / world, "unit": "s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    G.free()
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--cpu-sample-iters", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -153,6 +153,21 @@ int evocg_get_tile_precision(evocg_tiles_t A, uint8_t *map_out, int64_t len, voi
  */
 int evocg_spmv(evocg_tiles_t A, const double *x, double *y, void *stream);
 
+/* Flags of evocg_spmv_ex. */
+enum {
+    EVOCG_SPMV_REUSE_XCOPIES = 1  /* skip rounding x: reuse the FP32/BF16 copies of x made by
+                                     the previous evocg_spmv / evocg_spmv_ex call on this
+                                     handle; x must hold the same values as in that call */
+};
+
+/*
+ * evocg_spmv with flags (EVOCG_SPMV_*). With EVOCG_SPMV_REUSE_XCOPIES the call is exactly
+ * one SpMV kernel launch, which repeated products with one x and kernel timing use.
+ * x, y: DEVICE pointers when EVOCG_SPMV_REUSE_XCOPIES is set (EINVAL otherwise, and also
+ * when no earlier call on the handle made the copies); otherwise as evocg_spmv.
+ */
+int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int flags, void *stream);
+
 /*
  * CG (jacobi = 0) or Jacobi-preconditioned CG (jacobi = 1) for A x = b from x0 = 0, in
  * the order of EvoCG Algorithm 1 (the solver lines) and §4.6:

@@ -402,13 +402,19 @@ extern "C" int evocg_get_tile_precision(evocg_tiles_t A, uint8_t *map_out, int64
     return EVOCG_OK;
 }
 
-extern "C" int evocg_spmv(evocg_tiles_t A, const double *x, double *y, void *stream)
+extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int flags, void *stream)
 {
     g_err.clear();
     if (!A || (A->n > 0 && (!x || !y))) return fail(EVOCG_EINVAL, "NULL argument");
+    if (flags & ~EVOCG_SPMV_REUSE_XCOPIES) return fail(EVOCG_EINVAL, "unknown flags");
     if (A->n == 0) return EVOCG_OK;
     cudaStream_t s = (cudaStream_t)stream;
+    const bool reuse = (flags & EVOCG_SPMV_REUSE_XCOPIES) != 0;
     const bool xdev = is_device_ptr(x), ydev = is_device_ptr(y);
+    if (reuse && (!xdev || !ydev))
+        return fail(EVOCG_EINVAL, "EVOCG_SPMV_REUSE_XCOPIES needs device x and y");
+    if (reuse && !A->xcopies_valid)
+        return fail(EVOCG_EINVAL, "EVOCG_SPMV_REUSE_XCOPIES: no earlier SpMV made the copies");
     const size_t bytes = sizeof(double) * (size_t)A->n;
     const double *xd = x;
     double *yd = y;
@@ -421,7 +427,10 @@ extern "C" int evocg_spmv(evocg_tiles_t A, const double *x, double *y, void *str
         xd = A->xstage;
     }
     if (!ydev) yd = A->ystage;
-    CK(launch_xcopies(A->view(), xd, A->x32, A->x16, A->vec_grid, s), "launch x copies");
+    if (!reuse) {
+        CK(launch_xcopies(A->view(), xd, A->x32, A->x16, A->vec_grid, s), "launch x copies");
+        A->xcopies_valid = 1;
+    }
     SpmvLaunch S{};
     S.A = A->view();
     S.x64 = xd; S.x32 = A->x32; S.x16 = A->x16; S.y = yd;
@@ -434,6 +443,11 @@ extern "C" int evocg_spmv(evocg_tiles_t A, const double *x, double *y, void *str
         CK(cudaStreamSynchronize(s), "synchronise");
     }
     return EVOCG_OK;
+}
+
+extern "C" int evocg_spmv(evocg_tiles_t A, const double *x, double *y, void *stream)
+{
+    return evocg_spmv_ex(A, x, y, 0, stream);
 }
 
 extern "C" int evocg_round(const double *x, int64_t n, float *out32, uint16_t *out16, void *stream)
@@ -554,6 +568,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     H.eps_hi = (kind == EVOCG_CTRL_THRESHOLD) ? ctrl->eps : 0.0;
     CK(cudaMemcpyAsync(w.st, &H, sizeof(DevState), cudaMemcpyHostToDevice, s), "upload state");
     if (n > 0) CK(cudaMemcpyAsync(w.b, b, bytes, cudaMemcpyDefault, s), "copy b");
+    A->xcopies_valid = 0;  // the solve reuses the copy buffers for p
     CK(cudaGraphLaunch(w.exec, s), "cudaGraphLaunch");
     CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");
     CK(cudaStreamSynchronize(s), "synchronise solve");

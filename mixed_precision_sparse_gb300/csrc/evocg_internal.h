@@ -99,6 +99,7 @@ struct evocg_tiles {
     float *x32 = nullptr;
     uint16_t *x16 = nullptr;
     double *xstage = nullptr, *ystage = nullptr;
+    int xcopies_valid = 0;          // x32/x16 hold the copies of the last SpMV's x
     int spmv_grid = 0, vec_grid = 0;
     evocg::SolveWS ws;
 

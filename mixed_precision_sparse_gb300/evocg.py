@@ -92,6 +92,7 @@ def lib():
                 "evocg_set_tile_precision": [P, P, i64, i32, P],
                 "evocg_get_tile_precision": [P, P, i64, P],
                 "evocg_spmv": [P, P, P, P],
+                "evocg_spmv_ex": [P, P, P, i32, P],
                 "evocg_cg_solve": [P, P, P, dbl, i32, i32, C.POINTER(Ctrl), i32, P,
                                    C.POINTER(SolveInfo), P],
                 "evocg_ctrl_decide": [P, C.POINTER(Ctrl), P, P, P, P],
@@ -214,8 +215,16 @@ def get_tile_precision(A: Tiles, stream=None):
     return out
 
 
+SPMV_REUSE_XCOPIES = 1
+
+
 def spmv(A: Tiles, x, y, stream=None):
     _check(lib().evocg_spmv(A.h, _ptr(x), _ptr(y), _stream(stream)))
+    return y
+
+
+def spmv_ex(A: Tiles, x, y, flags: int = 0, stream=None):
+    _check(lib().evocg_spmv_ex(A.h, _ptr(x), _ptr(y), int(flags), _stream(stream)))
     return y
 
 
