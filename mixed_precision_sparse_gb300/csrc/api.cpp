@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -173,6 +174,7 @@ int build_graph(evocg_tiles *A, CgLaunch L, int restart, cudaGraph_t *graph_out,
     if (e == cudaSuccess) e = cudaGraphConditionalHandleCreate(&h, g, 1u, cudaGraphCondAssignDefault);
     if (e == cudaSuccess) {
         L.cond = h;
+        L.use_cond = 1;
         e = cudaStreamBeginCaptureToGraph(cs, g, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal);
     }
     bool capturing = (e == cudaSuccess);
@@ -233,6 +235,39 @@ int build_graph(evocg_tiles *A, CgLaunch L, int restart, cudaGraph_t *graph_out,
     *graph_out = g;
     *exec_out = ex;
     return rc;
+}
+
+// The same kernels as the graph, launched one by one, with the stop flag read back every
+// kPlainBatch iterations (kernels queued after the stop return at once). Selected with
+// EVOCG_GRAPH=0 in the environment; profilers that cannot see inside graphs with
+// conditional nodes list every kernel of the solve this way.
+constexpr int kPlainBatch = 32;
+
+int run_plain(evocg_tiles *A, CgLaunch L, int restart, cudaStream_t s)
+{
+    SolveWS &w = A->ws;
+    L.use_cond = 0;
+    L.cond = 0;
+    if (restart) {
+        SpmvLaunch S{};
+        S.A = L.A; S.x64 = L.x; S.y = L.q; S.force64 = 1; S.dot = 0; S.st = L.st;
+        S.census = 0; S.grid = L.spmv_grid;
+        CK(launch_spmv(S, s), "spmv (restart)");
+    }
+    CK(launch_cg_init(L, restart, s), "cg init");
+    for (;;) {
+        CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");
+        CK(cudaStreamSynchronize(s), "synchronise");
+        if (w.st_host->done) break;
+        for (int i = 0; i < kPlainBatch; ++i) CK(launch_cg_body(L, restart, s), "cg body");
+    }
+    return EVOCG_OK;
+}
+
+bool graphs_enabled()
+{
+    const char *v = std::getenv("EVOCG_GRAPH");
+    return !(v && v[0] == '0');
 }
 
 }  // namespace
@@ -551,7 +586,8 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
         const unsigned char *pb = reinterpret_cast<const unsigned char *>(&L);
         for (size_t i = 0; i < sizeof(L); ++i) key = (key ^ pb[i]) * 1099511628211ull;
     }
-    if (!w.exec || w.exec_key != key) {
+    const bool use_graph = graphs_enabled();
+    if (use_graph && (!w.exec || w.exec_key != key)) {
         if (w.exec) { cudaGraphExecDestroy(w.exec); w.exec = nullptr; }
         if (w.graph) { cudaGraphDestroy(w.graph); w.graph = nullptr; }
         rc = build_graph(A, L, 0, &w.graph, &w.exec);
@@ -569,7 +605,12 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     CK(cudaMemcpyAsync(w.st, &H, sizeof(DevState), cudaMemcpyHostToDevice, s), "upload state");
     if (n > 0) CK(cudaMemcpyAsync(w.b, b, bytes, cudaMemcpyDefault, s), "copy b");
     A->xcopies_valid = 0;  // the solve reuses the copy buffers for p
-    CK(cudaGraphLaunch(w.exec, s), "cudaGraphLaunch");
+    if (use_graph) {
+        CK(cudaGraphLaunch(w.exec, s), "cudaGraphLaunch");
+    } else {
+        rc = run_plain(A, L, 0, s);
+        if (rc) return rc;
+    }
     CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");
     CK(cudaStreamSynchronize(s), "synchronise solve");
 
@@ -587,7 +628,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
             CgLaunch R = L;
             R.ctrl = EVOCG_CTRL_STATIC;
             uint64_t rkey = key ^ 0x9E3779B97F4A7C15ull;
-            if (!w.exec_rs || w.exec_rs_key != rkey) {
+            if (use_graph && (!w.exec_rs || w.exec_rs_key != rkey)) {
                 if (w.exec_rs) { cudaGraphExecDestroy(w.exec_rs); w.exec_rs = nullptr; }
                 if (w.graph_rs) { cudaGraphDestroy(w.graph_rs); w.graph_rs = nullptr; }
                 rc = build_graph(A, R, 1, &w.graph_rs, &w.exec_rs);
@@ -595,7 +636,12 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
                 w.exec_rs_key = rkey;
             }
             restarts++;
-            CK(cudaGraphLaunch(w.exec_rs, s), "cudaGraphLaunch (restart)");
+            if (use_graph) {
+                CK(cudaGraphLaunch(w.exec_rs, s), "cudaGraphLaunch (restart)");
+            } else {
+                rc = run_plain(A, R, 1, s);
+                if (rc) return rc;
+            }
             CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");
             CK(cudaStreamSynchronize(s), "synchronise restart");
         }

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
                 st->done = 1;
                 st->status = EVOCG_ENOTCONV;
             }
-            cudaGraphSetConditional(L.cond, st->done ? 0u : 1u);
+            if (L.use_cond) cudaGraphSetConditional(L.cond, st->done ? 0u : 1u);
         }
     }
 }
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kVecThreads) cg_update_kernel(CgLaunch L)
 {
     DevState *st = L.st;
     if (st->done) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) cudaGraphSetConditional(L.cond, 0u);
+        if (L.use_cond && blockIdx.x == 0 && threadIdx.x == 0) cudaGraphSetConditional(L.cond, 0u);
         return;
     }
     const double alpha = st->alpha;
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kVecThreads) cg_update_kernel(CgLaunch L)
                 st->beta = rho_new / st->rho;
                 st->rho = rho_new;
             }
-            cudaGraphSetConditional(L.cond, st->done ? 0u : 1u);
+            if (L.use_cond) cudaGraphSetConditional(L.cond, st->done ? 0u : 1u);
         }
     }
 }

@@ -181,6 +181,7 @@ struct CgLaunch {
     DevState *st;
     int vec_grid, spmv_grid;
     cudaGraphConditionalHandle cond;
+    int use_cond;          // 1 inside the solve graph: the kernels drive its while node
 };
 cudaError_t launch_cg_init(const CgLaunch &L, int restart, cudaStream_t s);
 cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s);

@@ -175,3 +175,16 @@ def test_cg_history_full_size_first_iterations(cfg, iters):
     assert info["iters"] == ref["iters"] == iters
     assert np.allclose(h, ref["hist"], rtol=1e-8)
     assert np.linalg.norm(x - ref["x"]) <= 1e-8 * np.linalg.norm(ref["x"])
+
+
+def test_plain_launch_mode_matches_graph(monkeypatch):
+    """EVOCG_GRAPH=0 runs the same kernels launched one by one: bit-identical results."""
+    w = W.workload(2, scale=0.2)
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    ctrl = evocg.Ctrl.threshold(w.eps)
+    a = _solve(P, w.b, w.rtol, w.maxit, True, ctrl, True)
+    monkeypatch.setenv("EVOCG_GRAPH", "0")
+    b = _solve(P, w.b, w.rtol, w.maxit, True, ctrl, True)
+    monkeypatch.delenv("EVOCG_GRAPH")
+    assert a[0]["iters"] == b[0]["iters"] and a[0]["prec_nnz"] == b[0]["prec_nnz"]
+    assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
