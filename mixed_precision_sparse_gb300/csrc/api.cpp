@@ -60,7 +60,8 @@ cudaError_t dalloc(T **p, int64_t count)
 {
     *p = nullptr;
     if (count <= 0) count = 1;
-    return cudaMalloc((void **)p, sizeof(T) * (size_t)count);
+    // kSlack bytes past the end: the SpMV stages arrays in 16-byte granules
+    return cudaMalloc((void **)p, sizeof(T) * (size_t)count + kSlack);
 }
 
 template <class T>
@@ -309,6 +310,7 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     up(&A->tileRowPtr, H.tileRowPtr, H.nrb + 1);
     up(&A->tileColIdx, H.tileColIdx, H.ntiles);
     up(&A->tileNnzOff, H.tileNnzOff, H.ntiles + 1);
+    up(&A->tileRowIdx, H.tileRowIdx, H.ntiles);
     up(&A->rowEnd, H.rowEnd, H.ntiles * H.T);
     up(&A->colIdx, H.colIdx, H.nnz);
     up(&A->v64, H.v64, H.nnz);
@@ -322,7 +324,7 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     if (e == cudaSuccess) e = dalloc(&A->cbPrec, A->nrb);
     if (e == cudaSuccess) e = cudaMemset(A->cbPrec, 0, (size_t)(A->nrb > 0 ? A->nrb : 1));
     if (e == cudaSuccess) e = dalloc(&A->x32, A->n);
-    if (e == cudaSuccess) e = dalloc(&A->x16, A->n);
+    if (e == cudaSuccess) e = dalloc(&A->x16f, A->n);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         int code = cuda_fail(e, "uploading the tile structure");
@@ -340,9 +342,10 @@ extern "C" int evocg_tiles_free(evocg_tiles_t A)
     if (!A) return EVOCG_OK;
     cudaDeviceSynchronize();
     release_ws(A->ws);
-    dfree(A->tileRowPtr); dfree(A->tileColIdx); dfree(A->tileNnzOff); dfree(A->rowEnd);
+    dfree(A->tileRowPtr); dfree(A->tileColIdx); dfree(A->tileNnzOff); dfree(A->tileRowIdx);
+    dfree(A->rowEnd);
     dfree(A->colIdx); dfree(A->v64); dfree(A->v32); dfree(A->v16); dfree(A->colExp);
-    dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16);
+    dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16f);
     dfree(A->xstage); dfree(A->ystage);
     delete A;
     return EVOCG_OK;
@@ -463,12 +466,12 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     }
     if (!ydev) yd = A->ystage;
     if (!reuse) {
-        CK(launch_xcopies(A->view(), xd, A->x32, A->x16, A->vec_grid, s), "launch x copies");
+        CK(launch_xcopies(A->view(), xd, A->x32, A->x16f, A->vec_grid, s), "launch x copies");
         A->xcopies_valid = 1;
     }
     SpmvLaunch S{};
     S.A = A->view();
-    S.x64 = xd; S.x32 = A->x32; S.x16 = A->x16; S.y = yd;
+    S.x64 = xd; S.x32 = A->x32; S.x16f = A->x16f; S.y = yd;
     S.prec = (A->map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
     S.map_kind = A->map_kind;
     S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
@@ -572,7 +575,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     L.A = A->view();
     L.n = n; L.T = A->T; L.jacobi = jacobi ? 1 : 0; L.ctrl = kind; L.dinv = A->dinv;
     L.b = w.b; L.x = w.x; L.r = w.r; L.p = w.p; L.q = w.q; L.z = w.z;
-    L.x32 = A->x32; L.x16 = A->x16; L.hist = w.hist; L.partials = w.partials;
+    L.x32 = A->x32; L.x16f = A->x16f; L.hist = w.hist; L.partials = w.partials;
     L.cbPrec = w.cbPrec;
     L.prec = (A->map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
     L.map_kind = A->map_kind;

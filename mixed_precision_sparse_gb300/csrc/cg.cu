@@ -79,13 +79,13 @@ __device__ __forceinline__ void threshold_segments(uint64_t m, int64_t pair, int
     }
 }
 
-// Rounded copies of p for the next SpMV's low-precision tiles (x32, x16) and its
+// Rounded copies of p for the next SpMV's low-precision tiles (x32, x16f) and its
 // threshold features; entries past n are zero.
 __device__ __forceinline__ void write_copies(const CgLaunch &L, int64_t j, double v)
 {
     const float s = pow2f(L.A.colExp[j]);
     L.x32[j] = __fmul_rn(f32_from_f64_rn(v), s);
-    L.x16[j] = (uint16_t)(__float_as_uint(__fmul_rn(f32_from_bf16(bf16_from_f64_rn(v)), s)) >> 16);
+    L.x16f[j] = __fmul_rn(f32_from_bf16(bf16_from_f64_rn(v)), s);
 }
 
 // Start (restart = 0) or FP64-finish restart (restart = 1, after q = A x in FP64):
@@ -346,7 +346,7 @@ cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
     S.A = L.A;
     S.x64 = L.p;
     S.x32 = L.x32;
-    S.x16 = L.x16;
+    S.x16f = L.x16f;
     S.y = L.q;
     S.prec = (L.ctrl == EVOCG_CTRL_STATIC) ? L.prec : L.cbPrec;
     S.map_kind = (L.ctrl == EVOCG_CTRL_STATIC) ? L.map_kind : EVOCG_MAP_PER_COLBLOCK;

@@ -13,7 +13,10 @@ namespace evocg {
 constexpr int kMaxBlocks = 2048;      // upper bound of any grid here (partials buffers)
 constexpr int kVecThreads = 256;      // threads per block of the vector kernels
 constexpr int kSpmvThreads = 256;     // threads per block of the SpMV
+constexpr int kSpmvMinBlocks = 4;     // resident blocks per SM the SpMV registers are budgeted for
 constexpr int kMlpHiddenMax = 64;
+constexpr int kStages = 5;            // tile slots per warp in the SpMV's shared-memory ring
+constexpr int kSlack = 16;            // bytes past the end of every staged array
 
 // Device-resident solver state; one per handle. Written by the last block of each
 // reducing kernel, read by every block of the next kernel.
@@ -46,6 +49,7 @@ struct TilesView {
     const int64_t *tileRowPtr;
     const int32_t *tileColIdx;
     const int64_t *tileNnzOff;
+    const int32_t *tileRowIdx;  // row block of each tile (device-side helper, not exported)
     const uint16_t *rowEnd;
     const uint8_t *colIdx;
     const double *v64;
@@ -84,6 +88,7 @@ struct evocg_tiles {
     int64_t *tileRowPtr = nullptr;
     int32_t *tileColIdx = nullptr;
     int64_t *tileNnzOff = nullptr;
+    int32_t *tileRowIdx = nullptr;
     uint16_t *rowEnd = nullptr;
     uint8_t *colIdx = nullptr;
     double *v64 = nullptr;
@@ -97,16 +102,16 @@ struct evocg_tiles {
     int diag_ok = 0;               // every diagonal entry present and > 0
     // SpMV scratch: rounded x copies and host staging
     float *x32 = nullptr;
-    uint16_t *x16 = nullptr;
+    float *x16f = nullptr;          // BF16 roundings held in FP32 containers
     double *xstage = nullptr, *ystage = nullptr;
-    int xcopies_valid = 0;          // x32/x16 hold the copies of the last SpMV's x
+    int xcopies_valid = 0;          // x32/x16f hold the copies of the last SpMV's x
     int spmv_grid = 0, vec_grid = 0;
     evocg::SolveWS ws;
 
     evocg::TilesView view() const
     {
-        return evocg::TilesView{n, nrb, ntiles, T, tileRowPtr, tileColIdx, tileNnzOff, rowEnd,
-                                colIdx, v64, v32, v16, colExp};
+        return evocg::TilesView{n, nrb, ntiles, T, tileRowPtr, tileColIdx, tileNnzOff, tileRowIdx,
+                                rowEnd, colIdx, v64, v32, v16, colExp};
     }
 };
 
@@ -124,6 +129,7 @@ struct HostTiles {
     int64_t *tileRowPtr = nullptr;
     int32_t *tileColIdx = nullptr;
     int64_t *tileNnzOff = nullptr;
+    int32_t *tileRowIdx = nullptr;
     uint16_t *rowEnd = nullptr;
     uint8_t *colIdx = nullptr;
     double *v64 = nullptr;
@@ -142,7 +148,7 @@ struct SpmvLaunch {
     TilesView A;
     const double *x64;
     const float *x32;
-    const uint16_t *x16;
+    const float *x16f;
     double *y;
     const uint8_t *prec;   // tilePrec (map_kind 0) or cbPrec (map_kind 1); ignored if force64
     int map_kind;
@@ -155,10 +161,10 @@ struct SpmvLaunch {
     int grid;
 };
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
-cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, uint16_t *x16,
+cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, float *x16f,
                            int grid, cudaStream_t s);
 cudaError_t launch_round(const double *x, int64_t n, float *o32, uint16_t *o16, cudaStream_t s);
-int spmv_grid_for(int T, int sms);
+int spmv_grid_for(int T, int sms);   // also raises the kernels' shared-memory limit
 
 struct CgLaunch {
     TilesView A;
@@ -169,7 +175,7 @@ struct CgLaunch {
     const double *dinv;
     double *b, *x, *r, *p, *q, *z;
     float *x32;
-    uint16_t *x16;
+    float *x16f;
     double *hist;
     double *partials;
     uint8_t *cbPrec;       // controller output (map_kind 1 for the SpMV)

@@ -1,14 +1,41 @@
-// spmv.cu -- launchers of the tile-wise mixed-precision SpMV (the kernel body lives in
-// spmv_kernel.cuh), the rounded x copies it reads, and the device rounding entry point.
+// spmv.cu -- the tile-wise mixed-precision SpMV (EvoCG, "Self-Evolving Precision Control
+// for Faster Conjugate Gradient", §3.3 EvoSpMV, Eq. 2 / Eq. 5) for sm_103a, its launchers,
+// the rounded x copies it reads, and the device rounding entry point.
+//
+// Work mapping. A warp owns a row block (T rows) at a time and walks its tiles in
+// ascending column block, so every row is summed in column order. Lane l owns local row
+// l (T = 32), rows l and l+32 (T = 64), or, for T = 16, the two half-warps take
+// alternate tiles of the row block and are merged at the end. Each lane keeps its rows'
+// sums in registers for the whole row block: no cross-lane reduction at all.
+//
+// Arithmetic. An FP64 tile costs exactly one FP64 fused multiply-add per entry, the
+// floor for FP64 data. FP32 and BF16 tiles never touch the FP64 unit: their products
+// are exact in an FP32 pair (BF16 x BF16 fits in FP32; FP32 x FP32 is split by one
+// fused multiply-add), summed error-free (TwoSum) into an FP32 hi/lo pair, and merged
+// into the FP64 row sum once per row: about 48 bits of the sum are kept, so a
+// low-precision tile contributes its exactly rounded-operand products, as the paper's
+// model asks, and the row sum stays an FP64 sum. GB300 issues FP64 at about 1/58 of
+// the FP32 rate, so this split is what lets low-precision tiles run at memory speed.
+//
+// Operands. The x entries a low-precision tile reads are the FP32 / BF16 roundings of x
+// scaled by the column factor 2^e_j, made once per SpMV (xcopies_kernel, or the CG
+// p-update) with integer instructions.
 #include <cuda_runtime.h>
 
 #include "evocg_internal.h"
 #include "fpconv.cuh"
-#include "spmv_kernel.cuh"
 
 namespace evocg {
 
-// Last block of a grid: true in every thread of the block whose ticket comes last.
+template <int T>
+struct Geo {
+    static constexpr int G = T < 32 ? T : 32;  // lanes per row group
+    static constexpr int NG = 32 / G;          // row groups per warp
+    static constexpr int RPL = T / G;          // rows per lane
+};
+
+// Last block of a grid: sums per-block partials in a fixed order (deterministic) and
+// returns true in every thread of that block. `slot` selects the ticket counter.
 __device__ __forceinline__ bool last_block(DevState *st, int slot)
 {
     __shared__ bool amLast;
@@ -23,8 +50,7 @@ __device__ __forceinline__ bool last_block(DevState *st, int slot)
     return amLast;
 }
 
-// Deterministic block sum of one double per thread (fixed shuffle tree, fixed order);
-// the result is valid in thread 0.
+// Deterministic block sum of one double per thread (fixed shuffle tree, fixed order).
 __device__ __forceinline__ double block_sum(double v)
 {
     __shared__ double ws[32];
@@ -36,119 +62,99 @@ __device__ __forceinline__ double block_sum(double v)
     double s = 0.0;
     if (threadIdx.x == 0)
         for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += ws[i];
-    return s;
-}
-
-__device__ __forceinline__ int64_t shfl64(int64_t v, int src)
-{
-    const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)(uint64_t)v, src);
-    const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)((uint64_t)v >> 32), src);
-    return (int64_t)(((uint64_t)hi << 32) | lo);
+    return s;  // valid in thread 0
 }
 
 template <int T, bool FORCE64, bool DOT>
-__global__ void __launch_bounds__(kSpmvThreads) spmv_kernel(SpmvLaunch L)
+__global__ void __launch_bounds__(kSpmvThreads, kSpmvMinBlocks) spmv_kernel(SpmvLaunch L)
 {
     using Gm = Geo<T>;
     if (DOT && L.st->done) return;  // a stopped solve: nothing to compute or count
     const TilesView A = L.A;
-    const unsigned lane = lane_id();
-    const int gl = (int)(lane % Gm::G);
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / Gm::G;
+    const int gl = lane % Gm::G;
     const int64_t wpb = blockDim.x >> 5;
-    const int64_t W = (int64_t)gridDim.x * wpb;
-    const int64_t w = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
-    const int64_t rbA = w * A.nrb / W, rbB = (w + 1) * A.nrb / W;
+    const int64_t nwarps = (int64_t)gridDim.x * wpb;
+    const int64_t wid = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     double dotp = 0.0;
     unsigned long long cnt0 = 0, cnt1 = 0, cnt2 = 0;
-    double acc[Gm::RPL];
-    F32Pair pr[Gm::RPL];
-#pragma unroll
-    for (int rr = 0; rr < Gm::RPL; ++rr) acc[rr] = 0.0;
-    bool any64 = false, anylow = false;
-    int64_t rb_cur = rbA;
 
-    // write the rows of rb_cur, zero rows of the empty row blocks before new_rb, move on
-    auto flush_to = [&](int64_t new_rb) {
+    for (int64_t rb = wid; rb < A.nrb; rb += nwarps) {
+        const int64_t t0 = A.tileRowPtr[rb], t1 = A.tileRowPtr[rb + 1];
+        double acc64[Gm::RPL];
+        F32Pair accl[Gm::RPL];
 #pragma unroll
-        for (int rr = 0; rr < Gm::RPL; ++rr) {
-            const int64_t row = rb_cur * T + gl + rr * Gm::G;
-            if ((int)lane < Gm::G && row < A.n) {
-                double y = acc[rr];
-                if (anylow) {
-                    const double d = f64_from_f32(pr[rr].hi) + f64_from_f32(pr[rr].lo);
-                    y = any64 ? y + d : d;
+        for (int rr = 0; rr < Gm::RPL; ++rr) acc64[rr] = 0.0;
+        bool any64 = false, anylow = false;
+        for (int64_t t = t0 + grp; t < t1; t += Gm::NG) {
+            const int64_t cb = A.tileColIdx[t];
+            const int64_t off = A.tileNnzOff[t];
+            const int prec = FORCE64 ? 0 : (int)__ldg(L.prec + (L.map_kind ? cb : t));
+            const uint8_t *ci = A.colIdx + off;
+            const int64_t xb = cb * T;
+            const uint16_t *re = A.rowEnd + t * T;
+#pragma unroll
+            for (int rr = 0; rr < Gm::RPL; ++rr) {
+                const int r = gl + rr * Gm::G;
+                const int end = __ldg(re + r);
+                const int start = r ? (int)__ldg(re + r - 1) : 0;
+                if (prec == EVOCG_FP64) {
+                    const double *vv = A.v64 + off;
+                    const double *xs = L.x64 + xb;
+                    double a = acc64[rr];
+#pragma unroll 4
+                    for (int k = start; k < end; ++k)
+                        a = fma(__ldg(vv + k), __ldg(xs + __ldg(ci + k)), a);
+                    acc64[rr] = a;
+                } else if (prec == EVOCG_FP32) {
+                    const float *vv = A.v32 + off;
+                    const float *xs = L.x32 + xb;
+#pragma unroll 4
+                    for (int k = start; k < end; ++k)
+                        accl[rr].add_prod(__ldg(vv + k), __ldg(xs + __ldg(ci + k)));
+                } else {
+                    const uint16_t *vv = A.v16 + off;
+                    const float *xs = L.x16f + xb;
+#pragma unroll 4
+                    for (int k = start; k < end; ++k)  // BF16 x BF16 is exact in FP32
+                        accl[rr].add(__fmul_rn(f32_from_bf16(__ldg(vv + k)), __ldg(xs + __ldg(ci + k))));
                 }
-                L.y[row] = y;
-                if (DOT) dotp = fma(__ldg(L.x64 + row), y, dotp);
             }
-            acc[rr] = 0.0;
-            pr[rr] = F32Pair();
+            any64 |= (prec == EVOCG_FP64);
+            anylow |= (prec != EVOCG_FP64);
+            if (L.census && gl == 0) {
+                const unsigned long long c = __ldg(re + T - 1);
+                if (prec == 0) cnt0 += c; else if (prec == 1) cnt1 += c; else cnt2 += c;
+            }
         }
-        for (int64_t rb = rb_cur + 1; rb < new_rb; ++rb)
+        if (Gm::NG == 2) {  // T = 16: fold the odd-tile half-warp into the even one
+#pragma unroll
+            for (int rr = 0; rr < Gm::RPL; ++rr) {
+                acc64[rr] += __shfl_down_sync(0xffffffffu, acc64[rr], 16);
+                F32Pair o;
+                o.hi = __shfl_down_sync(0xffffffffu, accl[rr].hi, 16);
+                o.lo = __shfl_down_sync(0xffffffffu, accl[rr].lo, 16);
+                accl[rr].merge(o);
+            }
+        }
+        any64 = __any_sync(0xffffffffu, any64);
+        anylow = __any_sync(0xffffffffu, anylow);
+        if (grp == 0) {
 #pragma unroll
             for (int rr = 0; rr < Gm::RPL; ++rr) {
                 const int64_t row = rb * T + gl + rr * Gm::G;
-                if ((int)lane < Gm::G && row < A.n) L.y[row] = 0.0;
-            }
-        any64 = false;
-        anylow = false;
-        rb_cur = new_rb;
-    };
-
-    if (rbA < rbB) {
-        int64_t t = A.tileRowPtr[rbA];
-        const int64_t tEnd = A.tileRowPtr[rbB];
-        while (t < tEnd) {
-            const int64_t rb0 = rb_cur;
-            // ends of the row blocks rb0 .. rb0+31 (capped at this warp's range)
-            const int64_t wend = __ldg(A.tileRowPtr + min(rb0 + 1 + (int64_t)lane, rbB));
-            const int64_t wlast = shfl64(wend, 31);
-            if (wlast <= t) {  // those 32 row blocks have no tiles left
-                flush_to(min(rb0 + 32, rbB));
-                continue;
-            }
-            const int64_t cend = min(min(t + 32, tEnd), wlast);
-            const int nt = (int)(cend - t);
-            // row ends of the first two tiles, while the descriptors load
-            RowEnds<T> R0, R1;
-            load_rowends<T>(A, t, 0, nt, R0);
-            load_rowends<T>(A, t, 1, nt, R1);
-            // descriptors of the chunk: lane u holds tile t+u
-            const int64_t tt = t + lane;
-            int cbv = 0, pv = 0;
-            int64_t ov = 0;
-            if ((int)lane < nt) {
-                cbv = __ldcs(A.tileColIdx + tt);
-                ov = __ldcs(A.tileNnzOff + tt);
-                pv = FORCE64 ? 0 : (int)__ldg(L.prec + (L.map_kind ? (int64_t)cbv : tt));
-                if (L.census) {
-                    const unsigned long long c = (unsigned long long)(__ldcs(A.tileNnzOff + tt + 1) - ov);
-                    if (pv == 0) cnt0 += c; else if (pv == 1) cnt1 += c; else cnt2 += c;
+                if (row < A.n) {
+                    double y = acc64[rr];
+                    if (anylow) {
+                        const double d = f64_from_f32(accl[rr].hi) + f64_from_f32(accl[rr].lo);
+                        y = any64 ? y + d : d;
+                    }
+                    L.y[row] = y;
+                    if (DOT) dotp = fma(__ldg(L.x64 + row), y, dotp);
                 }
             }
-            int drb = 0;  // row block of tile tt, counted from rb0: window ends <= tt
-#pragma unroll
-            for (int step = 16; step; step >>= 1)
-                if (shfl64(wend, drb + step - 1) <= tt) drb += step;
-            const int64_t offbase = shfl64(ov, 0);
-            const uint32_t dw0 = (uint32_t)cbv | ((uint32_t)pv << 28);
-            const uint32_t dw1 = (uint32_t)(ov - offbase) | ((uint32_t)drb << 24);
-
-            TileStage<T> S0, S1;
-            load_stage<T>(A, L, dw0, dw1, offbase, 0, nt, R0, S0);
-            for (int u = 0; u < nt; ++u) {
-                load_stage<T>(A, L, dw0, dw1, offbase, u + 1, nt, R1, S1);
-                load_rowends<T>(A, t, u + 2, nt, R1);
-                const int64_t rbu = rb0 + S0.drb;
-                if (rbu != rb_cur) flush_to(rbu);
-                any64 |= (S0.prec == EVOCG_FP64);
-                anylow |= (S0.prec != EVOCG_FP64);
-                compute_stage<T>(A, L, S0, acc, pr);
-                S0 = S1;
-            }
-            t = cend;
         }
-        flush_to(rbB);
     }
     if (L.census) {
         for (int o = 16; o; o >>= 1) {
@@ -186,17 +192,18 @@ __global__ void __launch_bounds__(kSpmvThreads) spmv_kernel(SpmvLaunch L)
     }
 }
 
-// x copies for the low-precision tiles: x32_j = RN32(x_j) 2^e_j, x16_j = RN16(x_j) 2^e_j.
+// x copies for the low-precision tiles: x32_j = RN32(x_j) 2^e_j and x16f_j = RN16(x_j) 2^e_j,
+// the BF16 value held in an FP32 container (4-byte copies stage it like x32).
 __global__ void __launch_bounds__(kVecThreads)
     xcopies_kernel(int64_t n, const double *__restrict__ x, const int8_t *__restrict__ colExp,
-                   float *__restrict__ x32, uint16_t *__restrict__ x16)
+                   float *__restrict__ x32, float *__restrict__ x16f)
 {
     for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n;
          j += (int64_t)gridDim.x * blockDim.x) {
         const double v = x[j];
         const float s = pow2f(colExp[j]);
         x32[j] = __fmul_rn(f32_from_f64_rn(v), s);
-        x16[j] = (uint16_t)(__float_as_uint(__fmul_rn(f32_from_bf16(bf16_from_f64_rn(v)), s)) >> 16);
+        x16f[j] = __fmul_rn(f32_from_bf16(bf16_from_f64_rn(v)), s);
     }
 }
 
@@ -235,25 +242,32 @@ cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
     }
 }
 
-int spmv_grid_for(int T, int sms)
+template <int T>
+static int grid_T(int sms)
 {
     int per = 0;
-    cudaError_t e;
-    switch (T) {
-    case 16: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_kernel<16, false, true>, kSpmvThreads, 0); break;
-    case 64: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_kernel<64, false, true>, kSpmvThreads, 0); break;
-    default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_kernel<32, false, true>, kSpmvThreads, 0); break;
-    }
-    if (e != cudaSuccess || per < 1) per = 2;
-    int g = sms * per;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_kernel<T, false, true>, kSpmvThreads, 0) !=
+            cudaSuccess || per < 1)
+        per = 1;
+    cudaGetLastError();
+    const int g = sms * per;
     return g > kMaxBlocks ? kMaxBlocks : g;
 }
 
-cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, uint16_t *x16,
+int spmv_grid_for(int T, int sms)
+{
+    switch (T) {
+    case 16: return grid_T<16>(sms);
+    case 64: return grid_T<64>(sms);
+    default: return grid_T<32>(sms);
+    }
+}
+
+cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, float *x16f,
                            int grid, cudaStream_t s)
 {
     if (A.n == 0) return cudaSuccess;
-    xcopies_kernel<<<grid, kVecThreads, 0, s>>>(A.n, x, A.colExp, x32, x16);
+    xcopies_kernel<<<grid, kVecThreads, 0, s>>>(A.n, x, A.colExp, x32, x16f);
     return cudaGetLastError();
 }
 

@@ -26,9 +26,9 @@ namespace evocg {
 
 void HostTiles::release()
 {
-    delete[] tileRowPtr; delete[] tileColIdx; delete[] tileNnzOff; delete[] rowEnd;
+    delete[] tileRowPtr; delete[] tileColIdx; delete[] tileNnzOff; delete[] tileRowIdx; delete[] rowEnd;
     delete[] colIdx; delete[] v64; delete[] v32; delete[] v16; delete[] colExp; delete[] dinv;
-    tileRowPtr = nullptr; tileColIdx = nullptr; tileNnzOff = nullptr; rowEnd = nullptr;
+    tileRowPtr = nullptr; tileColIdx = nullptr; tileNnzOff = nullptr; tileRowIdx = nullptr; rowEnd = nullptr;
     colIdx = nullptr; v64 = nullptr; v32 = nullptr; v16 = nullptr; colExp = nullptr;
     dinv = nullptr;
 }
@@ -143,6 +143,7 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
         const int64_t nt = H.ntiles;
         H.tileColIdx = new int32_t[(size_t)std::max<int64_t>(nt, 1)];
         H.tileNnzOff = new int64_t[(size_t)nt + 1];
+        H.tileRowIdx = new int32_t[(size_t)std::max<int64_t>(nt, 1)];
         H.rowEnd = new uint16_t[(size_t)std::max<int64_t>(nt * T, 1)];
         H.colIdx = new uint8_t[(size_t)std::max<int64_t>(nnz, 1)];
         H.v64 = new double[(size_t)std::max<int64_t>(nnz, 1)];
@@ -164,6 +165,7 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
                         if (cur[(size_t)r] < rp[r0 + r + 1]) cb = std::min(cb, ci[cur[(size_t)r]] / T);
                     H.tileColIdx[t] = cb;
                     H.tileNnzOff[t] = pos;
+                    H.tileRowIdx[t] = (int32_t)rb;
                     const int64_t base = pos;
                     for (int r = 0; r < T; ++r) {
                         if (r < nr) {
