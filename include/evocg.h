@@ -169,6 +169,25 @@ enum {
 int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int flags, void *stream);
 
 /*
+ * evocg_spmv without any memory allocation. The EvoCG paper has no counterpart: this entry
+ * point exists for callers that must not have the library allocate at call time (device
+ * allocation can synchronise the whole GPU, is not allowed while a stream is being captured
+ * into a graph, and is off limits to programs that hand out all device memory from their
+ * own pool or run under a fixed budget). It computes the same product as evocg_spmv, with
+ * the rounded copies of x kept in a fixed 8 MiB array that is part of the loaded library
+ * (reserved on every GPU that loads it, until the process exits) instead of library-owned
+ * buffers.
+ *   x, y: DEVICE pointers, n FP64 each, not overlapping. n must be at most 1,048,576
+ *   (EINVAL otherwise, with a message naming the limit).
+ * The first call on a device looks up that array's device address (cudaGetSymbolAddress),
+ * once per device; make that first call before any stream capture. Every call shares the
+ * one array and overwrites all of it that it reads, so no state carries over between calls,
+ * but calls that may overlap on the GPU (concurrent streams, or several handles at once)
+ * race on it: order them. Asynchronous on `stream`.
+ */
+int evocg_spmv_noalloc(evocg_tiles_t A, const double *x, double *y, void *stream);
+
+/*
  * CG (jacobi = 0) or Jacobi-preconditioned CG (jacobi = 1) for A x = b from x0 = 0, in
  * the order of EvoCG Algorithm 1 (the solver lines) and §4.6:
  *   controller on p_k when k % kstar == 0; q = A~ p; sigma = p.q (breakdown unless

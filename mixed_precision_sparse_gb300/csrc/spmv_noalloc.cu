@@ -1,0 +1,93 @@
+// spmv_noalloc.cu -- an SpMV entry point that never allocates memory.
+//
+// evocg_spmv keeps the FP32 and BF16 roundings of x in buffers the library allocates with
+// cudaMalloc. Some programs cannot let a library do that at call time: cudaMalloc may
+// synchronise the whole device, it is not allowed while a stream is being captured into
+// a graph, and services that own all device memory through their own pool (or that run
+// under a fixed memory budget) forbid allocations they did not plan. For those callers
+// this file holds the scratch in a fixed array that is part of the loaded module: it is
+// reserved once, when the library is loaded on a device, and never grows.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+
+#include "evocg_internal.h"
+
+namespace {
+
+// Largest x length the allocation-free SpMV accepts.
+constexpr int64_t kNoAllocMaxN = 1 << 20;
+
+// Scratch for the rounded copies of x: kNoAllocMaxN FP32 roundings followed by
+// kNoAllocMaxN BF16 roundings (held in FP32 containers). 8 MiB; every GPU that loads this
+// library holds it until the process exits. Host code must not take this name as a
+// device address: it only names the symbol for cudaGetSymbolAddress.
+static __device__ __align__(256) float g_noalloc_scratch[2 * kNoAllocMaxN];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+float *g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch on the current device, looked up once per device.
+int scratch_for_current_device(float **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return evocg::cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return evocg::fail(EVOCG_EDEVICE, "device index out of range");
+    std::lock_guard<std::mutex> lock(g_setup_mutex);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return evocg::cuda_fail(e, "cudaGetSymbolAddress (allocation-free SpMV scratch)");
+        g_scratch_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return EVOCG_OK;
+}
+
+}  // namespace
+
+extern "C" int evocg_spmv_noalloc(evocg_tiles_t A, const double *x, double *y, void *stream)
+{
+    evocg::set_error("");
+    if (!A || (A->n > 0 && (!x || !y))) return evocg::fail(EVOCG_EINVAL, "NULL argument");
+    if (A->n > kNoAllocMaxN)
+        return evocg::fail(EVOCG_EINVAL, "evocg_spmv_noalloc: n = " + std::to_string(A->n) +
+                                             " exceeds the fixed scratch of " +
+                                             std::to_string(kNoAllocMaxN) + " entries");
+    if (A->n == 0) return EVOCG_OK;
+    for (const void *p : {static_cast<const void *>(x), static_cast<const void *>(y)}) {
+        cudaPointerAttributes at;
+        cudaError_t e = cudaPointerGetAttributes(&at, p);
+        if (e != cudaSuccess || (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)) {
+            cudaGetLastError();
+            return evocg::fail(EVOCG_EINVAL, "evocg_spmv_noalloc needs device pointers for x and y");
+        }
+    }
+    float *scratch = nullptr;
+    int rc = scratch_for_current_device(&scratch);
+    if (rc) return rc;
+    float *x32 = scratch, *x16f = scratch + kNoAllocMaxN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // every entry of the copies below n is rewritten here, so nothing needs clearing
+    cudaError_t e = evocg::launch_xcopies(A->view(), x, x32, x16f, A->vec_grid, s);
+    if (e != cudaSuccess) return evocg::cuda_fail(e, "launch x copies (allocation-free)");
+    evocg::SpmvLaunch S{};
+    S.A = A->view();
+    S.x64 = x;
+    S.x32 = x32;
+    S.x16f = x16f;
+    S.y = y;
+    S.prec = (A->map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
+    S.map_kind = A->map_kind;
+    S.force64 = 0;
+    S.dot = 0;
+    S.st = nullptr;
+    S.census = 0;
+    S.grid = A->spmv_grid;
+    e = evocg::launch_spmv(S, s);
+    if (e != cudaSuccess) return evocg::cuda_fail(e, "launch spmv (allocation-free)");
+    return EVOCG_OK;
+}

@@ -93,6 +93,7 @@ def lib():
                 "evocg_get_tile_precision": [P, P, i64, P],
                 "evocg_spmv": [P, P, P, P],
                 "evocg_spmv_ex": [P, P, P, i32, P],
+                "evocg_spmv_noalloc": [P, P, P, P],
                 "evocg_cg_solve": [P, P, P, dbl, i32, i32, C.POINTER(Ctrl), i32, P,
                                    C.POINTER(SolveInfo), P],
                 "evocg_ctrl_decide": [P, C.POINTER(Ctrl), P, P, P, P],
@@ -220,6 +221,12 @@ SPMV_REUSE_XCOPIES = 1
 
 def spmv(A: Tiles, x, y, stream=None):
     _check(lib().evocg_spmv(A.h, _ptr(x), _ptr(y), _stream(stream)))
+    return y
+
+
+def spmv_noalloc(A: Tiles, x, y, stream=None):
+    """evocg_spmv_noalloc: the same product with no allocation (device x, y; n <= 2^20)."""
+    _check(lib().evocg_spmv_noalloc(A.h, _ptr(x), _ptr(y), _stream(stream)))
     return y
 
 
