@@ -1,0 +1,98 @@
+"""Run and time the mixed-precision SpMV alone on the synthetic workloads.
+
+    python -m mixed_precision_sparse_gb300.spmv_run [--workloads 2,3,5] [--reps 50]
+                                                    [--maps mixed,fp64] [--launches K]
+
+For each workload: build the tile structure, set the seeded 40/40/20 per-tile map (or the
+all-FP64 map), and launch the SpMV kernel back to back on device-resident x and y (every
+workload's matrix streams are larger than L2 except the 64 x 64 Laplacian's), timed with
+CUDA events on the launching stream. Prints one JSON line per (workload, map) with the
+microseconds per launch and the algorithmic bytes of the launch (the active value stream of
+each tile, the index bytes, x read once and y written once).
+
+`--launches K` skips the timing and issues exactly K SpMV launches after one x-copy launch,
+for use under a profiler.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+import numpy as np
+
+if __package__ in (None, ""):
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+from mixed_precision_sparse_gb300 import evocg  # noqa: E402
+from mixed_precision_sparse_gb300 import workloads as W  # noqa: E402
+
+
+def spmv_bytes(G, nnz_by_prec):
+    """Algorithmic bytes of one SpMV launch on handle G given the stored entries per
+    precision: the active value stream of every tile, the index arrays the kernel reads
+    (as reported by evocg_tiles_info, minus the export-only entry offsets), x read once and
+    y written once."""
+    d = G.info()
+    vals = 8 * int(nnz_by_prec[0]) + 4 * int(nnz_by_prec[1]) + 2 * int(nnz_by_prec[2])
+    return vals + int(d.bytes_index) + 16 * int(d.n)
+
+
+def main(argv=None):
+    import torch
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--workloads", default="2,3,5")
+    ap.add_argument("--maps", default="mixed,fp64")
+    ap.add_argument("--reps", type=int, default=50)
+    ap.add_argument("--launches", type=int, default=0)
+    a = ap.parse_args(argv)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    for cfg in [int(c) for c in a.workloads.split(",") if c]:
+        w = W.workload(cfg)
+        G = evocg.tile_build(w.n, w.rp, w.ci, w.v, w.T)
+        trow, ex = G.tile_rows()
+        tnnz = np.diff(ex["tileNnzOff"])
+        x = torch.from_numpy(np.random.default_rng(7).uniform(-1, 1, w.n)).to(dev)
+        y = torch.empty_like(x)
+        for label in a.maps.split(","):
+            if label == "mixed":
+                mp = W.tile_map(trow, ex["tileColIdx"], G.nrb, 12345)
+            elif label == "fp32":
+                mp = np.ones(G.ntiles, np.uint8)
+            elif label == "bf16":
+                mp = np.full(G.ntiles, 2, np.uint8)
+            else:
+                mp = np.zeros(G.ntiles, np.uint8)
+            evocg.set_tile_precision(G, mp)
+            evocg.spmv(G, x, y)
+            if a.launches:
+                for _ in range(a.launches):
+                    evocg.spmv_ex(G, x, y, evocg.SPMV_REUSE_XCOPIES)
+                torch.cuda.synchronize()
+                continue
+            for _ in range(5):
+                evocg.spmv_ex(G, x, y, evocg.SPMV_REUSE_XCOPIES)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(a.reps):
+                evocg.spmv_ex(G, x, y, evocg.SPMV_REUSE_XCOPIES)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1000.0 / a.reps
+            per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
+            B = spmv_bytes(G, per)
+            print(json.dumps({"workload": w.name, "map": label, "n": w.n, "nnz": w.nnz,
+                              "ntiles": int(G.ntiles), "us": round(us, 2), "bytes": B,
+                              "gbs": round(B / us / 1e3, 1)}), flush=True)
+        G.free()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
