@@ -129,7 +129,7 @@ def _traffic_for(kernel_src_hash):
 
 def _src_hash():
     h = hashlib.sha256()
-    for name in ("spmv.cu", "fpconv.cuh", "evocg_internal.h"):
+    for name in ("spmv.cu", "spmv_staged.cu", "staged_plan.cpp", "fpconv.cuh", "evocg_internal.h"):
         with open(os.path.join(ROOT, "mixed_precision_sparse_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -322,7 +322,7 @@ def run_ours(args):
     mixed = spmv["mixed_40_40_20"]
     roofline = {"bound": "hbm", "achieved": mixed["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": mixed["frac_of_peak"], "traffic": traffic,
-                "kernel": "spmv_kernel<32> (mixed 40/40/20 map)", "peak_kind": peak_kind,
+                "kernel": "spmv_staged_kernel<32> (bulk-copy staged, mixed 40/40/20 map)", "peak_kind": peak_kind,
                 "frac_of_8tbs": mixed["frac_of_8tbs"], "bytes_per_launch": mixed["bytes"],
                 "us_per_launch": mixed["us"], "fp64_map": spmv["fp64"]}
 

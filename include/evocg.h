@@ -155,9 +155,14 @@ int evocg_spmv(evocg_tiles_t A, const double *x, double *y, void *stream);
 
 /* Flags of evocg_spmv_ex. */
 enum {
-    EVOCG_SPMV_REUSE_XCOPIES = 1  /* skip rounding x: reuse the FP32/BF16 copies of x made by
+    EVOCG_SPMV_REUSE_XCOPIES = 1, /* skip rounding x: reuse the FP32/BF16 copies of x made by
                                      the previous evocg_spmv / evocg_spmv_ex call on this
                                      handle; x must hold the same values as in that call */
+    EVOCG_SPMV_DIRECT = 2         /* run the direct kernel (every operand read from global
+                                     memory by the lanes) instead of the staged one (operands
+                                     copied into shared memory by bulk asynchronous copies);
+                                     both compute the same sums in the same order. The staged
+                                     kernel is the default whenever x is 16-byte aligned */
 };
 
 /*

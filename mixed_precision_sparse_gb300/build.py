@@ -36,6 +36,10 @@ def _headers():
 def _stale(obj, src, deps):
     if not os.path.exists(obj):
         return True
+    stamp = obj + ".flags"
+    flags = os.environ.get("EVOCG_NVCC_FLAGS", "")
+    if not os.path.exists(stamp) or open(stamp).read() != flags:
+        return True
     t = os.path.getmtime(obj)
     return any(os.path.getmtime(d) > t for d in [src, *deps])
 
@@ -46,6 +50,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     deps = _headers()
     common = ["-std=c++17", "-O3", "-I", INC, "-I", CSRC, "-Xcompiler", "-fPIC"]
+    # extra nvcc flags (e.g. -D overrides of kernel tuning constants); part of the stamp
+    extra = os.environ.get("EVOCG_NVCC_FLAGS", "").split()
+    common += extra
     jobs = []
     objs = []
     for s in srcs:
@@ -72,6 +79,9 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
                 sys.stderr.write(" ".join(cmd) + "\n" + r.stdout + r.stderr)
             if r.returncode:
                 failed.append(cmd[-3])
+            else:
+                with open(cmd[-1] + ".flags", "w") as f:
+                    f.write(os.environ.get("EVOCG_NVCC_FLAGS", ""))
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
     if force or jobs or not os.path.exists(LIB):

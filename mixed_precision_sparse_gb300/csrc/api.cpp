@@ -318,6 +318,24 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     up(&A->v16, H.v16, H.nnz);
     up(&A->colExp, H.colExp, H.n);
     up(&A->dinv, H.dinv, H.n);
+    StagedLimits lim;
+    if (e == cudaSuccess && H.nrb > 0 && staged_limits(H.T, &lim)) {
+        const int grid = staged_grid_for(H.T, sms);
+        if (grid > 0) {
+            std::vector<int32_t> wr, wbt;
+            std::vector<int64_t> bt;
+            std::vector<uint16_t> slot;
+            staged_plan(H, (int64_t)grid * lim.warps_per_block, lim, &wr, &wbt, &bt, &slot);
+            up(&A->warpRb, wr.data(), (int64_t)wr.size());
+            up(&A->warpBatch, wbt.data(), (int64_t)wbt.size());
+            up(&A->batchTile, bt.data(), (int64_t)bt.size());
+            up(&A->tileSlot, slot.data(), (int64_t)slot.size());
+            A->nbatches = (int64_t)bt.size() - 1;
+            A->staged_grid = grid;
+        }
+    }
+    if (e == cudaSuccess) e = dalloc(&A->errw, 1);
+    if (e == cudaSuccess) e = cudaMemset(A->errw, 0, sizeof(int));
     H.release();
     if (e == cudaSuccess) e = dalloc(&A->tilePrec, A->ntiles);
     if (e == cudaSuccess) e = cudaMemset(A->tilePrec, 0, (size_t)(A->ntiles > 0 ? A->ntiles : 1));
@@ -343,7 +361,8 @@ extern "C" int evocg_tiles_free(evocg_tiles_t A)
     cudaDeviceSynchronize();
     release_ws(A->ws);
     dfree(A->tileRowPtr); dfree(A->tileColIdx); dfree(A->tileNnzOff); dfree(A->tileRowIdx);
-    dfree(A->rowEnd);
+    dfree(A->rowEnd); dfree(A->warpRb); dfree(A->warpBatch); dfree(A->batchTile);
+    dfree(A->tileSlot); dfree(A->errw);
     dfree(A->colIdx); dfree(A->v64); dfree(A->v32); dfree(A->v16); dfree(A->colExp);
     dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16f);
     dfree(A->xstage); dfree(A->ystage);
@@ -444,7 +463,7 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
 {
     g_err.clear();
     if (!A || (A->n > 0 && (!x || !y))) return fail(EVOCG_EINVAL, "NULL argument");
-    if (flags & ~EVOCG_SPMV_REUSE_XCOPIES) return fail(EVOCG_EINVAL, "unknown flags");
+    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT)) return fail(EVOCG_EINVAL, "unknown flags");
     if (A->n == 0) return EVOCG_OK;
     cudaStream_t s = (cudaStream_t)stream;
     const bool reuse = (flags & EVOCG_SPMV_REUSE_XCOPIES) != 0;
@@ -475,10 +494,18 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     S.prec = (A->map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
     S.map_kind = A->map_kind;
     S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
+    S.direct = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
     CK(launch_spmv(S, s), "launch spmv");
     if (!ydev) {
+        int lost = 0;
         CK(cudaMemcpyAsync(y, yd, bytes, cudaMemcpyDeviceToHost, s), "copy y");
+        CK(cudaMemcpyAsync(&lost, A->errw, sizeof(int), cudaMemcpyDeviceToHost, s), "read error word");
         CK(cudaStreamSynchronize(s), "synchronise");
+        if (lost) {
+            cudaMemsetAsync(A->errw, 0, sizeof(int), s);
+            cudaStreamSynchronize(s);
+            return fail(EVOCG_ETIMEOUT, "an SpMV stage wait ran out (bulk copies did not complete)");
+        }
     }
     return EVOCG_OK;
 }
@@ -651,6 +678,8 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
         if (H.converged && true_res > rtol && H.status == EVOCG_OK) H.status = EVOCG_ENOTCONV;
     }
     const int k = H.k;
+    int lost = 0;
+    CK(cudaMemcpyAsync(&lost, A->errw, sizeof(int), cudaMemcpyDeviceToHost, s), "read error word");
     if (n > 0) CK(cudaMemcpyAsync(x, w.x, bytes, cudaMemcpyDefault, s), "copy x");
     if (res_hist) CK(cudaMemcpyAsync(res_hist, w.hist, sizeof(double) * (size_t)(k + 1), cudaMemcpyDefault, s), "copy history");
     CK(cudaStreamSynchronize(s), "synchronise outputs");
@@ -665,6 +694,12 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
         info->prec_nnz[1] = (int64_t)H.census[1];
         info->prec_nnz[2] = (int64_t)H.census[2];
         info->ctrl_calls = (int64_t)H.ctrl_calls;
+    }
+    if (lost) {
+        cudaMemsetAsync(A->errw, 0, sizeof(int), s);
+        cudaStreamSynchronize(s);
+        return fail(EVOCG_ETIMEOUT, "an SpMV stage wait ran out (bulk copies did not complete); "
+                                    "the solve's results are not valid");
     }
     if (H.status == EVOCG_ENOTCONV) set_error("CG did not reach rtol within maxit");
     if (H.status == EVOCG_EBREAKDOWN) set_error("CG breakdown: p.Ap <= 0 or not finite");

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <string>
+#include <vector>
 
 #include "evocg.h"
 
@@ -56,7 +57,38 @@ struct TilesView {
     const float *v32;
     const uint16_t *v16;
     const int8_t *colExp;
+    // staged SpMV plan (NULL warpRb = direct kernel only): row-block range and batch range
+    // of every warp (warps + 1 entries each), first tile of every batch (batches + 1), the
+    // shared-memory slot of every tile inside its batch's stage (kDirectSlot: a tile too
+    // large for a stage), the staged grid, and the error word a lost stage wait sets
+    const int32_t *warpRb;
+    const int32_t *warpBatch;
+    const int64_t *batchTile;
+    const uint16_t *tileSlot;
+    int staged_grid;
+    int *err;
 };
+
+constexpr uint16_t kDirectSlot = 0xFFFF;
+
+// Capacities of one stage of the staged SpMV for tile size T (spmv_staged.cu).
+struct StagedLimits {
+    int warps_per_block;
+    int nb;          // tiles per batch
+    int col_bytes;   // local-column bytes
+    int data_bytes;  // value slices + x segments
+};
+bool staged_limits(int T, StagedLimits *out);
+
+// Worst-case stage bytes of a tile with m entries: the 16-byte cover of its value slice in
+// any precision (at most 8m + 8 bytes before rounding) followed by its x segment in FP64.
+#ifdef __CUDACC__
+__host__ __device__
+#endif
+inline int staged_slot_bytes(int64_t m, int T)
+{
+    return (int)(((8 * m + 8 + 15) / 16) * 16) + 8 * T;
+}
 
 struct SolveWS {
     int64_t cap_n = 0, cap_ncb = 0;
@@ -95,6 +127,13 @@ struct evocg_tiles {
     float *v32 = nullptr;
     uint16_t *v16 = nullptr;
     int8_t *colExp = nullptr;
+    int32_t *warpRb = nullptr;     // staged SpMV plan (see TilesView)
+    int32_t *warpBatch = nullptr;
+    int64_t *batchTile = nullptr;
+    uint16_t *tileSlot = nullptr;
+    int64_t nbatches = 0;
+    int staged_grid = 0;
+    int *errw = nullptr;           // device error word (a lost stage wait)
     uint8_t *tilePrec = nullptr;   // per-tile map
     uint8_t *cbPrec = nullptr;     // per-column-block map
     int map_kind = EVOCG_MAP_PER_TILE;
@@ -111,7 +150,8 @@ struct evocg_tiles {
     evocg::TilesView view() const
     {
         return evocg::TilesView{n, nrb, ntiles, T, tileRowPtr, tileColIdx, tileNnzOff, tileRowIdx,
-                                rowEnd, colIdx, v64, v32, v16, colExp};
+                                rowEnd, colIdx, v64, v32, v16, colExp, warpRb, warpBatch, batchTile,
+                                tileSlot, staged_grid, errw};
     }
 };
 
@@ -158,9 +198,20 @@ struct SpmvLaunch {
     double *partials;
     DevState *st;
     int census;            // accumulate per-precision entry counts into st->census
-    int grid;
+    int grid;              // grid of the direct kernel
+    int direct;            // 1: the direct kernel even when the staged one could run
 };
+// The staged kernel runs when the view has warp ranges and every x operand is 16-byte
+// aligned; otherwise the direct kernel.
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
+cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s);
+cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s);
+int staged_grid_for(int T, int sms);   // 0 if it cannot run
+
+// Host: the staged SpMV plan for `warps` warps (api.cpp).
+void staged_plan(const HostTiles &H, int64_t warps, const StagedLimits &lim,
+                 std::vector<int32_t> *warpRb, std::vector<int32_t> *warpBatch,
+                 std::vector<int64_t> *batchTile, std::vector<uint16_t> *tileSlot);
 cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, float *x16f,
                            int grid, cudaStream_t s);
 cudaError_t launch_round(const double *x, int64_t n, float *o32, uint16_t *o16, cudaStream_t s);

@@ -234,6 +234,18 @@ static cudaError_t launch_T(const SpmvLaunch &L, cudaStream_t s)
 
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
 {
+    const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!L.direct && L.A.warpRb && L.A.staged_grid > 0 && al(L.x64) &&
+        (L.force64 || (al(L.x32) && al(L.x16f)))) {
+        SpmvLaunch S = L;
+        S.grid = L.A.staged_grid;
+        return launch_spmv_staged(S, s);
+    }
+    return launch_spmv_direct(L, s);
+}
+
+cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s)
+{
     switch (L.A.T) {
     case 16: return launch_T<16>(L, s);
     case 32: return launch_T<32>(L, s);

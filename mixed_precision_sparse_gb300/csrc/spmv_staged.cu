@@ -1,0 +1,687 @@
+// spmv_staged.cu -- the tile-wise mixed-precision SpMV (EvoCG, "Self-Evolving Precision
+// Control for Faster Conjugate Gradient", §3.3 EvoSpMV, Eq. 2 / Eq. 5) with every operand
+// staged into shared memory by the Tensor Memory Accelerator, for sm_103a.
+//
+// Work mapping. Each warp owns a contiguous range of row blocks and walks their tiles in
+// order, in batches fixed at build time (a static plan: staged_plan.cpp). Lane l owns local
+// row l (rows l and l+32 for T = 64; lanes 16..31 idle in the arithmetic for T = 16) and
+// keeps its row sums in registers for the whole row block: no cross-lane reduction, so an
+// FP64 tile costs one FP64 fused multiply-add per entry and nothing more.
+//
+// Staging. A warp holds S stages of shared memory; every tile of a batch has a fixed slot
+// in its stage, sized for FP64. For a batch, lane j issues two bulk asynchronous copies for
+// tile j: the tile's slice of the value stream its precision selects (the 16-byte aligned
+// cover of the slice: the same 32-byte sectors a plain load would fetch) and the x segment
+// of the tile's column block in that precision; one lane copies the batch's row-end table
+// and local-column bytes, which are contiguous. Copies land on the stage's mbarrier with
+// their byte count; the warp computes batch b while batches b+1 .. b+S-1 are in flight. So
+// a warp keeps kilobytes of reads in flight for a few instructions per tile, instead of a
+// dependent chain of global loads per tile. Matrix streams are read with an evict-first L2
+// policy so that x, which every tile column re-reads, stays in L2.
+//
+// Tile descriptors are loaded two batches ahead and their precision resolved one batch
+// ahead, so the issue step never waits on memory. A tile too large for a stage is computed
+// from global memory directly. Every mbarrier wait is bounded: if it runs out, the kernel
+// records the event in an error word the host reads, stops staging and returns.
+//
+// Arithmetic is that of the direct kernel: FP32 and BF16 products exact in FP32 pairs
+// summed error-free, merged into the FP64 row sum once per row.
+#include <cuda_runtime.h>
+
+#include "evocg_internal.h"
+#include "fpconv.cuh"
+
+namespace evocg {
+
+namespace {
+
+// Per tile size: warps per block, stages per warp, tiles per batch, local-column bytes and
+// value + x bytes per stage, and the resident blocks per SM the registers are capped for.
+#ifndef EVOCG_ST32_NW
+#define EVOCG_ST32_NW 4
+#endif
+#ifndef EVOCG_ST32_S
+#define EVOCG_ST32_S 2
+#endif
+#ifndef EVOCG_ST32_NB
+#define EVOCG_ST32_NB 16
+#endif
+#ifndef EVOCG_ST32_CB
+#define EVOCG_ST32_CB 768
+#endif
+#ifndef EVOCG_ST32_DB
+#define EVOCG_ST32_DB 4864
+#endif
+#ifndef EVOCG_ST32_MINB
+#define EVOCG_ST32_MINB 4
+#endif
+template <int NW_, int S_, int NB_, int CB_, int DB_, int MINB_>
+struct StParams {
+    static constexpr int NW = NW_, S = S_, NB = NB_, CB = CB_, DB = DB_, MINB = MINB_;
+};
+template <int T>
+struct StCfg;
+template <>
+struct StCfg<16> : StParams<4, 3, 16, 640, 2560, 4> {};
+template <>
+struct StCfg<32> : StParams<EVOCG_ST32_NW, EVOCG_ST32_S, EVOCG_ST32_NB, EVOCG_ST32_CB,
+                             EVOCG_ST32_DB, EVOCG_ST32_MINB> {};
+template <>
+struct StCfg<64> : StParams<4, 2, 16, 1024, 8192, 2> {};
+
+// Stage layout (bytes from the stage base): header, per-tile info, row ends, local
+// columns, values + x segments.
+template <int T>
+struct StLayout {
+    using C = StCfg<T>;
+    static constexpr int HDR = 0;                        // int64 tb, int32 nb, int32 direct
+    static constexpr int INFO = 16;                      // NB x uint4
+    static constexpr int RE = INFO + 16 * C::NB;         // NB x T x uint16
+    static constexpr int COL = RE + 2 * T * C::NB;       // CB bytes
+    static constexpr int DATA = COL + C::CB;             // DB bytes
+    static constexpr int STAGE = (DATA + C::DB + 127) / 128 * 128;
+    static constexpr int BARS = (C::NW * C::S * 8 + 127) / 128 * 128;
+    static constexpr int SMEM = BARS + C::NW * C::S * STAGE;
+};
+
+template <int T>
+constexpr bool layout_ok()
+{
+    return StCfg<T>::S * StLayout<T>::STAGE <= 65536 && StCfg<T>::NB <= 32 &&
+           StLayout<T>::SMEM <= 227 * 1024;
+}
+static_assert(layout_ok<16>() && layout_ok<32>() && layout_ok<64>(), "stage layout");
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kWaitLimit = 1 << 24;   // try_wait polls before a stage wait is declared lost
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t tx)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tx)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
+{
+    for (int i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Global -> shared bulk copy completing on an mbarrier. dst, src 16-byte aligned, bytes a
+// positive multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes,
+                                              uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+// Last block of a grid (see the direct kernel): fixed-order sums of per-block partials.
+__device__ __forceinline__ bool st_last_block(DevState *st, int slot)
+{
+    __shared__ bool amLast;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned t = atomicAdd(&st->tickets[slot], 1u);
+        amLast = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (amLast) __threadfence();
+    return amLast;
+}
+
+__device__ __forceinline__ double st_block_sum(double v)
+{
+    __shared__ double ws[32];
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    __syncthreads();
+    if (l == 0) ws[w] = v;
+    __syncthreads();
+    double s = 0.0;
+    if (threadIdx.x == 0)
+        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += ws[i];
+    return s;
+}
+
+// Descriptors of the tiles of one batch, one tile per lane.
+struct Desc {
+    int64_t o0;   // first entry
+    int m;        // entries
+    int cb, rb;   // column block, row block
+    int slot;     // byte offset of the tile's slot in the stage's data area
+    int prec;     // precision code (resolved)
+};
+
+template <int T, bool FORCE64, bool DOT>
+__global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
+    spmv_staged_kernel(SpmvLaunch L)
+{
+    using C = StCfg<T>;
+    using Y = StLayout<T>;
+    constexpr int RPL = T > 32 ? 2 : 1;            // rows per lane
+    if (DOT && L.st->done) return;                  // a stopped solve: nothing to do
+    extern __shared__ __align__(128) unsigned char sm[];
+    const TilesView A = L.A;
+    const int lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int gw = blockIdx.x * C::NW + wib;
+    const bool rowlane = (T >= 32) || (lane < T);   // lanes that own a row
+    const uint32_t bar0 = smem_u32(sm) + 8u * (uint32_t)(wib * C::S);
+    const uint32_t wofs = (uint32_t)Y::BARS + (uint32_t)(wib * C::S * Y::STAGE);  // warp region
+    const uint32_t wsm_u32 = smem_u32(sm) + wofs;
+    const uint64_t pol = policy_evict_first();
+
+    if (lane == 0) {
+        for (int s = 0; s < C::S; ++s) mbar_init(bar0 + 8u * s, 1u);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int rbBeg = L.A.warpRb[gw], rbEnd = L.A.warpRb[gw + 1];
+    const int bBeg = L.A.warpBatch[gw], bEnd = L.A.warpBatch[gw + 1];
+    const int n = (int)A.n;
+    unsigned long long cnt0 = 0, cnt1 = 0, cnt2 = 0;
+
+    // batch boundaries, 32 at a time: lane j holds batchTile[bw + j]
+    int bw = bBeg;
+    int64_t bwin = (bw + lane <= bEnd) ? __ldg(A.batchTile + bw + lane) : 0;
+    auto bounds = [&](int b, int64_t &tb, int64_t &te) {
+        if (b + 1 - bw > 31) {
+            bw = b;
+            bwin = (bw + lane <= bEnd) ? __ldg(A.batchTile + bw + lane) : 0;
+        }
+        tb = __shfl_sync(kFull, bwin, b - bw);
+        te = __shfl_sync(kFull, bwin, b + 1 - bw);
+    };
+
+    // descriptor prefetch: raw for the batch two ahead, resolved for the batch one ahead
+    int64_t r_o0 = 0, r_o1 = 0;
+    int r_cb = 0, r_rb = 0, r_slot = 0, r_pt = 0, r_nb = 0;
+    int64_t r_tb = 0;
+    auto load_raw = [&](int b) {
+        if (b >= bEnd) { r_nb = 0; return; }
+        int64_t tb, te;
+        bounds(b, tb, te);
+        r_tb = tb;
+        r_nb = (int)(te - tb);
+        if (lane < r_nb) {
+            const int64_t t = tb + lane;
+            r_o0 = __ldg(A.tileNnzOff + t);
+            r_o1 = __ldg(A.tileNnzOff + t + 1);
+            r_cb = __ldg(A.tileColIdx + t);
+            r_rb = __ldg(A.tileRowIdx + t);
+            r_slot = __ldg(A.tileSlot + t);
+            r_pt = (!FORCE64 && L.map_kind == EVOCG_MAP_PER_TILE) ? (int)__ldg(L.prec + t) : 0;
+        }
+    };
+    Desc d;
+    int d_nb = 0;
+    int64_t d_tb = 0;
+    auto resolve = [&]() {   // d <- raw
+        d_nb = r_nb;
+        d_tb = r_tb;
+        d.o0 = r_o0; d.m = (int)(r_o1 - r_o0); d.cb = r_cb; d.rb = r_rb; d.slot = r_slot;
+        if (FORCE64) d.prec = 0;
+        else if (L.map_kind == EVOCG_MAP_PER_TILE) d.prec = r_pt;
+        else d.prec = (lane < r_nb) ? (int)__ldg(L.prec + r_cb) : 0;
+    };
+
+    // ---- issue batch b (descriptors in d) into stage st
+    auto issue = [&](int st) {
+        const uint32_t stg = wofs + (uint32_t)(st * Y::STAGE);      // offset in sm
+        const uint32_t bar = bar0 + 8u * st;
+        const int nb = d_nb;
+        const bool valid = lane < nb;
+        const int prec = d.prec;
+        const unsigned cm = valid ? (unsigned)d.m : 0u;
+        if (L.census) {
+            cnt0 += __reduce_add_sync(kFull, prec == 0 ? cm : 0u);
+            cnt1 += __reduce_add_sync(kFull, prec == 1 ? cm : 0u);
+            cnt2 += __reduce_add_sync(kFull, prec == 2 ? cm : 0u);
+        }
+        const bool direct = (nb == 1) && (__shfl_sync(kFull, d.slot, 0) == (int)kDirectSlot);
+        if (direct) {
+            if (lane == 0) {
+                *reinterpret_cast<int4 *>(sm + stg + Y::HDR) =
+                    make_int4((int)(d_tb & 0xffffffff), (int)(d_tb >> 32), 1, 1);
+                *reinterpret_cast<uint4 *>(sm + stg + Y::INFO) =
+                    make_uint4(0u, (uint32_t)d.rb, (uint32_t)prec << 16, (uint32_t)d.m);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar);
+            return;
+        }
+        const int vw = prec == 0 ? 8 : (prec == 1 ? 4 : 2);
+        const int xw = prec == 0 ? 8 : 4;
+        const int xb = T * xw;
+        const int64_t vbyte0 = d.o0 * vw;
+        const int64_t va0 = vbyte0 & ~(int64_t)15;
+        const int vb = (int)(((vbyte0 + (int64_t)d.m * vw + 15) & ~(int64_t)15) - va0);
+        const bool full_x = (d.cb + 1) * T <= n;
+        const int64_t colFirst = __shfl_sync(kFull, d.o0, 0) & ~(int64_t)15;
+        const int64_t lastEnd = __shfl_sync(kFull, d.o0 + d.m, nb - 1);
+        const int colBytes = (int)(((lastEnd + 15) & ~(int64_t)15) - colFirst);
+        const unsigned tx = __reduce_add_sync(kFull, valid ? (unsigned)(vb + (full_x ? xb : 0)) : 0u) +
+                            (unsigned)(colBytes + nb * 2 * T);
+        const uint32_t dOff = stg - wofs + Y::DATA + (uint32_t)d.slot;   // offset in the warp region
+        const uint32_t valS = dOff + (uint32_t)(vbyte0 - va0);
+        const uint32_t xS = dOff + (uint32_t)(staged_slot_bytes(d.m, T) - 8 * T);
+        const uint32_t colS = stg - wofs + Y::COL + (uint32_t)(d.o0 - colFirst);
+        if (valid) {
+            *reinterpret_cast<uint4 *>(sm + stg + Y::INFO + 16 * lane) =
+                make_uint4(valS | (xS << 16), (uint32_t)d.rb, colS | ((uint32_t)prec << 16),
+                           (uint32_t)d.m);
+            if (!full_x) {  // the last column block of a matrix with T not dividing n
+                const int xb0 = d.cb * T;
+                if (prec == 0) {
+                    double *dd = reinterpret_cast<double *>(sm + wofs + xS);
+                    for (int i = 0; i < T; ++i) dd[i] = (xb0 + i < n) ? __ldg(L.x64 + xb0 + i) : 0.0;
+                } else {
+                    const float *src = prec == 1 ? L.x32 : L.x16f;
+                    float *dd = reinterpret_cast<float *>(sm + wofs + xS);
+                    for (int i = 0; i < T; ++i) dd[i] = (xb0 + i < n) ? __ldg(src + xb0 + i) : 0.f;
+                }
+            }
+        }
+        if (lane == 0)
+            *reinterpret_cast<int4 *>(sm + stg + Y::HDR) =
+                make_int4((int)(d_tb & 0xffffffff), (int)(d_tb >> 32), nb, 0);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(bar, tx);
+        __syncwarp();
+        if (valid) {
+            const unsigned char *vsrc =
+                prec == 0 ? reinterpret_cast<const unsigned char *>(A.v64)
+                          : (prec == 1 ? reinterpret_cast<const unsigned char *>(A.v32)
+                                       : reinterpret_cast<const unsigned char *>(A.v16));
+            bulk_g2s_hint(wsm_u32 + dOff, vsrc + va0, (uint32_t)vb, bar, pol);
+            if (full_x) {
+                const unsigned char *xsrc =
+                    prec == 0 ? reinterpret_cast<const unsigned char *>(L.x64)
+                              : (prec == 1 ? reinterpret_cast<const unsigned char *>(L.x32)
+                                           : reinterpret_cast<const unsigned char *>(L.x16f));
+                bulk_g2s(wsm_u32 + xS, xsrc + (size_t)d.cb * T * xw, (uint32_t)xb, bar);
+            }
+        }
+        if (lane == 0) {
+            bulk_g2s_hint(wsm_u32 + (stg - wofs) + Y::COL, A.colIdx + colFirst, (uint32_t)colBytes, bar, pol);
+            bulk_g2s_hint(wsm_u32 + (stg - wofs) + Y::RE, A.rowEnd + d_tb * T, (uint32_t)(nb * 2 * T),
+                          bar, pol);
+        }
+    };
+
+    // ---- row accumulation state (flags uniform over the warp, sums per lane)
+    double acc64[RPL];
+    F32Pair accl[RPL];
+    double xrow[RPL];
+    bool any64 = false, anylow = false;
+    int cur_rb = rbBeg;
+    double dotp = 0.0;
+    auto start_rb = [&](int rb) {
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            acc64[q] = 0.0;
+            accl[q].hi = 0.f;
+            accl[q].lo = 0.f;
+            const int row = rb * T + lane + 32 * q;
+            xrow[q] = (DOT && rowlane && row < n) ? __ldg(L.x64 + row) : 0.0;
+        }
+        any64 = false;
+        anylow = false;
+    };
+    auto finish_rb = [&](int rb) {
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            const int row = rb * T + lane + 32 * q;
+            if (rowlane && row < n) {
+                double y = acc64[q];
+                if (anylow) {  // FP32 -> FP64 widening is exact
+                    const double dd = (double)accl[q].hi + (double)accl[q].lo;
+                    y = any64 ? y + dd : dd;
+                }
+                L.y[row] = y;
+                if (DOT) dotp = fma(xrow[q], y, dotp);
+            }
+        }
+    };
+    auto zero_rows = [&](int z0, int z1) {   // row blocks [z0, z1) have no tiles
+        for (int z = z0; z < z1; ++z)
+#pragma unroll
+            for (int q = 0; q < RPL; ++q) {
+                const int row = z * T + lane + 32 * q;
+                if (rowlane && row < n) L.y[row] = 0.0;
+            }
+    };
+    auto goto_rb = [&](int rb) {
+        if (rb == cur_rb) return;
+        finish_rb(cur_rb);
+        zero_rows(cur_rb + 1, rb);
+        cur_rb = rb;
+        start_rb(rb);
+    };
+    auto get_starts = [&](const int (&e)[RPL], int (&s)[RPL]) {
+        const int u1 = __shfl_up_sync(kFull, e[0], 1);
+        s[0] = lane ? u1 : 0;
+        if (RPL == 2) {
+            const int u2 = __shfl_up_sync(kFull, e[RPL - 1], 1);
+            const int l1 = __shfl_sync(kFull, e[0], 31);
+            s[RPL - 1] = lane ? u2 : l1;
+        }
+        if (!rowlane) s[0] = e[0];
+    };
+
+    // one tile's products for my rows, operands in the warp's shared memory. Every address
+    // is a 32-bit offset into the block's shared array. The entry loop runs the warp's
+    // largest row count with per-lane predication: no divergent loop per lane.
+    auto tile_staged = [&](uint4 inf, const int (&s)[RPL], const int (&e)[RPL]) {
+        const int prec = (int)((inf.z >> 16) & 3u);
+        const uint32_t colo = wofs + (inf.z & 0xffffu), valo = wofs + (inf.x & 0xffffu);
+        const uint32_t xo = wofs + (inf.x >> 16);
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            const int cnt = e[q] - s[q];
+            const int kmax = (int)__reduce_max_sync(kFull, (unsigned)cnt);
+            const uint32_t co = colo + (uint32_t)s[q];
+            if (prec == EVOCG_FP64) {
+                const uint32_t vo = valo + 8u * (uint32_t)s[q];
+                double a = acc64[q];
+#pragma unroll 1
+                for (int k = 0; k < kmax; ++k)
+                    if (k < cnt) {
+                        const uint32_t c = sm[co + k];
+                        a = fma(*reinterpret_cast<const double *>(sm + vo + 8u * k),
+                                *reinterpret_cast<const double *>(sm + xo + 8u * c), a);
+                    }
+                acc64[q] = a;
+            } else if (prec == EVOCG_FP32) {
+                const uint32_t vo = valo + 4u * (uint32_t)s[q];
+#pragma unroll 1
+                for (int k = 0; k < kmax; ++k)
+                    if (k < cnt) {
+                        const uint32_t c = sm[co + k];
+                        accl[q].add_prod(*reinterpret_cast<const float *>(sm + vo + 4u * k),
+                                         *reinterpret_cast<const float *>(sm + xo + 4u * c));
+                    }
+            } else {
+                const uint32_t vo = valo + 2u * (uint32_t)s[q];
+#pragma unroll 1
+                for (int k = 0; k < kmax; ++k)  // BF16 x BF16 is exact in FP32
+                    if (k < cnt) {
+                        const uint32_t c = sm[co + k];
+                        const uint16_t h = *reinterpret_cast<const uint16_t *>(sm + vo + 2u * k);
+                        accl[q].add(__fmul_rn(f32_from_bf16(h),
+                                              *reinterpret_cast<const float *>(sm + xo + 4u * c)));
+                    }
+            }
+        }
+        if (prec == EVOCG_FP64) any64 = true; else anylow = true;
+    };
+
+    // one tile's products straight from global memory (a tile larger than a stage)
+    auto tile_direct = [&](int64_t t, int prec) {
+        const int64_t off = __ldg(A.tileNnzOff + t);
+        const int xb0 = __ldg(A.tileColIdx + t) * T;
+        const uint16_t *re = A.rowEnd + t * T;
+        const uint8_t *ci = A.colIdx + off;
+        int e[RPL], s[RPL];
+        e[0] = rowlane ? (int)__ldg(re + lane) : 0;
+        if (RPL == 2) e[RPL - 1] = (int)__ldg(re + lane + 32);
+        get_starts(e, s);
+#pragma unroll
+        for (int q = 0; q < RPL; ++q) {
+            for (int k = s[q]; k < e[q]; ++k) {
+                const int jx = xb0 + __ldg(ci + k);
+                if (prec == EVOCG_FP64) acc64[q] = fma(__ldg(A.v64 + off + k), __ldg(L.x64 + jx), acc64[q]);
+                else if (prec == EVOCG_FP32) accl[q].add_prod(__ldg(A.v32 + off + k), __ldg(L.x32 + jx));
+                else accl[q].add(__fmul_rn(f32_from_bf16(__ldg(A.v16 + off + k)), __ldg(L.x16f + jx)));
+            }
+        }
+        if (prec == EVOCG_FP64) any64 = true; else anylow = true;
+    };
+
+    // ---- pipeline: S batches in flight, compute the oldest, refill its stage
+    if (rbBeg < rbEnd) {
+        start_rb(rbBeg);
+        const int nbat = bEnd - bBeg;
+        load_raw(bBeg);
+        resolve();
+        load_raw(bBeg + 1);
+        int issued = 0;
+        for (int st = 0; st < C::S && issued < nbat; ++st) {
+            issue(st);
+            ++issued;
+            resolve();
+            load_raw(bBeg + issued + 1);
+        }
+        bool lost = false;
+        for (int b = 0; b < nbat; ++b) {
+            const int st = b % C::S;
+            if (!mbar_wait_bounded(bar0 + 8u * st, (uint32_t)((b / C::S) & 1))) {
+                lost = true;
+                if (lane == 0 && L.A.err) atomicExch(L.A.err, 1);
+                // let the copies still in flight land before the block exits
+                for (int b2 = b + 1; b2 < issued; ++b2)
+                    mbar_wait_bounded(bar0 + 8u * (b2 % C::S), (uint32_t)((b2 / C::S) & 1));
+                break;
+            }
+            const uint32_t stg = wofs + (uint32_t)(st * Y::STAGE);
+            const int4 h = *reinterpret_cast<const int4 *>(sm + stg + Y::HDR);
+            const uint32_t info = stg + Y::INFO;
+            if (h.w) {  // one tile too large for a stage
+                const int64_t tb = (int64_t)(uint32_t)h.x | ((int64_t)h.y << 32);
+                const uint4 inf = *reinterpret_cast<const uint4 *>(sm + info);
+                goto_rb((int)inf.y);
+                tile_direct(tb, (int)((inf.z >> 16) & 3u));
+            } else {
+                const int nb = h.z;
+                const uint32_t re = stg + Y::RE + 2u * (uint32_t)lane;   // my row's entry
+                uint4 inf = *reinterpret_cast<const uint4 *>(sm + info);
+                int e[RPL], s[RPL];
+                e[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re) : 0;
+                if (RPL == 2) e[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 64u);
+                for (int jt = 0; jt < nb; ++jt) {
+                    // the next tile's descriptor and row ends load while this one computes
+                    uint4 infn = inf;
+                    int en[RPL];
+#pragma unroll
+                    for (int q = 0; q < RPL; ++q) en[q] = 0;
+                    if (jt + 1 < nb) {
+                        const uint32_t jn = (uint32_t)(jt + 1);
+                        infn = *reinterpret_cast<const uint4 *>(sm + info + 16u * jn);
+                        en[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn) : 0;
+                        if (RPL == 2)
+                            en[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn + 64u);
+                    }
+                    get_starts(e, s);
+                    goto_rb((int)inf.y);
+                    tile_staged(inf, s, e);
+                    inf = infn;
+#pragma unroll
+                    for (int q = 0; q < RPL; ++q) e[q] = en[q];
+                }
+            }
+            __syncwarp();
+            if (issued < nbat) {
+                issue(st);
+                ++issued;
+                resolve();
+                load_raw(bBeg + issued + 1);
+            }
+        }
+        if (!lost) {
+            finish_rb(cur_rb);
+            zero_rows(cur_rb + 1, rbEnd);
+        }
+    }
+
+    if (L.census && lane == 0) {
+        if (cnt0) atomicAdd(&L.st->census[0], cnt0);
+        if (cnt1) atomicAdd(&L.st->census[1], cnt1);
+        if (cnt2) atomicAdd(&L.st->census[2], cnt2);
+    }
+    if (DOT) {
+        DevState *st = L.st;
+        const double sd = st_block_sum(dotp);
+        if (threadIdx.x == 0) L.partials[blockIdx.x] = sd;
+        if (st_last_block(st, TK_SPMV)) {
+            double v = 0.0;
+            for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) v += __ldcg(L.partials + i);
+            const double sigma = st_block_sum(v);
+            if (threadIdx.x == 0) {
+                st->tickets[TK_SPMV] = 0;
+                if (!st->done) {
+                    if (!(sigma > 0.0) || !isfinite(sigma)) {
+                        st->status = EVOCG_EBREAKDOWN;
+                        st->done = 1;
+                    } else {
+                        st->sigma = sigma;
+                        st->alpha = st->rho / sigma;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int T>
+cudaError_t staged_T(const SpmvLaunch &L, cudaStream_t s)
+{
+    constexpr int threads = StCfg<T>::NW * 32;
+    constexpr int smem = StLayout<T>::SMEM;
+    if (L.force64) {
+        if (L.dot) spmv_staged_kernel<T, true, true><<<L.grid, threads, smem, s>>>(L);
+        else spmv_staged_kernel<T, true, false><<<L.grid, threads, smem, s>>>(L);
+    } else {
+        if (L.dot) spmv_staged_kernel<T, false, true><<<L.grid, threads, smem, s>>>(L);
+        else spmv_staged_kernel<T, false, false><<<L.grid, threads, smem, s>>>(L);
+    }
+    return cudaGetLastError();
+}
+
+template <int T>
+int staged_grid_T(int sms)
+{
+    constexpr int threads = StCfg<T>::NW * 32;
+    constexpr int smem = StLayout<T>::SMEM;
+    const void *ks[4] = {(const void *)spmv_staged_kernel<T, true, true>,
+                         (const void *)spmv_staged_kernel<T, true, false>,
+                         (const void *)spmv_staged_kernel<T, false, true>,
+                         (const void *)spmv_staged_kernel<T, false, false>};
+    for (const void *k : ks)
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+    int per = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_staged_kernel<T, false, true>,
+                                                      threads, smem) != cudaSuccess || per < 1) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int g = sms * per;
+    return g > kMaxBlocks ? kMaxBlocks : g;
+}
+
+template <int T>
+void limits_T(StagedLimits *o)
+{
+    o->warps_per_block = StCfg<T>::NW;
+    o->nb = StCfg<T>::NB;
+    o->col_bytes = StCfg<T>::CB;
+    o->data_bytes = StCfg<T>::DB;
+}
+
+}  // namespace
+
+cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s)
+{
+    switch (L.A.T) {
+    case 16: return staged_T<16>(L, s);
+    case 32: return staged_T<32>(L, s);
+    case 64: return staged_T<64>(L, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+int staged_grid_for(int T, int sms)
+{
+    switch (T) {
+    case 16: return staged_grid_T<16>(sms);
+    case 32: return staged_grid_T<32>(sms);
+    case 64: return staged_grid_T<64>(sms);
+    default: return 0;
+    }
+}
+
+bool staged_limits(int T, StagedLimits *out)
+{
+    switch (T) {
+    case 16: limits_T<16>(out); return true;
+    case 32: limits_T<32>(out); return true;
+    case 64: limits_T<64>(out); return true;
+    default: return false;
+    }
+}
+
+}  // namespace evocg

@@ -217,6 +217,7 @@ def get_tile_precision(A: Tiles, stream=None):
 
 
 SPMV_REUSE_XCOPIES = 1
+SPMV_DIRECT = 2
 
 
 def spmv(A: Tiles, x, y, stream=None):

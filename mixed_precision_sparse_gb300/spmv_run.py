@@ -47,6 +47,8 @@ def main(argv=None):
     ap.add_argument("--maps", default="mixed,fp64")
     ap.add_argument("--reps", type=int, default=50)
     ap.add_argument("--launches", type=int, default=0)
+    ap.add_argument("--direct", action="store_true",
+                    help="time the direct kernel instead of the staged one")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -69,25 +71,27 @@ def main(argv=None):
                 mp = np.zeros(G.ntiles, np.uint8)
             evocg.set_tile_precision(G, mp)
             evocg.spmv(G, x, y)
+            flags = evocg.SPMV_REUSE_XCOPIES | (evocg.SPMV_DIRECT if a.direct else 0)
             if a.launches:
                 for _ in range(a.launches):
-                    evocg.spmv_ex(G, x, y, evocg.SPMV_REUSE_XCOPIES)
+                    evocg.spmv_ex(G, x, y, flags)
                 torch.cuda.synchronize()
                 continue
             for _ in range(5):
-                evocg.spmv_ex(G, x, y, evocg.SPMV_REUSE_XCOPIES)
+                evocg.spmv_ex(G, x, y, flags)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
             e0.record(stream)
             for _ in range(a.reps):
-                evocg.spmv_ex(G, x, y, evocg.SPMV_REUSE_XCOPIES)
+                evocg.spmv_ex(G, x, y, flags)
             e1.record(stream)
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1000.0 / a.reps
             per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
             B = spmv_bytes(G, per)
-            print(json.dumps({"workload": w.name, "map": label, "n": w.n, "nnz": w.nnz,
+            print(json.dumps({"workload": w.name, "map": label,
+                              "kernel": "direct" if a.direct else "staged", "n": w.n, "nnz": w.nnz,
                               "ntiles": int(G.ntiles), "us": round(us, 2), "bytes": B,
                               "gbs": round(B / us / 1e3, 1)}), flush=True)
         G.free()

@@ -172,3 +172,51 @@ def test_spmv_parity_full_size(cfg):
     x = np.random.default_rng(cfg).uniform(-1, 1, P.n)
     _check_spmv(P, None, x, TOL64)
     _check_spmv(P, P.tile_map(cfg), x, TOLMIX)
+
+
+@pytest.mark.parametrize("name,m,T", CASES + [
+    ("dense_t32", W.dense_to_csr(np.random.default_rng(0).standard_normal((100, 100)) + 200 * np.eye(100)), 32),
+    ("dense_t64", W.dense_to_csr(np.random.default_rng(1).standard_normal((200, 200)) + 300 * np.eye(200)), 64),
+], ids=[c[0] for c in CASES] + ["dense_t32", "dense_t64"])
+def test_spmv_staged_equals_direct(name, m, T):
+    """The staged kernel (operands copied to shared memory by bulk asynchronous copies) and
+    the direct kernel sum the same products in the same order for T >= 32: identical bits.
+    For T = 16 the direct kernel gives alternate tiles of a row block to the two half-warps
+    and merges them at the end, so the two agree to rounding only. Dense tiles exercise the
+    path for tiles larger than a stage; n not a multiple of T the partial last x segment."""
+    P = Pair(m, T)
+    rng = np.random.default_rng(5)
+    x = torch.from_numpy(rng.uniform(-1, 1, P.n) * 10.0 ** rng.uniform(-3, 3, P.n)).cuda()
+    for mp in (np.zeros(P.t.ntiles, np.uint8), P.tile_map(1), P.tile_map(2, (0, 0, 1)), P.tile_map(3, (0, 1, 0))):
+        evocg.set_tile_precision(P.G, mp)
+        ys = torch.full((P.n,), np.nan, dtype=torch.float64, device="cuda")
+        yd = torch.full((P.n,), np.nan, dtype=torch.float64, device="cuda")
+        evocg.spmv(P.G, x, ys)
+        evocg.spmv_ex(P.G, x, yd, evocg.SPMV_REUSE_XCOPIES | evocg.SPMV_DIRECT)
+        torch.cuda.synchronize()
+        want = oracle.mixed_spmv(P.A, P.t, mp, x.cpu().numpy())
+        if T >= 32:
+            assert torch.equal(ys.view(torch.int64), yd.view(torch.int64))
+        else:
+            e2 = row_rel_err(ys.cpu().numpy(), yd.cpu().numpy(), P.abs_sum(mp, x.cpu().numpy()))
+            assert e2.max() <= 1e-12
+        err = row_rel_err(ys.cpu().numpy(), want, P.abs_sum(mp, x.cpu().numpy()))
+        assert err.max() <= (TOL64 if not mp.any() else TOLMIX)
+
+
+def test_spmv_misaligned_x_uses_direct_kernel():
+    """An x that is not 16-byte aligned cannot be a bulk-copy source: the library runs the
+    direct kernel and the result is unchanged."""
+    P = Pair(W.diffusion3d_7pt(16, 2), 32)
+    mp = P.tile_map(4)
+    evocg.set_tile_precision(P.G, mp)
+    buf = torch.from_numpy(np.random.default_rng(9).standard_normal(P.n + 1)).cuda()
+    xa = buf[1:]                       # 8 bytes past a 256-byte boundary
+    xb = buf[1:].clone()               # aligned copy of the same values
+    assert xa.data_ptr() % 16 == 8 and xb.data_ptr() % 16 == 0
+    ya = torch.empty(P.n, dtype=torch.float64, device="cuda")
+    yb = torch.empty_like(ya)
+    evocg.spmv(P.G, xa, ya)
+    evocg.spmv(P.G, xb, yb)
+    torch.cuda.synchronize()
+    assert torch.equal(ya.view(torch.int64), yb.view(torch.int64))
