@@ -291,6 +291,21 @@ def run_ours(args):
     h2d = 8 * w.n
     d2h = 8 * w.n + 8 * (e2e_infos[-1]["iters"] + 1)
 
+    # ---- the same solve with every tile in FP64 and no controller (the all-FP64 GPU path the
+    # mixed-precision solve is compared with), outside the timed region
+    evocg.set_tile_precision(G, np.zeros(G.ntiles, np.uint8))
+    fp64_info = evocg.cg_solve(G, b, x, w.rtol, w.maxit, w.jacobi, None, True, hist)
+    torch.cuda.synchronize()
+    fp64_steps = max(1, min(args.steps, 3))
+    e0.record(stream)
+    for _ in range(fp64_steps):
+        fp64_info = evocg.cg_solve(G, b, x, w.rtol, w.maxit, w.jacobi, None, True, hist)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    fp64_s = e0.elapsed_time(e1) / 1000.0 / fp64_steps
+    fp64_solve = {"s": fp64_s, "iters": fp64_info["iters"], "true_res": fp64_info["true_res"],
+                  "mixed_over_fp64": value * world / fp64_s}
+
     # ---- the dominant kernel (the SpMV) timed alone on the same stream, CUDA events,
     # back-to-back launches (inputs > L2), with the seeded 40/40/20 mixed map and all-FP64
     trow, ex = G.tile_rows()
@@ -350,6 +365,7 @@ def run_ours(args):
                       "prec_nnz": info["prec_nnz"], "ctrl_calls": info["ctrl_calls"],
                       "status": info["status"], "tile_build_s": build_s,
                       "s_per_iter": value / max(1, info["iters"]) * world},
+            "fp64_solve": fp64_solve,
             "clocks": clk.summary(),
             "e2e": {"value": e2e_ms / 1000.0 / world, "unit": "s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

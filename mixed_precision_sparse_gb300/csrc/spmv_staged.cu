@@ -80,7 +80,8 @@ struct StLayout {
     static constexpr int COL = RE + 2 * T * C::NB;       // CB bytes
     static constexpr int DATA = COL + C::CB;             // DB bytes
     static constexpr int STAGE = (DATA + C::DB + 127) / 128 * 128;
-    static constexpr int BARS = (C::NW * C::S * 8 + 127) / 128 * 128;
+    static constexpr int TABS = C::NW * C::S * 8;                     // per-warp source tables
+    static constexpr int BARS = (TABS + C::NW * 64 + 127) / 128 * 128;
     static constexpr int SMEM = BARS + C::NW * C::S * STAGE;
 };
 
@@ -205,7 +206,7 @@ __device__ __forceinline__ double st_block_sum(double v)
 
 // Descriptors of the tiles of one batch, one tile per lane.
 struct Desc {
-    int64_t o0;   // first entry
+    uint32_t o0;  // first entry, relative to the warp's first entry
     int m;        // entries
     int cb, rb;   // column block, row block
     int slot;     // byte offset of the tile's slot in the stage's data area
@@ -242,6 +243,28 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
     const int n = (int)A.n;
     unsigned long long cnt0 = 0, cnt1 = 0, cnt2 = 0;
 
+    // entry offsets inside the warp are 32-bit, relative to the warp's first entry (the plan
+    // keeps every warp's entry range below 2^28); the value and x sources by precision code
+    // sit in a small per-warp table in shared memory
+    // (the base is rounded down to a multiple of 16 entries, so that the bases of the local
+    // column bytes and of every value stream stay 16-byte aligned for the bulk copies)
+    const int64_t wE0 = rbBeg < rbEnd ? (__ldg(A.tileNnzOff + A.tileRowPtr[rbBeg]) & ~(int64_t)15) : 0;
+    const uint32_t tab = (uint32_t)Y::TABS + 64u * (uint32_t)wib;
+    if (lane < 6) {
+        const unsigned char *src;
+        switch (lane) {
+        case 0: src = reinterpret_cast<const unsigned char *>(A.v64 + wE0); break;
+        case 1: src = reinterpret_cast<const unsigned char *>(A.v32 + wE0); break;
+        case 2: src = reinterpret_cast<const unsigned char *>(A.v16 + wE0); break;
+        case 3: src = reinterpret_cast<const unsigned char *>(L.x64); break;
+        case 4: src = reinterpret_cast<const unsigned char *>(L.x32); break;
+        default: src = reinterpret_cast<const unsigned char *>(L.x16f); break;
+        }
+        *reinterpret_cast<const unsigned char **>(sm + tab + 8u * lane) = src;
+    }
+    __syncwarp();
+    const uint8_t *colBase = A.colIdx + wE0;
+
     // batch boundaries, 32 at a time: lane j holds batchTile[bw + j]
     int bw = bBeg;
     int64_t bwin = (bw + lane <= bEnd) ? __ldg(A.batchTile + bw + lane) : 0;
@@ -255,7 +278,7 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
     };
 
     // descriptor prefetch: raw for the batch two ahead, resolved for the batch one ahead
-    int64_t r_o0 = 0, r_o1 = 0;
+    uint32_t r_o0 = 0, r_o1 = 0;
     int r_cb = 0, r_rb = 0, r_slot = 0, r_pt = 0, r_nb = 0;
     int64_t r_tb = 0;
     auto load_raw = [&](int b) {
@@ -266,8 +289,8 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
         r_nb = (int)(te - tb);
         if (lane < r_nb) {
             const int64_t t = tb + lane;
-            r_o0 = __ldg(A.tileNnzOff + t);
-            r_o1 = __ldg(A.tileNnzOff + t + 1);
+            r_o0 = (uint32_t)(__ldg(A.tileNnzOff + t) - wE0);
+            r_o1 = (uint32_t)(__ldg(A.tileNnzOff + t + 1) - wE0);
             r_cb = __ldg(A.tileColIdx + t);
             r_rb = __ldg(A.tileRowIdx + t);
             r_slot = __ldg(A.tileSlot + t);
@@ -311,16 +334,16 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
             if (lane == 0) mbar_arrive(bar);
             return;
         }
-        const int vw = prec == 0 ? 8 : (prec == 1 ? 4 : 2);
+        const int vsh = prec == 0 ? 3 : (prec == 1 ? 2 : 1);       // log2 of the value width
         const int xw = prec == 0 ? 8 : 4;
         const int xb = T * xw;
-        const int64_t vbyte0 = d.o0 * vw;
-        const int64_t va0 = vbyte0 & ~(int64_t)15;
-        const int vb = (int)(((vbyte0 + (int64_t)d.m * vw + 15) & ~(int64_t)15) - va0);
+        const uint32_t vbyte0 = d.o0 << vsh;
+        const uint32_t va0 = vbyte0 & ~15u;
+        const int vb = (int)(((vbyte0 + ((uint32_t)d.m << vsh) + 15u) & ~15u) - va0);
         const bool full_x = (d.cb + 1) * T <= n;
-        const int64_t colFirst = __shfl_sync(kFull, d.o0, 0) & ~(int64_t)15;
-        const int64_t lastEnd = __shfl_sync(kFull, d.o0 + d.m, nb - 1);
-        const int colBytes = (int)(((lastEnd + 15) & ~(int64_t)15) - colFirst);
+        const uint32_t colFirst = __shfl_sync(kFull, d.o0, 0) & ~15u;
+        const uint32_t lastEnd = __shfl_sync(kFull, d.o0 + (uint32_t)d.m, nb - 1);
+        const int colBytes = (int)(((lastEnd + 15u) & ~15u) - colFirst);
         const unsigned tx = __reduce_add_sync(kFull, valid ? (unsigned)(vb + (full_x ? xb : 0)) : 0u) +
                             (unsigned)(colBytes + nb * 2 * T);
         const uint32_t dOff = stg - wofs + Y::DATA + (uint32_t)d.slot;   // offset in the warp region
@@ -351,21 +374,16 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
         if (lane == 0) mbar_arrive_expect_tx(bar, tx);
         __syncwarp();
         if (valid) {
-            const unsigned char *vsrc =
-                prec == 0 ? reinterpret_cast<const unsigned char *>(A.v64)
-                          : (prec == 1 ? reinterpret_cast<const unsigned char *>(A.v32)
-                                       : reinterpret_cast<const unsigned char *>(A.v16));
+            const unsigned char *vsrc = *reinterpret_cast<const unsigned char *const *>(sm + tab + 8u * prec);
             bulk_g2s_hint(wsm_u32 + dOff, vsrc + va0, (uint32_t)vb, bar, pol);
             if (full_x) {
                 const unsigned char *xsrc =
-                    prec == 0 ? reinterpret_cast<const unsigned char *>(L.x64)
-                              : (prec == 1 ? reinterpret_cast<const unsigned char *>(L.x32)
-                                           : reinterpret_cast<const unsigned char *>(L.x16f));
-                bulk_g2s(wsm_u32 + xS, xsrc + (size_t)d.cb * T * xw, (uint32_t)xb, bar);
+                    *reinterpret_cast<const unsigned char *const *>(sm + tab + 24u + 8u * prec);
+                bulk_g2s(wsm_u32 + xS, xsrc + (size_t)d.cb * (size_t)xb, (uint32_t)xb, bar);
             }
         }
         if (lane == 0) {
-            bulk_g2s_hint(wsm_u32 + (stg - wofs) + Y::COL, A.colIdx + colFirst, (uint32_t)colBytes, bar, pol);
+            bulk_g2s_hint(wsm_u32 + (stg - wofs) + Y::COL, colBase + colFirst, (uint32_t)colBytes, bar, pol);
             bulk_g2s_hint(wsm_u32 + (stg - wofs) + Y::RE, A.rowEnd + d_tb * T, (uint32_t)(nb * 2 * T),
                           bar, pol);
         }
@@ -446,13 +464,21 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
             if (prec == EVOCG_FP64) {
                 const uint32_t vo = valo + 8u * (uint32_t)s[q];
                 double a = acc64[q];
-#pragma unroll 1
-                for (int k = 0; k < kmax; ++k)
-                    if (k < cnt) {
-                        const uint32_t c = sm[co + k];
-                        a = fma(*reinterpret_cast<const double *>(sm + vo + 8u * k),
+                if (kmax == 1) {   // at most one entry per row: the common stencil tile
+                    if (cnt) {
+                        const uint32_t c = sm[co];
+                        a = fma(*reinterpret_cast<const double *>(sm + vo),
                                 *reinterpret_cast<const double *>(sm + xo + 8u * c), a);
                     }
+                } else {
+#pragma unroll 1
+                    for (int k = 0; k < kmax; ++k)
+                        if (k < cnt) {
+                            const uint32_t c = sm[co + k];
+                            a = fma(*reinterpret_cast<const double *>(sm + vo + 8u * k),
+                                    *reinterpret_cast<const double *>(sm + xo + 8u * c), a);
+                        }
+                }
                 acc64[q] = a;
             } else if (prec == EVOCG_FP32) {
                 const uint32_t vo = valo + 4u * (uint32_t)s[q];
