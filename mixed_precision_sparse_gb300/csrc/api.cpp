@@ -318,8 +318,13 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     up(&A->v16, H.v16, H.nnz);
     up(&A->colExp, H.colExp, H.n);
     up(&A->dinv, H.dinv, H.n);
+    // The staged kernel pays a fixed issue cost per batch of tiles and stages each tile's
+    // whole x segment; for sparse tiles (banded matrices: a handful of entries per 64 x 64
+    // tile) the direct kernel is faster, so the staged plan is built only when tiles hold
+    // on average at least kStagedMinEntries entries.
+    constexpr int64_t kStagedMinEntries = 12;
     StagedLimits lim;
-    if (e == cudaSuccess && H.nrb > 0 && staged_limits(H.T, &lim)) {
+    if (e == cudaSuccess && H.nrb > 0 && H.nnz >= kStagedMinEntries * H.ntiles && staged_limits(H.T, &lim)) {
         const int grid = staged_grid_for(H.T, sms);
         if (grid > 0) {
             std::vector<int32_t> wr, wbt;

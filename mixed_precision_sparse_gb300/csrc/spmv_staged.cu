@@ -35,42 +35,31 @@ namespace evocg {
 
 namespace {
 
-// Per tile size: warps per block, stages per warp, tiles per batch, local-column bytes and
-// value + x bytes per stage, and the resident blocks per SM the registers are capped for.
-#ifndef EVOCG_ST32_NW
-#define EVOCG_ST32_NW 4
-#endif
-#ifndef EVOCG_ST32_S
-#define EVOCG_ST32_S 2
-#endif
-#ifndef EVOCG_ST32_NB
-#define EVOCG_ST32_NB 16
-#endif
-#ifndef EVOCG_ST32_CB
-#define EVOCG_ST32_CB 768
-#endif
-#ifndef EVOCG_ST32_DB
-#define EVOCG_ST32_DB 4864
-#endif
-#ifndef EVOCG_ST32_MINB
-#define EVOCG_ST32_MINB 4
-#endif
-template <int NW_, int S_, int NB_, int CB_, int DB_, int MINB_>
+// Per tile size: consumer warps per block (plus one producer warp), stages per consumer,
+// tiles per consumer batch (NC * NB <= 32: a producer round covers one batch of every
+// consumer, one tile per lane), local-column bytes and value + x bytes per stage, and the
+// resident blocks per SM the registers are capped for.
+template <int NC_, int S_, int NB_, int CB_, int DB_, int MINB_>
 struct StParams {
-    static constexpr int NW = NW_, S = S_, NB = NB_, CB = CB_, DB = DB_, MINB = MINB_;
+    static constexpr int NC = NC_, S = S_, NB = NB_, CB = CB_, DB = DB_, MINB = MINB_;
+    static constexpr int NW = NC;        // plan warps per block (the consumers)
+    static constexpr int THREADS = (NC + 1) * 32;
 };
 template <int T>
 struct StCfg;
 template <>
-struct StCfg<16> : StParams<4, 3, 16, 640, 2560, 4> {};
+struct StCfg<16> : StParams<4, 3, 8, 512, 2560, 4> {};
+#ifndef EVOCG_ST32
+#define EVOCG_ST32 2, 2, 16, 768, 4096, 8
+#endif
 template <>
-struct StCfg<32> : StParams<EVOCG_ST32_NW, EVOCG_ST32_S, EVOCG_ST32_NB, EVOCG_ST32_CB,
-                             EVOCG_ST32_DB, EVOCG_ST32_MINB> {};
+struct StCfg<32> : StParams<EVOCG_ST32> {};
 template <>
-struct StCfg<64> : StParams<4, 2, 16, 1024, 8192, 2> {};
+struct StCfg<64> : StParams<4, 2, 8, 1024, 8192, 2> {};
 
 // Stage layout (bytes from the stage base): header, per-tile info, row ends, local
-// columns, values + x segments.
+// columns, values + x segments. Block layout: full and empty mbarriers of every consumer
+// stage, then each consumer's S stages.
 template <int T>
 struct StLayout {
     using C = StCfg<T>;
@@ -80,16 +69,15 @@ struct StLayout {
     static constexpr int COL = RE + 2 * T * C::NB;       // CB bytes
     static constexpr int DATA = COL + C::CB;             // DB bytes
     static constexpr int STAGE = (DATA + C::DB + 127) / 128 * 128;
-    static constexpr int TABS = C::NW * C::S * 8;                     // per-warp source tables
-    static constexpr int BARS = (TABS + C::NW * 64 + 127) / 128 * 128;
-    static constexpr int SMEM = BARS + C::NW * C::S * STAGE;
+    static constexpr int BARS = (2 * C::NC * C::S * 8 + 127) / 128 * 128;
+    static constexpr int SMEM = BARS + C::NC * C::S * STAGE;
 };
 
 template <int T>
 constexpr bool layout_ok()
 {
-    return StCfg<T>::S * StLayout<T>::STAGE <= 65536 && StCfg<T>::NB <= 32 &&
-           StLayout<T>::SMEM <= 227 * 1024;
+    return StCfg<T>::S * StLayout<T>::STAGE <= 65536 && StCfg<T>::NC * StCfg<T>::NB <= 32 &&
+           32 % StCfg<T>::NC == 0 && StCfg<T>::NB <= 32 / StCfg<T>::NC && StLayout<T>::SMEM <= 227 * 1024;
 }
 static_assert(layout_ok<16>() && layout_ok<32>() && layout_ok<64>(), "stage layout");
 
@@ -204,404 +192,366 @@ __device__ __forceinline__ double st_block_sum(double v)
     return s;
 }
 
-// Descriptors of the tiles of one batch, one tile per lane.
-struct Desc {
-    uint32_t o0;  // first entry, relative to the warp's first entry
-    int m;        // entries
-    int cb, rb;   // column block, row block
-    int slot;     // byte offset of the tile's slot in the stage's data area
-    int prec;     // precision code (resolved)
-};
-
 template <int T, bool FORCE64, bool DOT>
-__global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
+__global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
     spmv_staged_kernel(SpmvLaunch L)
 {
     using C = StCfg<T>;
     using Y = StLayout<T>;
-    constexpr int RPL = T > 32 ? 2 : 1;            // rows per lane
+    constexpr int RPL = T > 32 ? 2 : 1;            // rows per lane (consumers)
+    constexpr int G = 32 / C::NC;                   // producer lanes per consumer
     if (DOT && L.st->done) return;                  // a stopped solve: nothing to do
     extern __shared__ __align__(128) unsigned char sm[];
     const TilesView A = L.A;
     const int lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    const int gw = blockIdx.x * C::NW + wib;
-    const bool rowlane = (T >= 32) || (lane < T);   // lanes that own a row
-    const uint32_t bar0 = smem_u32(sm) + 8u * (uint32_t)(wib * C::S);
-    const uint32_t wofs = (uint32_t)Y::BARS + (uint32_t)(wib * C::S * Y::STAGE);  // warp region
-    const uint32_t wsm_u32 = smem_u32(sm) + wofs;
-    const uint64_t pol = policy_evict_first();
+    const uint32_t sbase = smem_u32(sm);
+    // full[c][s]: the stage's copies landed (producer arrival + bytes); empty[c][s]: the
+    // consumer finished reading the stage
+    auto full_bar = [&](int c, int st) { return sbase + 8u * (uint32_t)(c * C::S + st); };
+    auto empty_bar = [&](int c, int st) { return sbase + 8u * (uint32_t)((C::NC + c) * C::S + st); };
+    auto region = [&](int c) { return (uint32_t)Y::BARS + (uint32_t)(c * C::S * Y::STAGE); };
 
-    if (lane == 0) {
-        for (int s = 0; s < C::S; ++s) mbar_init(bar0 + 8u * s, 1u);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2 * C::NC * C::S; ++i) mbar_init(sbase + 8u * i, 1u);
         fence_mbar_init();
     }
-    __syncwarp();
+    __syncthreads();
 
-    const int rbBeg = L.A.warpRb[gw], rbEnd = L.A.warpRb[gw + 1];
-    const int bBeg = L.A.warpBatch[gw], bEnd = L.A.warpBatch[gw + 1];
     const int n = (int)A.n;
+    double dotp = 0.0;
     unsigned long long cnt0 = 0, cnt1 = 0, cnt2 = 0;
 
-    // entry offsets inside the warp are 32-bit, relative to the warp's first entry (the plan
-    // keeps every warp's entry range below 2^28); the value and x sources by precision code
-    // sit in a small per-warp table in shared memory
-    // (the base is rounded down to a multiple of 16 entries, so that the bases of the local
-    // column bytes and of every value stream stay 16-byte aligned for the bulk copies)
-    const int64_t wE0 = rbBeg < rbEnd ? (__ldg(A.tileNnzOff + A.tileRowPtr[rbBeg]) & ~(int64_t)15) : 0;
-    const uint32_t tab = (uint32_t)Y::TABS + 64u * (uint32_t)wib;
-    if (lane < 6) {
-        const unsigned char *src;
-        switch (lane) {
-        case 0: src = reinterpret_cast<const unsigned char *>(A.v64 + wE0); break;
-        case 1: src = reinterpret_cast<const unsigned char *>(A.v32 + wE0); break;
-        case 2: src = reinterpret_cast<const unsigned char *>(A.v16 + wE0); break;
-        case 3: src = reinterpret_cast<const unsigned char *>(L.x64); break;
-        case 4: src = reinterpret_cast<const unsigned char *>(L.x32); break;
-        default: src = reinterpret_cast<const unsigned char *>(L.x16f); break;
-        }
-        *reinterpret_cast<const unsigned char **>(sm + tab + 8u * lane) = src;
-    }
-    __syncwarp();
-    const uint8_t *colBase = A.colIdx + wE0;
+    if (wib == C::NC) {
+        // =============================== producer ===============================
+        // Lane l serves consumer c = l / G, tile i = l % G of that consumer's current batch.
+        const uint64_t pol = policy_evict_first();
+        const int c = lane / G, i = lane % G;
+        const int gw = blockIdx.x * C::NC + c;
+        const int bBeg = A.warpBatch[gw], bEnd = A.warpBatch[gw + 1];
+        int rounds = bEnd - bBeg;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
+        const uint32_t wreg = region(c);
 
-    // batch boundaries, 32 at a time: lane j holds batchTile[bw + j]
-    int bw = bBeg;
-    int64_t bwin = (bw + lane <= bEnd) ? __ldg(A.batchTile + bw + lane) : 0;
-    auto bounds = [&](int b, int64_t &tb, int64_t &te) {
-        if (b + 1 - bw > 31) {
-            bw = b;
-            bwin = (bw + lane <= bEnd) ? __ldg(A.batchTile + bw + lane) : 0;
-        }
-        tb = __shfl_sync(kFull, bwin, b - bw);
-        te = __shfl_sync(kFull, bwin, b + 1 - bw);
-    };
-
-    // descriptor prefetch: raw for the batch two ahead, resolved for the batch one ahead
-    uint32_t r_o0 = 0, r_o1 = 0;
-    int r_cb = 0, r_rb = 0, r_slot = 0, r_pt = 0, r_nb = 0;
-    int64_t r_tb = 0;
-    auto load_raw = [&](int b) {
-        if (b >= bEnd) { r_nb = 0; return; }
-        int64_t tb, te;
-        bounds(b, tb, te);
-        r_tb = tb;
-        r_nb = (int)(te - tb);
-        if (lane < r_nb) {
-            const int64_t t = tb + lane;
-            r_o0 = (uint32_t)(__ldg(A.tileNnzOff + t) - wE0);
-            r_o1 = (uint32_t)(__ldg(A.tileNnzOff + t + 1) - wE0);
-            r_cb = __ldg(A.tileColIdx + t);
-            r_rb = __ldg(A.tileRowIdx + t);
-            r_slot = __ldg(A.tileSlot + t);
-            r_pt = (!FORCE64 && L.map_kind == EVOCG_MAP_PER_TILE) ? (int)__ldg(L.prec + t) : 0;
-        }
-    };
-    Desc d;
-    int d_nb = 0;
-    int64_t d_tb = 0;
-    auto resolve = [&]() {   // d <- raw
-        d_nb = r_nb;
-        d_tb = r_tb;
-        d.o0 = r_o0; d.m = (int)(r_o1 - r_o0); d.cb = r_cb; d.rb = r_rb; d.slot = r_slot;
-        if (FORCE64) d.prec = 0;
-        else if (L.map_kind == EVOCG_MAP_PER_TILE) d.prec = r_pt;
-        else d.prec = (lane < r_nb) ? (int)__ldg(L.prec + r_cb) : 0;
-    };
-
-    // ---- issue batch b (descriptors in d) into stage st
-    auto issue = [&](int st) {
-        const uint32_t stg = wofs + (uint32_t)(st * Y::STAGE);      // offset in sm
-        const uint32_t bar = bar0 + 8u * st;
-        const int nb = d_nb;
-        const bool valid = lane < nb;
-        const int prec = d.prec;
-        const unsigned cm = valid ? (unsigned)d.m : 0u;
-        if (L.census) {
-            cnt0 += __reduce_add_sync(kFull, prec == 0 ? cm : 0u);
-            cnt1 += __reduce_add_sync(kFull, prec == 1 ? cm : 0u);
-            cnt2 += __reduce_add_sync(kFull, prec == 2 ? cm : 0u);
-        }
-        const bool direct = (nb == 1) && (__shfl_sync(kFull, d.slot, 0) == (int)kDirectSlot);
-        if (direct) {
-            if (lane == 0) {
-                *reinterpret_cast<int4 *>(sm + stg + Y::HDR) =
-                    make_int4((int)(d_tb & 0xffffffff), (int)(d_tb >> 32), 1, 1);
-                *reinterpret_cast<uint4 *>(sm + stg + Y::INFO) =
-                    make_uint4(0u, (uint32_t)d.rb, (uint32_t)prec << 16, (uint32_t)d.m);
+        // raw descriptors of round r (loaded one round ahead)
+        int64_t r_o0 = 0, r_o1 = 0, r_tb = 0;
+        int r_cb = 0, r_rb = 0, r_slot = 0, r_pt = 0, r_nb = 0;
+        auto load_raw = [&](int r) {
+            const int bb = bBeg + r;
+            r_nb = 0;
+            if (bb < bEnd) {
+                r_tb = __ldg(A.batchTile + bb);
+                r_nb = (int)(__ldg(A.batchTile + bb + 1) - r_tb);
+                if (i < r_nb) {
+                    const int64_t t = r_tb + i;
+                    r_o0 = __ldg(A.tileNnzOff + t);
+                    r_o1 = __ldg(A.tileNnzOff + t + 1);
+                    r_cb = __ldg(A.tileColIdx + t);
+                    r_rb = __ldg(A.tileRowIdx + t);
+                    r_slot = __ldg(A.tileSlot + t);
+                    r_pt = (!FORCE64 && L.map_kind == EVOCG_MAP_PER_TILE) ? (int)__ldg(L.prec + t) : 0;
+                }
+            }
+        };
+        load_raw(0);
+        bool lost = false;
+        for (int r = 0; r < rounds && !lost; ++r) {
+            const int st = r % C::S;
+            // this round's descriptors, and the next round's raw loads in flight
+            const int nb = r_nb;
+            const int64_t tb = r_tb, o0 = r_o0;
+            const int m = (int)(r_o1 - r_o0), cb = r_cb, rb = r_rb, slot = r_slot;
+            const bool valid = i < nb;
+            int prec = 0;
+            if (!FORCE64) prec = (L.map_kind == EVOCG_MAP_PER_TILE) ? r_pt : (valid ? (int)__ldg(L.prec + cb) : 0);
+            load_raw(r + 1);
+            // wait until each consumer has released the stage this round refills
+            bool timedout = false;
+            if (r >= C::S && i == 0 && nb > 0)
+                timedout = !mbar_wait_bounded(empty_bar(c, st), (uint32_t)(((r / C::S) - 1) & 1));
+            if (__any_sync(kFull, timedout)) {   // a consumer stopped: issue nothing more
+                if (lane == 0 && A.err) atomicExch(A.err, 1);
+                lost = true;
+                break;
+            }
+            fence_proxy_async();
+            if (L.census) {
+                const unsigned cm = valid ? (unsigned)m : 0u;
+                cnt0 += __reduce_add_sync(kFull, prec == 0 ? cm : 0u);
+                cnt1 += __reduce_add_sync(kFull, prec == 1 ? cm : 0u);
+                cnt2 += __reduce_add_sync(kFull, prec == 2 ? cm : 0u);
+            }
+            const uint32_t stg = wreg + (uint32_t)(st * Y::STAGE);     // consumer stage in sm
+            const uint32_t srel = stg - wreg;                             // ... in its region
+            const int slot0 = __shfl_sync(kFull, slot, 0, G);   // every lane takes part
+            const bool direct = (nb == 1) && (slot0 == (int)kDirectSlot);
+            const int vw = prec == 0 ? 8 : (prec == 1 ? 4 : 2);
+            const int xw = prec == 0 ? 8 : 4;
+            const int xb = T * xw;
+            const int64_t vbyte0 = o0 * vw;
+            const int64_t va0 = vbyte0 & ~(int64_t)15;
+            const int vb = (int)(((vbyte0 + (int64_t)m * vw + 15) & ~(int64_t)15) - va0);
+            const bool full_x = (cb + 1) * T <= n;
+            const int64_t colFirst = __shfl_sync(kFull, o0, 0, G) & ~(int64_t)15;
+            const int64_t lastEnd = __shfl_sync(kFull, o0 + m, nb > 0 ? nb - 1 : 0, G);
+            const int colBytes = (int)(((lastEnd + 15) & ~(int64_t)15) - colFirst);
+            int txl = (valid && !direct) ? vb + (full_x ? xb : 0) : 0;
+#pragma unroll
+            for (int o = G / 2; o; o >>= 1) txl += __shfl_xor_sync(kFull, txl, o, G);
+            const uint32_t dOff = srel + Y::DATA + (uint32_t)slot;
+            const uint32_t valS = dOff + (uint32_t)(vbyte0 - va0);
+            const uint32_t xS = dOff + (uint32_t)(staged_slot_bytes(m, T) - 8 * T);
+            const uint32_t colS = srel + Y::COL + (uint32_t)(o0 - colFirst);
+            if (valid) {
+                if (direct) {
+                    *reinterpret_cast<int4 *>(sm + stg + Y::HDR) =
+                        make_int4((int)(tb & 0xffffffff), (int)(tb >> 32), 1, 1);
+                    *reinterpret_cast<uint4 *>(sm + stg + Y::INFO) =
+                        make_uint4(0u, (uint32_t)rb, (uint32_t)prec << 16, (uint32_t)m);
+                } else {
+                    *reinterpret_cast<uint4 *>(sm + stg + Y::INFO + 16 * i) =
+                        make_uint4(valS | (xS << 16), (uint32_t)rb, colS | ((uint32_t)prec << 16),
+                                   (uint32_t)m);
+                    if (!full_x) {  // the last column block of a matrix with T not dividing n
+                        const int xb0 = cb * T;
+                        if (prec == 0) {
+                            double *dd = reinterpret_cast<double *>(sm + wreg + xS);
+                            for (int k = 0; k < T; ++k) dd[k] = (xb0 + k < n) ? __ldg(L.x64 + xb0 + k) : 0.0;
+                        } else {
+                            const float *src = prec == 1 ? L.x32 : L.x16f;
+                            float *dd = reinterpret_cast<float *>(sm + wreg + xS);
+                            for (int k = 0; k < T; ++k) dd[k] = (xb0 + k < n) ? __ldg(src + xb0 + k) : 0.f;
+                        }
+                    }
+                    if (i == 0)
+                        *reinterpret_cast<int4 *>(sm + stg + Y::HDR) =
+                            make_int4((int)(tb & 0xffffffff), (int)(tb >> 32), nb, 0);
+                }
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (i == 0 && nb > 0) {
+                if (direct) mbar_arrive(full_bar(c, st));
+                else mbar_arrive_expect_tx(full_bar(c, st), (uint32_t)(txl + colBytes + nb * 2 * T));
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar);
-            return;
-        }
-        const int vsh = prec == 0 ? 3 : (prec == 1 ? 2 : 1);       // log2 of the value width
-        const int xw = prec == 0 ? 8 : 4;
-        const int xb = T * xw;
-        const uint32_t vbyte0 = d.o0 << vsh;
-        const uint32_t va0 = vbyte0 & ~15u;
-        const int vb = (int)(((vbyte0 + ((uint32_t)d.m << vsh) + 15u) & ~15u) - va0);
-        const bool full_x = (d.cb + 1) * T <= n;
-        const uint32_t colFirst = __shfl_sync(kFull, d.o0, 0) & ~15u;
-        const uint32_t lastEnd = __shfl_sync(kFull, d.o0 + (uint32_t)d.m, nb - 1);
-        const int colBytes = (int)(((lastEnd + 15u) & ~15u) - colFirst);
-        const unsigned tx = __reduce_add_sync(kFull, valid ? (unsigned)(vb + (full_x ? xb : 0)) : 0u) +
-                            (unsigned)(colBytes + nb * 2 * T);
-        const uint32_t dOff = stg - wofs + Y::DATA + (uint32_t)d.slot;   // offset in the warp region
-        const uint32_t valS = dOff + (uint32_t)(vbyte0 - va0);
-        const uint32_t xS = dOff + (uint32_t)(staged_slot_bytes(d.m, T) - 8 * T);
-        const uint32_t colS = stg - wofs + Y::COL + (uint32_t)(d.o0 - colFirst);
-        if (valid) {
-            *reinterpret_cast<uint4 *>(sm + stg + Y::INFO + 16 * lane) =
-                make_uint4(valS | (xS << 16), (uint32_t)d.rb, colS | ((uint32_t)prec << 16),
-                           (uint32_t)d.m);
-            if (!full_x) {  // the last column block of a matrix with T not dividing n
-                const int xb0 = d.cb * T;
-                if (prec == 0) {
-                    double *dd = reinterpret_cast<double *>(sm + wofs + xS);
-                    for (int i = 0; i < T; ++i) dd[i] = (xb0 + i < n) ? __ldg(L.x64 + xb0 + i) : 0.0;
-                } else {
-                    const float *src = prec == 1 ? L.x32 : L.x16f;
-                    float *dd = reinterpret_cast<float *>(sm + wofs + xS);
-                    for (int i = 0; i < T; ++i) dd[i] = (xb0 + i < n) ? __ldg(src + xb0 + i) : 0.f;
+            if (valid && !direct) {
+                const unsigned char *vsrc =
+                    prec == 0 ? reinterpret_cast<const unsigned char *>(A.v64)
+                              : (prec == 1 ? reinterpret_cast<const unsigned char *>(A.v32)
+                                           : reinterpret_cast<const unsigned char *>(A.v16));
+                bulk_g2s_hint(sbase + wreg + dOff, vsrc + va0, (uint32_t)vb, full_bar(c, st), pol);
+                if (full_x) {
+                    const unsigned char *xsrc =
+                        prec == 0 ? reinterpret_cast<const unsigned char *>(L.x64)
+                                  : (prec == 1 ? reinterpret_cast<const unsigned char *>(L.x32)
+                                               : reinterpret_cast<const unsigned char *>(L.x16f));
+                    bulk_g2s(sbase + wreg + xS, xsrc + (size_t)cb * (size_t)xb, (uint32_t)xb, full_bar(c, st));
+                }
+                if (i == 0) {
+                    bulk_g2s_hint(sbase + stg + Y::COL, A.colIdx + colFirst, (uint32_t)colBytes, full_bar(c, st), pol);
+                    bulk_g2s_hint(sbase + stg + Y::RE, A.rowEnd + tb * T, (uint32_t)(nb * 2 * T), full_bar(c, st), pol);
                 }
             }
         }
-        if (lane == 0)
-            *reinterpret_cast<int4 *>(sm + stg + Y::HDR) =
-                make_int4((int)(d_tb & 0xffffffff), (int)(d_tb >> 32), nb, 0);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar, tx);
-        __syncwarp();
-        if (valid) {
-            const unsigned char *vsrc = *reinterpret_cast<const unsigned char *const *>(sm + tab + 8u * prec);
-            bulk_g2s_hint(wsm_u32 + dOff, vsrc + va0, (uint32_t)vb, bar, pol);
-            if (full_x) {
-                const unsigned char *xsrc =
-                    *reinterpret_cast<const unsigned char *const *>(sm + tab + 24u + 8u * prec);
-                bulk_g2s(wsm_u32 + xS, xsrc + (size_t)d.cb * (size_t)xb, (uint32_t)xb, bar);
-            }
-        }
-        if (lane == 0) {
-            bulk_g2s_hint(wsm_u32 + (stg - wofs) + Y::COL, colBase + colFirst, (uint32_t)colBytes, bar, pol);
-            bulk_g2s_hint(wsm_u32 + (stg - wofs) + Y::RE, A.rowEnd + d_tb * T, (uint32_t)(nb * 2 * T),
-                          bar, pol);
-        }
-    };
+    } else {
+        // =============================== consumer ===============================
+        const int gw = blockIdx.x * C::NC + wib;
+        const bool rowlane = (T >= 32) || (lane < T);   // lanes that own a row
+        const uint32_t wofs = region(wib);
+        const int rbBeg = A.warpRb[gw], rbEnd = A.warpRb[gw + 1];
+        const int nbat = A.warpBatch[gw + 1] - A.warpBatch[gw];
 
-    // ---- row accumulation state (flags uniform over the warp, sums per lane)
-    double acc64[RPL];
-    F32Pair accl[RPL];
-    double xrow[RPL];
-    bool any64 = false, anylow = false;
-    int cur_rb = rbBeg;
-    double dotp = 0.0;
-    auto start_rb = [&](int rb) {
-#pragma unroll
-        for (int q = 0; q < RPL; ++q) {
-            acc64[q] = 0.0;
-            accl[q].hi = 0.f;
-            accl[q].lo = 0.f;
-            const int row = rb * T + lane + 32 * q;
-            xrow[q] = (DOT && rowlane && row < n) ? __ldg(L.x64 + row) : 0.0;
-        }
-        any64 = false;
-        anylow = false;
-    };
-    auto finish_rb = [&](int rb) {
-#pragma unroll
-        for (int q = 0; q < RPL; ++q) {
-            const int row = rb * T + lane + 32 * q;
-            if (rowlane && row < n) {
-                double y = acc64[q];
-                if (anylow) {  // FP32 -> FP64 widening is exact
-                    const double dd = (double)accl[q].hi + (double)accl[q].lo;
-                    y = any64 ? y + dd : dd;
-                }
-                L.y[row] = y;
-                if (DOT) dotp = fma(xrow[q], y, dotp);
-            }
-        }
-    };
-    auto zero_rows = [&](int z0, int z1) {   // row blocks [z0, z1) have no tiles
-        for (int z = z0; z < z1; ++z)
+        double acc64[RPL];
+        F32Pair accl[RPL];
+        double xrow[RPL];
+        bool any64 = false, anylow = false;
+        int cur_rb = rbBeg;
+        auto start_rb = [&](int rb) {
 #pragma unroll
             for (int q = 0; q < RPL; ++q) {
-                const int row = z * T + lane + 32 * q;
-                if (rowlane && row < n) L.y[row] = 0.0;
+                acc64[q] = 0.0;
+                accl[q].hi = 0.f;
+                accl[q].lo = 0.f;
+                const int row = rb * T + lane + 32 * q;
+                xrow[q] = (DOT && rowlane && row < n) ? __ldg(L.x64 + row) : 0.0;
             }
-    };
-    auto goto_rb = [&](int rb) {
-        if (rb == cur_rb) return;
-        finish_rb(cur_rb);
-        zero_rows(cur_rb + 1, rb);
-        cur_rb = rb;
-        start_rb(rb);
-    };
-    auto get_starts = [&](const int (&e)[RPL], int (&s)[RPL]) {
-        const int u1 = __shfl_up_sync(kFull, e[0], 1);
-        s[0] = lane ? u1 : 0;
-        if (RPL == 2) {
-            const int u2 = __shfl_up_sync(kFull, e[RPL - 1], 1);
-            const int l1 = __shfl_sync(kFull, e[0], 31);
-            s[RPL - 1] = lane ? u2 : l1;
-        }
-        if (!rowlane) s[0] = e[0];
-    };
-
-    // one tile's products for my rows, operands in the warp's shared memory. Every address
-    // is a 32-bit offset into the block's shared array. The entry loop runs the warp's
-    // largest row count with per-lane predication: no divergent loop per lane.
-    auto tile_staged = [&](uint4 inf, const int (&s)[RPL], const int (&e)[RPL]) {
-        const int prec = (int)((inf.z >> 16) & 3u);
-        const uint32_t colo = wofs + (inf.z & 0xffffu), valo = wofs + (inf.x & 0xffffu);
-        const uint32_t xo = wofs + (inf.x >> 16);
+            any64 = false;
+            anylow = false;
+        };
+        auto finish_rb = [&](int rb) {
 #pragma unroll
-        for (int q = 0; q < RPL; ++q) {
-            const int cnt = e[q] - s[q];
-            const int kmax = (int)__reduce_max_sync(kFull, (unsigned)cnt);
-            const uint32_t co = colo + (uint32_t)s[q];
-            if (prec == EVOCG_FP64) {
-                const uint32_t vo = valo + 8u * (uint32_t)s[q];
-                double a = acc64[q];
-                if (kmax == 1) {   // at most one entry per row: the common stencil tile
-                    if (cnt) {
-                        const uint32_t c = sm[co];
-                        a = fma(*reinterpret_cast<const double *>(sm + vo),
-                                *reinterpret_cast<const double *>(sm + xo + 8u * c), a);
+            for (int q = 0; q < RPL; ++q) {
+                const int row = rb * T + lane + 32 * q;
+                if (rowlane && row < n) {
+                    double y = acc64[q];
+                    if (anylow) {  // FP32 -> FP64 widening is exact
+                        const double dd = (double)accl[q].hi + (double)accl[q].lo;
+                        y = any64 ? y + dd : dd;
                     }
-                } else {
+                    L.y[row] = y;
+                    if (DOT) dotp = fma(xrow[q], y, dotp);
+                }
+            }
+        };
+        auto zero_rows = [&](int z0, int z1) {   // row blocks [z0, z1) have no tiles
+            for (int z = z0; z < z1; ++z)
+#pragma unroll
+                for (int q = 0; q < RPL; ++q) {
+                    const int row = z * T + lane + 32 * q;
+                    if (rowlane && row < n) L.y[row] = 0.0;
+                }
+        };
+        auto goto_rb = [&](int rb) {
+            if (rb == cur_rb) return;
+            finish_rb(cur_rb);
+            zero_rows(cur_rb + 1, rb);
+            cur_rb = rb;
+            start_rb(rb);
+        };
+        auto get_starts = [&](const int (&e)[RPL], int (&s)[RPL]) {
+            const int u1 = __shfl_up_sync(kFull, e[0], 1);
+            s[0] = lane ? u1 : 0;
+            if (RPL == 2) {
+                const int u2 = __shfl_up_sync(kFull, e[RPL - 1], 1);
+                const int l1 = __shfl_sync(kFull, e[0], 31);
+                s[RPL - 1] = lane ? u2 : l1;
+            }
+            if (!rowlane) s[0] = e[0];
+        };
+        // one tile's products for my rows, operands in my shared-memory region (32-bit
+        // offsets); the entry loop runs the warp's largest row count with predication
+        auto tile_staged = [&](uint4 inf, const int (&s)[RPL], const int (&e)[RPL]) {
+            const int prec = (int)((inf.z >> 16) & 3u);
+            const uint32_t colo = wofs + (inf.z & 0xffffu), valo = wofs + (inf.x & 0xffffu);
+            const uint32_t xo = wofs + (inf.x >> 16);
+#pragma unroll
+            for (int q = 0; q < RPL; ++q) {
+                const int cnt = e[q] - s[q];
+                const int kmax = (int)__reduce_max_sync(kFull, (unsigned)cnt);
+                const uint32_t co = colo + (uint32_t)s[q];
+                if (prec == EVOCG_FP64) {
+                    const uint32_t vo = valo + 8u * (uint32_t)s[q];
+                    double a = acc64[q];
+                    if (kmax == 1) {   // at most one entry per row: the common stencil tile
+                        if (cnt) {
+                            const uint32_t cc = sm[co];
+                            a = fma(*reinterpret_cast<const double *>(sm + vo),
+                                    *reinterpret_cast<const double *>(sm + xo + 8u * cc), a);
+                        }
+                    } else {
+#pragma unroll 1
+                        for (int k = 0; k < kmax; ++k)
+                            if (k < cnt) {
+                                const uint32_t cc = sm[co + k];
+                                a = fma(*reinterpret_cast<const double *>(sm + vo + 8u * k),
+                                        *reinterpret_cast<const double *>(sm + xo + 8u * cc), a);
+                            }
+                    }
+                    acc64[q] = a;
+                } else if (prec == EVOCG_FP32) {
+                    const uint32_t vo = valo + 4u * (uint32_t)s[q];
 #pragma unroll 1
                     for (int k = 0; k < kmax; ++k)
                         if (k < cnt) {
-                            const uint32_t c = sm[co + k];
-                            a = fma(*reinterpret_cast<const double *>(sm + vo + 8u * k),
-                                    *reinterpret_cast<const double *>(sm + xo + 8u * c), a);
+                            const uint32_t cc = sm[co + k];
+                            accl[q].add_prod(*reinterpret_cast<const float *>(sm + vo + 4u * k),
+                                             *reinterpret_cast<const float *>(sm + xo + 4u * cc));
+                        }
+                } else {
+                    const uint32_t vo = valo + 2u * (uint32_t)s[q];
+#pragma unroll 1
+                    for (int k = 0; k < kmax; ++k)  // BF16 x BF16 is exact in FP32
+                        if (k < cnt) {
+                            const uint32_t cc = sm[co + k];
+                            const uint16_t h = *reinterpret_cast<const uint16_t *>(sm + vo + 2u * k);
+                            accl[q].add(__fmul_rn(f32_from_bf16(h),
+                                                  *reinterpret_cast<const float *>(sm + xo + 4u * cc)));
                         }
                 }
-                acc64[q] = a;
-            } else if (prec == EVOCG_FP32) {
-                const uint32_t vo = valo + 4u * (uint32_t)s[q];
-#pragma unroll 1
-                for (int k = 0; k < kmax; ++k)
-                    if (k < cnt) {
-                        const uint32_t c = sm[co + k];
-                        accl[q].add_prod(*reinterpret_cast<const float *>(sm + vo + 4u * k),
-                                         *reinterpret_cast<const float *>(sm + xo + 4u * c));
-                    }
-            } else {
-                const uint32_t vo = valo + 2u * (uint32_t)s[q];
-#pragma unroll 1
-                for (int k = 0; k < kmax; ++k)  // BF16 x BF16 is exact in FP32
-                    if (k < cnt) {
-                        const uint32_t c = sm[co + k];
-                        const uint16_t h = *reinterpret_cast<const uint16_t *>(sm + vo + 2u * k);
-                        accl[q].add(__fmul_rn(f32_from_bf16(h),
-                                              *reinterpret_cast<const float *>(sm + xo + 4u * c)));
-                    }
             }
-        }
-        if (prec == EVOCG_FP64) any64 = true; else anylow = true;
-    };
-
-    // one tile's products straight from global memory (a tile larger than a stage)
-    auto tile_direct = [&](int64_t t, int prec) {
-        const int64_t off = __ldg(A.tileNnzOff + t);
-        const int xb0 = __ldg(A.tileColIdx + t) * T;
-        const uint16_t *re = A.rowEnd + t * T;
-        const uint8_t *ci = A.colIdx + off;
-        int e[RPL], s[RPL];
-        e[0] = rowlane ? (int)__ldg(re + lane) : 0;
-        if (RPL == 2) e[RPL - 1] = (int)__ldg(re + lane + 32);
-        get_starts(e, s);
+            if (prec == EVOCG_FP64) any64 = true; else anylow = true;
+        };
+        // one tile's products straight from global memory (a tile larger than a stage)
+        auto tile_direct = [&](int64_t t, int prec) {
+            const int64_t off = __ldg(A.tileNnzOff + t);
+            const int xb0 = __ldg(A.tileColIdx + t) * T;
+            const uint16_t *re = A.rowEnd + t * T;
+            const uint8_t *ci = A.colIdx + off;
+            int e[RPL], s[RPL];
+            e[0] = rowlane ? (int)__ldg(re + lane) : 0;
+            if (RPL == 2) e[RPL - 1] = (int)__ldg(re + lane + 32);
+            get_starts(e, s);
 #pragma unroll
-        for (int q = 0; q < RPL; ++q) {
-            for (int k = s[q]; k < e[q]; ++k) {
-                const int jx = xb0 + __ldg(ci + k);
-                if (prec == EVOCG_FP64) acc64[q] = fma(__ldg(A.v64 + off + k), __ldg(L.x64 + jx), acc64[q]);
-                else if (prec == EVOCG_FP32) accl[q].add_prod(__ldg(A.v32 + off + k), __ldg(L.x32 + jx));
-                else accl[q].add(__fmul_rn(f32_from_bf16(__ldg(A.v16 + off + k)), __ldg(L.x16f + jx)));
-            }
-        }
-        if (prec == EVOCG_FP64) any64 = true; else anylow = true;
-    };
-
-    // ---- pipeline: S batches in flight, compute the oldest, refill its stage
-    if (rbBeg < rbEnd) {
-        start_rb(rbBeg);
-        const int nbat = bEnd - bBeg;
-        load_raw(bBeg);
-        resolve();
-        load_raw(bBeg + 1);
-        int issued = 0;
-        for (int st = 0; st < C::S && issued < nbat; ++st) {
-            issue(st);
-            ++issued;
-            resolve();
-            load_raw(bBeg + issued + 1);
-        }
-        bool lost = false;
-        for (int b = 0; b < nbat; ++b) {
-            const int st = b % C::S;
-            if (!mbar_wait_bounded(bar0 + 8u * st, (uint32_t)((b / C::S) & 1))) {
-                lost = true;
-                if (lane == 0 && L.A.err) atomicExch(L.A.err, 1);
-                // let the copies still in flight land before the block exits
-                for (int b2 = b + 1; b2 < issued; ++b2)
-                    mbar_wait_bounded(bar0 + 8u * (b2 % C::S), (uint32_t)((b2 / C::S) & 1));
-                break;
-            }
-            const uint32_t stg = wofs + (uint32_t)(st * Y::STAGE);
-            const int4 h = *reinterpret_cast<const int4 *>(sm + stg + Y::HDR);
-            const uint32_t info = stg + Y::INFO;
-            if (h.w) {  // one tile too large for a stage
-                const int64_t tb = (int64_t)(uint32_t)h.x | ((int64_t)h.y << 32);
-                const uint4 inf = *reinterpret_cast<const uint4 *>(sm + info);
-                goto_rb((int)inf.y);
-                tile_direct(tb, (int)((inf.z >> 16) & 3u));
-            } else {
-                const int nb = h.z;
-                const uint32_t re = stg + Y::RE + 2u * (uint32_t)lane;   // my row's entry
-                uint4 inf = *reinterpret_cast<const uint4 *>(sm + info);
-                int e[RPL], s[RPL];
-                e[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re) : 0;
-                if (RPL == 2) e[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 64u);
-                for (int jt = 0; jt < nb; ++jt) {
-                    // the next tile's descriptor and row ends load while this one computes
-                    uint4 infn = inf;
-                    int en[RPL];
-#pragma unroll
-                    for (int q = 0; q < RPL; ++q) en[q] = 0;
-                    if (jt + 1 < nb) {
-                        const uint32_t jn = (uint32_t)(jt + 1);
-                        infn = *reinterpret_cast<const uint4 *>(sm + info + 16u * jn);
-                        en[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn) : 0;
-                        if (RPL == 2)
-                            en[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn + 64u);
-                    }
-                    get_starts(e, s);
-                    goto_rb((int)inf.y);
-                    tile_staged(inf, s, e);
-                    inf = infn;
-#pragma unroll
-                    for (int q = 0; q < RPL; ++q) e[q] = en[q];
+            for (int q = 0; q < RPL; ++q) {
+                for (int k = s[q]; k < e[q]; ++k) {
+                    const int jx = xb0 + __ldg(ci + k);
+                    if (prec == EVOCG_FP64) acc64[q] = fma(__ldg(A.v64 + off + k), __ldg(L.x64 + jx), acc64[q]);
+                    else if (prec == EVOCG_FP32) accl[q].add_prod(__ldg(A.v32 + off + k), __ldg(L.x32 + jx));
+                    else accl[q].add(__fmul_rn(f32_from_bf16(__ldg(A.v16 + off + k)), __ldg(L.x16f + jx)));
                 }
             }
-            __syncwarp();
-            if (issued < nbat) {
-                issue(st);
-                ++issued;
-                resolve();
-                load_raw(bBeg + issued + 1);
+            if (prec == EVOCG_FP64) any64 = true; else anylow = true;
+        };
+
+        if (rbBeg < rbEnd) {
+            start_rb(rbBeg);
+            bool lost = false;
+            for (int b = 0; b < nbat; ++b) {
+                const int st = b % C::S;
+                if (!mbar_wait_bounded(full_bar(wib, st), (uint32_t)((b / C::S) & 1))) {
+                    lost = true;
+                    if (lane == 0 && A.err) atomicExch(A.err, 1);
+                    break;
+                }
+                const uint32_t stg = wofs + (uint32_t)(st * Y::STAGE);
+                const int4 h = *reinterpret_cast<const int4 *>(sm + stg + Y::HDR);
+                const uint32_t info = stg + Y::INFO;
+                if (h.w) {  // one tile too large for a stage
+                    const int64_t tb = (int64_t)(uint32_t)h.x | ((int64_t)h.y << 32);
+                    const uint4 inf = *reinterpret_cast<const uint4 *>(sm + info);
+                    goto_rb((int)inf.y);
+                    tile_direct(tb, (int)((inf.z >> 16) & 3u));
+                } else {
+                    const int nb = h.z;
+                    const uint32_t re = stg + Y::RE + 2u * (uint32_t)lane;   // my row's entry
+                    uint4 inf = *reinterpret_cast<const uint4 *>(sm + info);
+                    int e[RPL], s[RPL];
+                    e[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re) : 0;
+                    if (RPL == 2) e[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 64u);
+                    for (int jt = 0; jt < nb; ++jt) {
+                        // the next tile's descriptor and row ends load while this one computes
+                        uint4 infn = inf;
+                        int en[RPL];
+#pragma unroll
+                        for (int q = 0; q < RPL; ++q) en[q] = 0;
+                        if (jt + 1 < nb) {
+                            const uint32_t jn = (uint32_t)(jt + 1);
+                            infn = *reinterpret_cast<const uint4 *>(sm + info + 16u * jn);
+                            en[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn) : 0;
+                            if (RPL == 2)
+                                en[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn + 64u);
+                        }
+                        get_starts(e, s);
+                        goto_rb((int)inf.y);
+                        tile_staged(inf, s, e);
+                        inf = infn;
+#pragma unroll
+                        for (int q = 0; q < RPL; ++q) e[q] = en[q];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(wib, st));   // the stage may be refilled
             }
-        }
-        if (!lost) {
-            finish_rb(cur_rb);
-            zero_rows(cur_rb + 1, rbEnd);
+            if (!lost) {
+                finish_rb(cur_rb);
+                zero_rows(cur_rb + 1, rbEnd);
+            }
         }
     }
 
-    if (L.census && lane == 0) {
+    if (L.census && wib == C::NC && lane == 0) {
         if (cnt0) atomicAdd(&L.st->census[0], cnt0);
         if (cnt1) atomicAdd(&L.st->census[1], cnt1);
         if (cnt2) atomicAdd(&L.st->census[2], cnt2);
@@ -612,7 +562,7 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
         if (threadIdx.x == 0) L.partials[blockIdx.x] = sd;
         if (st_last_block(st, TK_SPMV)) {
             double v = 0.0;
-            for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) v += __ldcg(L.partials + i);
+            for (int k = threadIdx.x; k < (int)gridDim.x; k += blockDim.x) v += __ldcg(L.partials + k);
             const double sigma = st_block_sum(v);
             if (threadIdx.x == 0) {
                 st->tickets[TK_SPMV] = 0;
@@ -633,7 +583,7 @@ __global__ void __launch_bounds__(StCfg<T>::NW * 32, StCfg<T>::MINB)
 template <int T>
 cudaError_t staged_T(const SpmvLaunch &L, cudaStream_t s)
 {
-    constexpr int threads = StCfg<T>::NW * 32;
+    constexpr int threads = StCfg<T>::THREADS;
     constexpr int smem = StLayout<T>::SMEM;
     if (L.force64) {
         if (L.dot) spmv_staged_kernel<T, true, true><<<L.grid, threads, smem, s>>>(L);
@@ -648,7 +598,7 @@ cudaError_t staged_T(const SpmvLaunch &L, cudaStream_t s)
 template <int T>
 int staged_grid_T(int sms)
 {
-    constexpr int threads = StCfg<T>::NW * 32;
+    constexpr int threads = StCfg<T>::THREADS;
     constexpr int smem = StLayout<T>::SMEM;
     const void *ks[4] = {(const void *)spmv_staged_kernel<T, true, true>,
                          (const void *)spmv_staged_kernel<T, true, false>,

@@ -190,3 +190,35 @@ def test_plain_launch_mode_matches_graph(monkeypatch):
     monkeypatch.delenv("EVOCG_GRAPH")
     assert a[0]["iters"] == b[0]["iters"] and a[0]["prec_nnz"] == b[0]["prec_nnz"]
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+
+
+def _golden_iterations():
+    import json
+    import os
+    p = os.path.join(os.path.dirname(__file__), "golden", "oracle_iterations.json")
+    with open(p) as f:
+        return json.load(f)
+
+
+@pytest.mark.parametrize("cfg", [2, 3, 4])
+def test_cg_full_solve_matches_oracle_count(cfg):
+    """Full-size workloads solved to rtol exactly as the benchmark configures them (solver,
+    map or controller, FP64 finish): the iteration count is within 3% of the oracle's full
+    solve (stored by tests/golden/make_oracle_iterations.py, which calls only the oracle)
+    and the FP64 true residual, recomputed by the oracle from the GPU's x, is <= rtol."""
+    gold = _golden_iterations().get(str(cfg))
+    if gold is None:
+        pytest.skip(f"no oracle full-solve count stored for workload {cfg}")
+    w = W.workload(cfg)
+    P = Pair((w.n, w.rp, w.ci, w.v), w.T)
+    if w.ctrl == "threshold":
+        ctrl = evocg.Ctrl.threshold(w.eps, w.kstar)
+    elif w.ctrl == "mlp":
+        ctrl = evocg.Ctrl.mlp(W.mlp_weights(w.T, w.mlp_seed), w.kstar, w.delta)
+    else:
+        ctrl = None
+        evocg.set_tile_precision(P.G, P.tile_map(w.map_seed))
+    info, x, _ = _solve(P, w.b, w.rtol, w.maxit, w.jacobi, ctrl, True)
+    assert info["status"] == gold["status"] == evocg.OK, (info, gold)
+    assert abs(info["iters"] - gold["iters"]) <= max(2, 0.03 * gold["iters"]), (info, gold)
+    assert oracle.true_residual(P.A, w.b, x) <= w.rtol
