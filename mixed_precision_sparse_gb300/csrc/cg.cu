@@ -2,8 +2,8 @@
 // for Faster Conjugate Gradient": the solver lines of Algorithm 1, §2.1 Fig. 1, §3.4
 // fused step, §4.6 Jacobi-PCG) for sm_103a.
 //
-// One iteration is three kernels in a CUDA graph: the SpMV with p.q fused into its
-// epilogue (its last block forms alpha), cg_update (x, r, z and the two dot products;
+// One iteration is four kernels in a CUDA graph: the SpMV, cg_pq (p.q; its last block forms
+// alpha), cg_update (x, r, z and the two dot products;
 // its last block forms beta, the history entry and the stop flag, and drives the graph's
 // while node), and cg_pupdate (p, the rounded copies of p that the next SpMV reads, and
 // the threshold controller's decisions). Reductions are per-thread FP64 partials in a
@@ -20,9 +20,9 @@ namespace evocg {
 __device__ __forceinline__ bool last_block_cg(DevState *st, int slot)
 {
     __shared__ bool amLast;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {   // thread 0 wrote the block's partial: publish it, take a ticket
+        __threadfence();
         const unsigned t = atomicAdd(&st->tickets[slot], 1u);
         amLast = (t == gridDim.x - 1);
     }
@@ -158,6 +158,43 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
                 st->status = EVOCG_ENOTCONV;
             }
             if (L.use_cond) cudaGraphSetConditional(L.cond, st->done ? 0u : 1u);
+        }
+    }
+}
+
+// sigma = p.q (q = A p from the SpMV); the last block forms alpha = rho / sigma, or stops the
+// solve with EVOCG_EBREAKDOWN when sigma is not finite and positive.
+__global__ void __launch_bounds__(kVecThreads) cg_pq_kernel(CgLaunch L)
+{
+    DevState *st = L.st;
+    if (st->done) return;
+    const int64_t n = L.n, npairs = (n + 1) / 2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    double pq = 0.0;
+    for (int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; pair < npairs; pair += stride) {
+        const int64_t j = 2 * pair;
+        if (j + 1 < n) {
+            const double2 p = *reinterpret_cast<const double2 *>(L.p + j);
+            const double2 q = *reinterpret_cast<const double2 *>(L.q + j);
+            pq = fma(p.x, q.x, pq);
+            pq = fma(p.y, q.y, pq);
+        } else {
+            pq = fma(L.p[j], L.q[j], pq);
+        }
+    }
+    const double s = block_sum_cg(pq);
+    if (threadIdx.x == 0) L.partials[blockIdx.x] = s;
+    if (last_block_cg(st, TK_SPMV)) {
+        const double sigma = sum_partials(L.partials);
+        if (threadIdx.x == 0) {
+            st->tickets[TK_SPMV] = 0;
+            if (!(sigma > 0.0) || !isfinite(sigma)) {
+                st->status = EVOCG_EBREAKDOWN;
+                st->done = 1;
+            } else {
+                st->sigma = sigma;
+                st->alpha = st->rho / sigma;
+            }
         }
     }
 }
@@ -351,12 +388,16 @@ cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
     S.prec = (L.ctrl == EVOCG_CTRL_STATIC) ? L.prec : L.cbPrec;
     S.map_kind = (L.ctrl == EVOCG_CTRL_STATIC) ? L.map_kind : EVOCG_MAP_PER_COLBLOCK;
     S.force64 = force64;
-    S.dot = 1;
+    S.dot = 0;             // p.q in its own pass: a reduction epilogue in the SpMV costs more
+    S.gate = 1;
     S.partials = L.partials;
     S.st = L.st;
     S.census = 1;
     S.grid = L.spmv_grid;
     e = launch_spmv(S, s);
+    if (e != cudaSuccess) return e;
+    cg_pq_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cg_update_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L);
     e = cudaGetLastError();

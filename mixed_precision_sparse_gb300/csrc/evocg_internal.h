@@ -198,6 +198,7 @@ struct SpmvLaunch {
     double *partials;
     DevState *st;
     int census;            // accumulate per-precision entry counts into st->census
+    int gate;              // return at once when st->done is set (a stopped solve)
     int grid;              // grid of the direct kernel
     int direct;            // 1: the direct kernel even when the staged one could run
 };

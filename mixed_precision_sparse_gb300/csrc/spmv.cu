@@ -39,9 +39,9 @@ struct Geo {
 __device__ __forceinline__ bool last_block(DevState *st, int slot)
 {
     __shared__ bool amLast;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {   // thread 0 wrote the block's partial: publish it, take a ticket
+        __threadfence();
         const unsigned t = atomicAdd(&st->tickets[slot], 1u);
         amLast = (t == gridDim.x - 1);
     }
@@ -69,7 +69,7 @@ template <int T, bool FORCE64, bool DOT>
 __global__ void __launch_bounds__(kSpmvThreads, kSpmvMinBlocks) spmv_kernel(SpmvLaunch L)
 {
     using Gm = Geo<T>;
-    if (DOT && L.st->done) return;  // a stopped solve: nothing to compute or count
+    if ((DOT || L.gate) && L.st->done) return;  // a stopped solve: nothing to compute or count
     const TilesView A = L.A;
     const int lane = threadIdx.x & 31;
     const int grp = lane / Gm::G;

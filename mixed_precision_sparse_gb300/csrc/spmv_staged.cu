@@ -167,9 +167,9 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uin
 __device__ __forceinline__ bool st_last_block(DevState *st, int slot)
 {
     __shared__ bool amLast;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {   // thread 0 wrote the block's partial: publish it, take a ticket
+        __threadfence();
         const unsigned t = atomicAdd(&st->tickets[slot], 1u);
         amLast = (t == gridDim.x - 1);
     }
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
     using Y = StLayout<T>;
     constexpr int RPL = T > 32 ? 2 : 1;            // rows per lane (consumers)
     constexpr int G = 32 / C::NC;                   // producer lanes per consumer
-    if (DOT && L.st->done) return;                  // a stopped solve: nothing to do
+    if ((DOT || L.gate) && L.st->done) return;      // a stopped solve: nothing to do
     extern __shared__ __align__(128) unsigned char sm[];
     const TilesView A = L.A;
     const int lane = threadIdx.x & 31;
@@ -234,9 +234,20 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
         for (int o = 16; o; o >>= 1) rounds = max(rounds, __shfl_xor_sync(kFull, rounds, o));
         const uint32_t wreg = region(c);
 
-        // raw descriptors of round r (loaded one round ahead)
+        // Descriptors: raw for round r + 1 (loaded two rounds ahead) and resolved, with the
+        // precision looked up, for round r (its precision load issued one round ahead), so
+        // the producer never waits on memory inside a round.
         int64_t r_o0 = 0, r_o1 = 0, r_tb = 0;
         int r_cb = 0, r_rb = 0, r_slot = 0, r_pt = 0, r_nb = 0;
+        int64_t d_o0 = 0, d_tb = 0;
+        int d_m = 0, d_cb = 0, d_rb = 0, d_slot = 0, d_nb = 0, d_prec = 0;
+        auto resolve = [&]() {   // d <- raw
+            d_nb = r_nb; d_tb = r_tb; d_o0 = r_o0; d_m = (int)(r_o1 - r_o0);
+            d_cb = r_cb; d_rb = r_rb; d_slot = r_slot;
+            if (FORCE64) d_prec = 0;
+            else if (L.map_kind == EVOCG_MAP_PER_TILE) d_prec = r_pt;
+            else d_prec = (i < r_nb) ? (int)__ldg(L.prec + r_cb) : 0;
+        };
         auto load_raw = [&](int r) {
             const int bb = bBeg + r;
             r_nb = 0;
@@ -255,17 +266,17 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
             }
         };
         load_raw(0);
+        resolve();
+        load_raw(1);
         bool lost = false;
         for (int r = 0; r < rounds && !lost; ++r) {
             const int st = r % C::S;
-            // this round's descriptors, and the next round's raw loads in flight
-            const int nb = r_nb;
-            const int64_t tb = r_tb, o0 = r_o0;
-            const int m = (int)(r_o1 - r_o0), cb = r_cb, rb = r_rb, slot = r_slot;
+            // this round's descriptors; the next round's resolve and the one after's raw
+            // loads are issued at the end of the round
+            const int nb = d_nb;
+            const int64_t tb = d_tb, o0 = d_o0;
+            const int m = d_m, cb = d_cb, rb = d_rb, slot = d_slot, prec = d_prec;
             const bool valid = i < nb;
-            int prec = 0;
-            if (!FORCE64) prec = (L.map_kind == EVOCG_MAP_PER_TILE) ? r_pt : (valid ? (int)__ldg(L.prec + cb) : 0);
-            load_raw(r + 1);
             // wait until each consumer has released the stage this round refills
             bool timedout = false;
             if (r >= C::S && i == 0 && nb > 0)
@@ -354,6 +365,8 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
                     bulk_g2s_hint(sbase + stg + Y::RE, A.rowEnd + tb * T, (uint32_t)(nb * 2 * T), full_bar(c, st), pol);
                 }
             }
+            resolve();
+            load_raw(r + 2);
         }
     } else {
         // =============================== consumer ===============================
@@ -365,7 +378,6 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
 
         double acc64[RPL];
         F32Pair accl[RPL];
-        double xrow[RPL];
         bool any64 = false, anylow = false;
         int cur_rb = rbBeg;
         auto start_rb = [&](int rb) {
@@ -374,8 +386,6 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
                 acc64[q] = 0.0;
                 accl[q].hi = 0.f;
                 accl[q].lo = 0.f;
-                const int row = rb * T + lane + 32 * q;
-                xrow[q] = (DOT && rowlane && row < n) ? __ldg(L.x64 + row) : 0.0;
             }
             any64 = false;
             anylow = false;
@@ -391,7 +401,7 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
                         y = any64 ? y + dd : dd;
                     }
                     L.y[row] = y;
-                    if (DOT) dotp = fma(xrow[q], y, dotp);
+                    if (DOT) dotp = fma(__ldg(L.x64 + row), y, dotp);   // p.q of CG
                 }
             }
         };
