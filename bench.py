@@ -266,9 +266,9 @@ def run_ours(args):
     value = ms / 1000.0 / world      # seconds per solve for the whole job
     launches = 0
     for inf in infos:
-        # init + 4 kernels per iteration (+1 policy kernel per iteration with the MLP),
+        # init + 3 kernels per iteration (+1 policy kernel per iteration with the MLP),
         # true-residual check 2 per check, each restart graph: SpMV + init
-        per_it = 4 + (1 if w.ctrl == "mlp" else 0)
+        per_it = 3 + (1 if w.ctrl == "mlp" else 0)
         launches += 1 + per_it * inf["iters"] + 2 * (1 + inf["restarts"]) + 2 * inf["restarts"]
 
     # ---- end to end through the C ABI with pinned host buffers

@@ -102,7 +102,7 @@ void release_ws(SolveWS &w)
 {
     release_graphs(w);
     dfree(w.b); dfree(w.x); dfree(w.r); dfree(w.p); dfree(w.q); dfree(w.z); dfree(w.hist);
-    dfree(w.partials); dfree(w.cbPrec); dfree(w.mlpW); dfree(w.st);
+    dfree(w.partials); dfree(w.pq); dfree(w.cbPrec); dfree(w.mlpW); dfree(w.st);
     if (w.st_host) cudaFreeHost(w.st_host);
     w.st_host = nullptr;
     w.cap_n = 0; w.cap_hist = 0; w.cap_ncb = 0; w.cap_mlp = 0;
@@ -121,6 +121,7 @@ int ensure_ws(evocg_tiles *A, int maxit)
         CK(dalloc(&w.q, n), "cudaMalloc q");
         CK(dalloc(&w.z, n), "cudaMalloc z");
         CK(dalloc(&w.partials, 2 * kMaxBlocks), "cudaMalloc partials");
+        CK(dalloc(&w.pq, kMaxPq), "cudaMalloc p.q partials");
         CK(dalloc(&w.cbPrec, A->nrb), "cudaMalloc cbPrec");
         CK(dalloc(&w.st, 1), "cudaMalloc state");
         CK(cudaMemset(w.st, 0, sizeof(DevState)), "cudaMemset state");
@@ -613,7 +614,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     L.A = A->view();
     L.n = n; L.T = A->T; L.jacobi = jacobi ? 1 : 0; L.ctrl = kind; L.dinv = A->dinv;
     L.b = w.b; L.x = w.x; L.r = w.r; L.p = w.p; L.q = w.q; L.z = w.z;
-    L.x32 = A->x32; L.x16f = A->x16f; L.hist = w.hist; L.partials = w.partials;
+    L.x32 = A->x32; L.x16f = A->x16f; L.hist = w.hist; L.partials = w.partials; L.pq = w.pq;
     L.cbPrec = w.cbPrec;
     L.prec = (A->map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
     L.map_kind = A->map_kind;

@@ -2,8 +2,8 @@
 // for Faster Conjugate Gradient": the solver lines of Algorithm 1, §2.1 Fig. 1, §3.4
 // fused step, §4.6 Jacobi-PCG) for sm_103a.
 //
-// One iteration is four kernels in a CUDA graph: the SpMV, cg_pq (p.q; its last block forms
-// alpha), cg_update (x, r, z and the two dot products;
+// One iteration is three kernels in a CUDA graph: the SpMV (with one p.q partial per warp),
+// cg_update (alpha from those partials; x, r, z and the two dot products;
 // its last block forms beta, the history entry and the stop flag, and drives the graph's
 // while node), and cg_pupdate (p, the rounded copies of p that the next SpMV reads, and
 // the threshold controller's decisions). Reductions are per-thread FP64 partials in a
@@ -162,53 +162,41 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
     }
 }
 
-// sigma = p.q (q = A p from the SpMV); the last block forms alpha = rho / sigma, or stops the
-// solve with EVOCG_EBREAKDOWN when sigma is not finite and positive.
-__global__ void __launch_bounds__(kVecThreads) cg_pq_kernel(CgLaunch L)
-{
-    DevState *st = L.st;
-    if (st->done) return;
-    const int64_t n = L.n, npairs = (n + 1) / 2;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    double pq = 0.0;
-    for (int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; pair < npairs; pair += stride) {
-        const int64_t j = 2 * pair;
-        if (j + 1 < n) {
-            const double2 p = *reinterpret_cast<const double2 *>(L.p + j);
-            const double2 q = *reinterpret_cast<const double2 *>(L.q + j);
-            pq = fma(p.x, q.x, pq);
-            pq = fma(p.y, q.y, pq);
-        } else {
-            pq = fma(L.p[j], L.q[j], pq);
-        }
-    }
-    const double s = block_sum_cg(pq);
-    if (threadIdx.x == 0) L.partials[blockIdx.x] = s;
-    if (last_block_cg(st, TK_SPMV)) {
-        const double sigma = sum_partials(L.partials);
-        if (threadIdx.x == 0) {
-            st->tickets[TK_SPMV] = 0;
-            if (!(sigma > 0.0) || !isfinite(sigma)) {
-                st->status = EVOCG_EBREAKDOWN;
-                st->done = 1;
-            } else {
-                st->sigma = sigma;
-                st->alpha = st->rho / sigma;
-            }
-        }
-    }
-}
-
-// x += alpha p; r -= alpha q; z = D^-1 r; r.z and ||r||^2. The last block appends the
-// history entry, tests convergence and forms beta.
-__global__ void __launch_bounds__(kVecThreads) cg_update_kernel(CgLaunch L)
+// sigma = p.q from the SpMV's per-warp partials (summed in warp order, identically in every
+// block), alpha = rho / sigma; then x += alpha p; r -= alpha q; z = D^-1 r; r.z and ||r||^2.
+// The last block appends the history entry, tests convergence and forms beta. A sigma that
+// is not finite and positive stops the solve with EVOCG_EBREAKDOWN.
+__global__ void __launch_bounds__(kVecThreads) cg_update_kernel(CgLaunch L, int npq)
 {
     DevState *st = L.st;
     if (st->done) {
         if (L.use_cond && blockIdx.x == 0 && threadIdx.x == 0) cudaGraphSetConditional(L.cond, 0u);
         return;
     }
-    const double alpha = st->alpha;
+    __shared__ double s_alpha;
+    {
+        double v = 0.0;
+        for (int i = threadIdx.x; i < npq; i += blockDim.x) v += __ldcg(L.pq + i);
+        const double sigma = block_sum_cg(v);
+        if (threadIdx.x == 0) {
+            const bool ok = (sigma > 0.0) && isfinite(sigma);
+            s_alpha = ok ? st->rho / sigma : 0.0;
+            if (blockIdx.x == 0) {
+                st->sigma = sigma;
+                if (ok) {
+                    st->alpha = s_alpha;
+                } else {
+                    st->status = EVOCG_EBREAKDOWN;
+                    st->done = 1;
+                    if (L.use_cond) cudaGraphSetConditional(L.cond, 0u);
+                }
+            }
+            if (!ok) s_alpha = __longlong_as_double(0x7FF8000000000000ll);   // NaN marks the stop
+        }
+        __syncthreads();
+    }
+    const double alpha = s_alpha;
+    if (isnan(alpha)) return;   // every block saw the same sigma
     const int64_t n = L.n, npairs = (n + 1) / 2;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     double rz = 0.0, rr = 0.0;
@@ -388,18 +376,18 @@ cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
     S.prec = (L.ctrl == EVOCG_CTRL_STATIC) ? L.prec : L.cbPrec;
     S.map_kind = (L.ctrl == EVOCG_CTRL_STATIC) ? L.map_kind : EVOCG_MAP_PER_COLBLOCK;
     S.force64 = force64;
-    S.dot = 0;             // p.q in its own pass: a reduction epilogue in the SpMV costs more
+    S.dot = 1;             // per-warp p.q partials, summed by the update kernel
+    S.pq = L.pq;
     S.gate = 1;
     S.partials = L.partials;
     S.st = L.st;
     S.census = 1;
     S.grid = L.spmv_grid;
+    const int npq = spmv_dot_partials(S);
+    if (npq > kMaxPq) return cudaErrorInvalidConfiguration;
     e = launch_spmv(S, s);
     if (e != cudaSuccess) return e;
-    cg_pq_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    cg_update_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L);
+    cg_update_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L, npq);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (L.T) {

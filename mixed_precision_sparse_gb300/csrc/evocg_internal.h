@@ -12,6 +12,7 @@
 namespace evocg {
 
 constexpr int kMaxBlocks = 2048;      // upper bound of any grid here (partials buffers)
+constexpr int kMaxPq = 16384;         // per-warp p.q partials of one SpMV (grid x warps)
 constexpr int kVecThreads = 256;      // threads per block of the vector kernels
 constexpr int kSpmvThreads = 256;     // threads per block of the SpMV
 constexpr int kSpmvMinBlocks = 4;     // resident blocks per SM the SpMV registers are budgeted for
@@ -95,7 +96,8 @@ struct SolveWS {
     int cap_hist = 0;
     double *b = nullptr, *x = nullptr, *r = nullptr, *p = nullptr, *q = nullptr, *z = nullptr;
     double *hist = nullptr;
-    double *partials = nullptr;       // 4 * kMaxBlocks
+    double *partials = nullptr;       // 2 * kMaxBlocks
+    double *pq = nullptr;             // kMaxPq per-warp p.q partials of the SpMV
     uint8_t *cbPrec = nullptr;        // controller decisions per column block
     float *mlpW = nullptr;            // packed MLP weights on the device
     int64_t cap_mlp = 0;
@@ -193,8 +195,10 @@ struct SpmvLaunch {
     const uint8_t *prec;   // tilePrec (map_kind 0) or cbPrec (map_kind 1); ignored if force64
     int map_kind;
     int force64;
-    // fused p.q for CG (dot != 0): partial sums, then the last block computes alpha
+    // p.q for CG (dot != 0): every warp writes the sum over its rows of x_i y_i to pq[warp]
+    // (spmv_dot_partials() of them); the update kernel sums them in warp order
     int dot;
+    double *pq;
     double *partials;
     DevState *st;
     int census;            // accumulate per-precision entry counts into st->census
@@ -206,8 +210,10 @@ struct SpmvLaunch {
 // aligned; otherwise the direct kernel.
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
 cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s);
+int spmv_dot_partials(const SpmvLaunch &L);   // warps that write a p.q partial
 cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s);
 int staged_grid_for(int T, int sms);   // 0 if it cannot run
+int staged_warps_per_block(int T);      // consumer warps (the ones with rows) per block
 
 // Host: the staged SpMV plan for `warps` warps (api.cpp).
 void staged_plan(const HostTiles &H, int64_t warps, const StagedLimits &lim,
@@ -230,6 +236,7 @@ struct CgLaunch {
     float *x16f;
     double *hist;
     double *partials;
+    double *pq;            // the SpMV's per-warp p.q partials
     uint8_t *cbPrec;       // controller output (map_kind 1 for the SpMV)
     const uint8_t *prec;   // static map
     int map_kind;

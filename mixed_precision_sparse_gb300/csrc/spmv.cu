@@ -34,37 +34,6 @@ struct Geo {
     static constexpr int RPL = T / G;          // rows per lane
 };
 
-// Last block of a grid: sums per-block partials in a fixed order (deterministic) and
-// returns true in every thread of that block. `slot` selects the ticket counter.
-__device__ __forceinline__ bool last_block(DevState *st, int slot)
-{
-    __shared__ bool amLast;
-    __syncthreads();
-    if (threadIdx.x == 0) {   // thread 0 wrote the block's partial: publish it, take a ticket
-        __threadfence();
-        const unsigned t = atomicAdd(&st->tickets[slot], 1u);
-        amLast = (t == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (amLast) __threadfence();
-    return amLast;
-}
-
-// Deterministic block sum of one double per thread (fixed shuffle tree, fixed order).
-__device__ __forceinline__ double block_sum(double v)
-{
-    __shared__ double ws[32];
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) ws[w] = v;
-    __syncthreads();
-    double s = 0.0;
-    if (threadIdx.x == 0)
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += ws[i];
-    return s;  // valid in thread 0
-}
-
 template <int T, bool FORCE64, bool DOT>
 __global__ void __launch_bounds__(kSpmvThreads, kSpmvMinBlocks) spmv_kernel(SpmvLaunch L)
 {
@@ -168,27 +137,9 @@ __global__ void __launch_bounds__(kSpmvThreads, kSpmvMinBlocks) spmv_kernel(Spmv
             if (cnt2) atomicAdd(&L.st->census[2], cnt2);
         }
     }
-    if (DOT) {
-        DevState *st = L.st;
-        const double s = block_sum(dotp);
-        if (threadIdx.x == 0) L.partials[blockIdx.x] = s;
-        if (last_block(st, TK_SPMV)) {
-            double v = 0.0;
-            for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) v += __ldcg(L.partials + i);
-            const double sigma = block_sum(v);
-            if (threadIdx.x == 0) {
-                st->tickets[TK_SPMV] = 0;
-                if (!st->done) {
-                    if (!(sigma > 0.0) || !isfinite(sigma)) {
-                        st->status = EVOCG_EBREAKDOWN;
-                        st->done = 1;
-                    } else {
-                        st->sigma = sigma;
-                        st->alpha = st->rho / sigma;
-                    }
-                }
-            }
-        }
+    if (DOT) {   // this warp's p.q partial (lanes summed in a fixed tree)
+        for (int o = 16; o; o >>= 1) dotp += __shfl_xor_sync(0xffffffffu, dotp, o);
+        if (lane == 0) L.pq[wid] = dotp;
     }
 }
 
@@ -232,11 +183,22 @@ static cudaError_t launch_T(const SpmvLaunch &L, cudaStream_t s)
     return cudaGetLastError();
 }
 
-cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
+static bool use_staged(const SpmvLaunch &L)
 {
     const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (!L.direct && L.A.warpRb && L.A.staged_grid > 0 && al(L.x64) &&
-        (L.force64 || (al(L.x32) && al(L.x16f)))) {
+    return !L.direct && L.A.warpRb && L.A.staged_grid > 0 && al(L.x64) &&
+           (L.force64 || (al(L.x32) && al(L.x16f)));
+}
+
+int spmv_dot_partials(const SpmvLaunch &L)
+{
+    if (use_staged(L)) return L.A.staged_grid * staged_warps_per_block(L.A.T);
+    return L.grid * (kSpmvThreads / 32);
+}
+
+cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
+{
+    if (use_staged(L)) {
         SpmvLaunch S = L;
         S.grid = L.A.staged_grid;
         return launch_spmv_staged(S, s);

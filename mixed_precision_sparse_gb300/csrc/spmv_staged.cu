@@ -163,35 +163,6 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void *src, uin
         : "memory");
 }
 
-// Last block of a grid (see the direct kernel): fixed-order sums of per-block partials.
-__device__ __forceinline__ bool st_last_block(DevState *st, int slot)
-{
-    __shared__ bool amLast;
-    __syncthreads();
-    if (threadIdx.x == 0) {   // thread 0 wrote the block's partial: publish it, take a ticket
-        __threadfence();
-        const unsigned t = atomicAdd(&st->tickets[slot], 1u);
-        amLast = (t == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (amLast) __threadfence();
-    return amLast;
-}
-
-__device__ __forceinline__ double st_block_sum(double v)
-{
-    __shared__ double ws[32];
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    __syncthreads();
-    if (l == 0) ws[w] = v;
-    __syncthreads();
-    double s = 0.0;
-    if (threadIdx.x == 0)
-        for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += ws[i];
-    return s;
-}
-
 template <int T, bool FORCE64, bool DOT>
 __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
     spmv_staged_kernel(SpmvLaunch L)
@@ -566,27 +537,9 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
         if (cnt1) atomicAdd(&L.st->census[1], cnt1);
         if (cnt2) atomicAdd(&L.st->census[2], cnt2);
     }
-    if (DOT) {
-        DevState *st = L.st;
-        const double sd = st_block_sum(dotp);
-        if (threadIdx.x == 0) L.partials[blockIdx.x] = sd;
-        if (st_last_block(st, TK_SPMV)) {
-            double v = 0.0;
-            for (int k = threadIdx.x; k < (int)gridDim.x; k += blockDim.x) v += __ldcg(L.partials + k);
-            const double sigma = st_block_sum(v);
-            if (threadIdx.x == 0) {
-                st->tickets[TK_SPMV] = 0;
-                if (!st->done) {
-                    if (!(sigma > 0.0) || !isfinite(sigma)) {
-                        st->status = EVOCG_EBREAKDOWN;
-                        st->done = 1;
-                    } else {
-                        st->sigma = sigma;
-                        st->alpha = st->rho / sigma;
-                    }
-                }
-            }
-        }
+    if (DOT && wib < C::NC) {   // this consumer warp's p.q partial (fixed shuffle tree)
+        for (int o = 16; o; o >>= 1) dotp += __shfl_xor_sync(kFull, dotp, o);
+        if (lane == 0) L.pq[blockIdx.x * C::NC + wib] = dotp;
     }
 }
 
@@ -656,6 +609,16 @@ int staged_grid_for(int T, int sms)
     case 16: return staged_grid_T<16>(sms);
     case 32: return staged_grid_T<32>(sms);
     case 64: return staged_grid_T<64>(sms);
+    default: return 0;
+    }
+}
+
+int staged_warps_per_block(int T)
+{
+    switch (T) {
+    case 16: return StCfg<16>::NC;
+    case 32: return StCfg<32>::NC;
+    case 64: return StCfg<64>::NC;
     default: return 0;
     }
 }
