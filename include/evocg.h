@@ -160,9 +160,13 @@ enum {
                                      handle; x must hold the same values as in that call */
     EVOCG_SPMV_DIRECT = 2         /* run the direct kernel (every operand read from global
                                      memory by the lanes) instead of the staged one (operands
-                                     copied into shared memory by bulk asynchronous copies);
-                                     both compute the same sums in the same order. The staged
-                                     kernel is the default whenever x is 16-byte aligned */
+                                     copied into shared memory by bulk asynchronous copies).
+                                     For tiles of 32 and 64 both compute the same sums in the
+                                     same order; for tiles of 16 the direct kernel splits a row
+                                     block's tiles over two half-warps (same sums to rounding).
+                                     The staged kernel is the default when x is 16-byte
+                                     aligned and the tiles hold at least 12 entries on average
+                                     (the direct kernel is faster for sparser tiles) */
 };
 
 /*
