@@ -54,9 +54,9 @@ def _load():
             lib.ora_csr_check.argtypes = [i64, P, P, P]
             lib.ora_csr_check.restype = i32
             lib.ora_col_exp.argtypes = [i64, P, P, P, P]
-            lib.ora_tile_count.argtypes = [i64, P, P, i32, P, P]
+            lib.ora_tile_count.argtypes = [i64, P, P, i32, P, P, P]
             lib.ora_tile_count.restype = i32
-            lib.ora_tile_build.argtypes = [i64, P, P, P, i32] + [P] * 9
+            lib.ora_tile_build.argtypes = [i64, P, P, P, i32] + [P] * 10
             lib.ora_tile_build.restype = i32
             lib.ora_mixed_spmv.argtypes = [i64, P, P, P, i32, P, P, P, P, P, P]
             lib.ora_ctrl_threshold.argtypes = [i64, i32, P, dbl, P]
@@ -127,41 +127,60 @@ def col_exp(A: CSR):
 
 
 class Tiles:
-    """The oracle's own tile layout (arrays named as in the GPU library's export)."""
+    """The oracle's own tile layout (arrays named as in the GPU library's export).
+
+    Inside tile t: rowMask[t] marks its nonempty local rows, tileWidth[t] = w is its
+    longest row, and slot (k, j) at tileNnzOff[t] + k*h + j (h = nonempty rows) holds
+    the k-th entry of the j-th nonempty row or a pad (local column T, value +0)."""
 
     def __init__(self, A: CSR, T: int):
         lib = _load()
-        nt, nz = C.c_int64(), C.c_int64()
-        st = lib.ora_tile_count(A.n, _p(A.rp), _p(A.ci), int(T), C.byref(nt), C.byref(nz))
+        nt, nz, ns = C.c_int64(), C.c_int64(), C.c_int64()
+        st = lib.ora_tile_count(A.n, _p(A.rp), _p(A.ci), int(T), C.byref(nt), C.byref(nz),
+                                C.byref(ns))
         if st != OK:
             raise ValueError(f"tile count failed: status {st}")
         self.n, self.T = A.n, int(T)
         self.nrb = (A.n + T - 1) // T
-        self.ntiles, self.nnz = nt.value, nz.value
+        self.ntiles, self.nnz, self.nslots = nt.value, nz.value, ns.value
         self.tileRowPtr = np.empty(self.nrb + 1, np.int64)
         self.tileColIdx = np.empty(max(self.ntiles, 1), np.int32)
         self.tileNnzOff = np.empty(self.ntiles + 1, np.int64)
-        self.rowEnd = np.empty(max(self.ntiles * T, 1), np.uint16)
-        self.colIdx = np.empty(max(self.nnz, 1), np.uint8)
-        self.v64 = np.empty(max(self.nnz, 1), np.float64)
-        self.v32 = np.empty(max(self.nnz, 1), np.float32)
-        self.v16 = np.empty(max(self.nnz, 1), np.uint16)
+        self.rowMask = np.empty(max(self.ntiles, 1), np.uint64)
+        self.tileWidth = np.empty(max(self.ntiles, 1), np.uint8)
+        self.colIdx = np.empty(max(self.nslots, 1), np.uint8)
+        self.v64 = np.empty(max(self.nslots, 1), np.float64)
+        self.v32 = np.empty(max(self.nslots, 1), np.float32)
+        self.v16 = np.empty(max(self.nslots, 1), np.uint16)
         self.colExp = np.empty(max(A.n, 1), np.int8)
         st = lib.ora_tile_build(A.n, _p(A.rp), _p(A.ci), _p(A.v), int(T), _p(self.tileRowPtr),
-                                _p(self.tileColIdx), _p(self.tileNnzOff), _p(self.rowEnd),
-                                _p(self.colIdx), _p(self.v64), _p(self.v32), _p(self.v16),
-                                _p(self.colExp))
+                                _p(self.tileColIdx), _p(self.tileNnzOff), _p(self.rowMask),
+                                _p(self.tileWidth), _p(self.colIdx), _p(self.v64), _p(self.v32),
+                                _p(self.v16), _p(self.colExp))
         if st != OK:
             raise ValueError(f"tile build failed: status {st}")
         self.tileColIdx = self.tileColIdx[: self.ntiles]
-        self.rowEnd = self.rowEnd[: self.ntiles * T]
-        self.colIdx, self.v64 = self.colIdx[: self.nnz], self.v64[: self.nnz]
-        self.v32, self.v16 = self.v32[: self.nnz], self.v16[: self.nnz]
+        self.rowMask, self.tileWidth = self.rowMask[: self.ntiles], self.tileWidth[: self.ntiles]
+        self.colIdx, self.v64 = self.colIdx[: self.nslots], self.v64[: self.nslots]
+        self.v32, self.v16 = self.v32[: self.nslots], self.v16[: self.nslots]
         self.colExp = self.colExp[: A.n]
 
     def tile_rows(self):
         """Row-block index of every tile."""
         return np.repeat(np.arange(self.nrb, dtype=np.int64), np.diff(self.tileRowPtr))
+
+    def tile_entries(self):
+        """Stored entries (slots that are not pads) of every tile."""
+        real = (self.colIdx < self.T).astype(np.int64)
+        c = np.concatenate([[0], np.cumsum(real)])
+        return c[self.tileNnzOff[1:]] - c[self.tileNnzOff[:-1]]
+
+    def slots(self, t):
+        """(local row, slot index) of every slot of tile t, slot order."""
+        m = int(self.rowMask[t])
+        rows = [r for r in range(self.T) if (m >> r) & 1]
+        h, w, off = len(rows), int(self.tileWidth[t]), int(self.tileNnzOff[t])
+        return [(rows[j], off + k * h + j) for k in range(w) for j in range(h)]
 
     def to_csr(self) -> CSR:
         """Rebuild CSR (FP64 stream) from the layout: the round-trip check."""
@@ -169,15 +188,12 @@ class Tiles:
         rows, cols, vals = [], [], []
         trow = self.tile_rows()
         for t in range(self.ntiles):
-            off = int(self.tileNnzOff[t])
-            start = 0
-            for r in range(T):
-                end = int(self.rowEnd[t * T + r])
-                for k in range(off + start, off + end):
-                    rows.append(trow[t] * T + r)
-                    cols.append(int(self.tileColIdx[t]) * T + int(self.colIdx[k]))
-                    vals.append(self.v64[k])
-                start = end
+            for r, s in self.slots(t):
+                if self.colIdx[s] == T:
+                    continue
+                rows.append(trow[t] * T + r)
+                cols.append(int(self.tileColIdx[t]) * T + int(self.colIdx[s]))
+                vals.append(self.v64[s])
         rows, cols, vals = np.array(rows, np.int64), np.array(cols, np.int64), np.array(vals)
         order = np.lexsort((cols, rows))
         rows, cols, vals = rows[order], cols[order], vals[order]

@@ -24,10 +24,11 @@
  *  - A low-precision tile multiplies RN(a_ij / s_j) by RN(x_j) (the x entry rounded
  *    to the tile's own format) and scales the product by s_j. Both factors have at
  *    most 24 significant bits, so the FP64 product is exact.
- *  - Intra-tile order is row-major: a tile stores, row by row, the (local column,
- *    value) pairs of its nonzeros in ascending column order, with one end offset
- *    per local row. The inter-tile level is CSR over row blocks as in EvoCG
- *    Fig. 4(a).
+ *  - Intra-tile order is slot-major over the tile's nonempty rows: a row mask
+ *    names them, the tile is padded to a w x h rectangle (w = its longest row,
+ *    h = its nonempty rows) and slot (k, j) holds the k-th entry of the j-th
+ *    nonempty row, so that one lane per row reads consecutive slots. The
+ *    inter-tile level is CSR over row blocks as in EvoCG Fig. 4(a).
  *
  * Parity pins live in tests/test_oracle_*.py. The MLP controller is pinned only
  * through special cases and invariances (its weights are seeded, not trained):
@@ -153,83 +154,128 @@ void ora_col_exp(int64_t n, const int64_t *rp, const int32_t *ci, const double *
 /* §3.3.2: three value streams over one set of indices).                     */
 /* ------------------------------------------------------------------------ */
 
-/* Count the nonempty T x T tiles and stored entries. */
-int ora_tile_count(int64_t n, const int64_t *rp, const int32_t *ci, int T,
-                   int64_t *ntiles_out, int64_t *nnz_out)
+/* Entries of local row r of row block rb that fall in column block cb: the
+ * half-open CSR range [*k0, *k1). cur[r] is where the row's scan stands. */
+static void row_range_in_block(const int64_t *rp, const int32_t *ci, int64_t row,
+                               int64_t cur, int64_t cb, int T, int64_t *k0, int64_t *k1)
 {
-    if (T < 1 || n < 0) return ORA_EINVAL;
-    int64_t nrb = (n + T - 1) / T, ntiles = 0;
-    int64_t *cur = (int64_t *)malloc(sizeof(int64_t) * (size_t)T);
+    int64_t k = cur;
+    *k0 = k;
+    while (k < rp[row + 1] && ci[k] / T == cb) k++;
+    *k1 = k;
+}
+
+/* Smallest column block still unvisited among the rows of a row block, or -1. */
+static int64_t next_col_block(const int64_t *rp, const int32_t *ci, int64_t r0, int64_t nr,
+                              const int64_t *cur, int T)
+{
+    int64_t cbmin = -1;
+    for (int64_t r = 0; r < nr; ++r)
+        if (cur[r] < rp[r0 + r + 1]) {
+            int64_t cb = ci[cur[r]] / T;
+            if (cbmin < 0 || cb < cbmin) cbmin = cb;
+        }
+    return cbmin;
+}
+
+/* Count the nonempty T x T tiles, the stored entries and the slots of the layout
+ * below (entries plus the padding that makes every tile a w x h rectangle). */
+int ora_tile_count(int64_t n, const int64_t *rp, const int32_t *ci, int T,
+                   int64_t *ntiles_out, int64_t *nnz_out, int64_t *nslots_out)
+{
+    if (T < 1 || T > 64 || n < 0) return ORA_EINVAL;
+    int64_t nrb = (n + T - 1) / T, ntiles = 0, nslots = 0;
+    int64_t cur[64];
     for (int64_t rb = 0; rb < nrb; ++rb) {
         int64_t r0 = rb * T, nr = (n - r0 < T) ? n - r0 : T;
         for (int64_t r = 0; r < nr; ++r) cur[r] = rp[r0 + r];
         for (;;) {
-            int64_t cbmin = -1;
-            for (int64_t r = 0; r < nr; ++r)
-                if (cur[r] < rp[r0 + r + 1]) {
-                    int64_t cb = ci[cur[r]] / T;
-                    if (cbmin < 0 || cb < cbmin) cbmin = cb;
-                }
-            if (cbmin < 0) break;
-            for (int64_t r = 0; r < nr; ++r)
-                while (cur[r] < rp[r0 + r + 1] && ci[cur[r]] / T == cbmin) cur[r]++;
+            int64_t cb = next_col_block(rp, ci, r0, nr, cur, T);
+            if (cb < 0) break;
+            int64_t h = 0, w = 0;
+            for (int64_t r = 0; r < nr; ++r) {
+                int64_t k0, k1;
+                row_range_in_block(rp, ci, r0 + r, cur[r], cb, T, &k0, &k1);
+                if (k1 > k0) h++;
+                if (k1 - k0 > w) w = k1 - k0;
+                cur[r] = k1;
+            }
+            nslots += w * h;
             ntiles++;
         }
     }
-    free(cur);
     *ntiles_out = ntiles;
     *nnz_out = (n > 0) ? rp[n] : 0;
+    *nslots_out = nslots;
     return ORA_OK;
 }
 
-/* Fill the layout. Tiles of a row block are listed in ascending column block;
- * inside a tile, rows in ascending order, and inside a row, columns in
- * ascending order. rowEnd[t*T + r] is the end of local row r, counted from the
- * tile's first entry; rows past n have length zero. */
+/* Fill the layout. Inter-tile level (EvoCG Fig. 4(a)): CSR over row blocks, the
+ * tiles of a row block in ascending column block. Inside a tile:
+ *   rowMask[t]  bit r set when local row r has at least one entry in the tile;
+ *   tileWidth[t] w = the largest number of entries of one local row in the tile;
+ *   the tile's h = popcount(rowMask[t]) nonempty rows, ascending, are numbered
+ *   j = 0..h-1, and slot (k, j), k = 0..w-1, sits at tileNnzOff[t] + k*h + j: it
+ *   holds the k-th entry (ascending column) of row j, or, when that row has k or
+ *   fewer entries, a pad: local column T (one past the last column, like the
+ *   sentinel row index of EvoCG Fig. 4(b)) and value +0 in all three streams.
+ * tileNnzOff counts slots; colIdx and the value streams have one element per slot. */
 int ora_tile_build(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int T,
                    int64_t *tileRowPtr, int32_t *tileColIdx, int64_t *tileNnzOff,
-                   uint16_t *rowEnd, uint8_t *colIdx, double *v64, float *v32,
-                   uint16_t *v16, int8_t *colExp)
+                   uint64_t *rowMask, uint8_t *tileWidth, uint8_t *colIdx, double *v64,
+                   float *v32, uint16_t *v16, int8_t *colExp)
 {
-    if (T < 1 || T > 255 || n < 0) return ORA_EINVAL;
+    if (T < 1 || T > 64 || n < 0) return ORA_EINVAL;
     ora_col_exp(n, rp, ci, v, colExp);
     int64_t nrb = (n + T - 1) / T, t = 0, pos = 0;
-    int64_t *cur = (int64_t *)malloc(sizeof(int64_t) * (size_t)T);
+    int64_t cur[64], k0[64], k1[64];
     tileRowPtr[0] = 0;
     for (int64_t rb = 0; rb < nrb; ++rb) {
         int64_t r0 = rb * T, nr = (n - r0 < T) ? n - r0 : T;
         for (int64_t r = 0; r < nr; ++r) cur[r] = rp[r0 + r];
         for (;;) {
-            int64_t cbmin = -1;
-            for (int64_t r = 0; r < nr; ++r)
-                if (cur[r] < rp[r0 + r + 1]) {
-                    int64_t cb = ci[cur[r]] / T;
-                    if (cbmin < 0 || cb < cbmin) cbmin = cb;
-                }
-            if (cbmin < 0) break;
-            tileColIdx[t] = (int32_t)cbmin;
-            tileNnzOff[t] = pos;
-            for (int64_t r = 0; r < T; ++r) {
-                if (r < nr) {
-                    while (cur[r] < rp[r0 + r + 1] && ci[cur[r]] / T == cbmin) {
-                        int64_t k = cur[r]++;
-                        int j = ci[k];
-                        int ej = colExp[j];
-                        colIdx[pos] = (uint8_t)(j - cbmin * T);
-                        v64[pos] = v[k];
-                        v32[pos] = f32_of(ldexp(v[k], -ej));
-                        v16[pos] = bf16_bits_of(ldexp(v[k], -ej));
-                        pos++;
-                    }
-                }
-                rowEnd[t * T + r] = (uint16_t)(pos - tileNnzOff[t]);
+            int64_t cb = next_col_block(rp, ci, r0, nr, cur, T);
+            if (cb < 0) break;
+            uint64_t mask = 0;
+            int64_t h = 0, w = 0;
+            for (int64_t r = 0; r < nr; ++r) {
+                row_range_in_block(rp, ci, r0 + r, cur[r], cb, T, &k0[r], &k1[r]);
+                if (k1[r] > k0[r]) { mask |= (uint64_t)1 << r; h++; }
+                if (k1[r] - k0[r] > w) w = k1[r] - k0[r];
+                cur[r] = k1[r];
             }
+            tileColIdx[t] = (int32_t)cb;
+            tileNnzOff[t] = pos;
+            rowMask[t] = mask;
+            tileWidth[t] = (uint8_t)w;
+            for (int64_t kk = 0; kk < w; ++kk) {
+                int64_t j = 0;
+                for (int64_t r = 0; r < nr; ++r) {
+                    if (!((mask >> r) & 1)) continue;
+                    int64_t slot = pos + kk * h + j;
+                    if (k0[r] + kk < k1[r]) {
+                        int64_t k = k0[r] + kk;
+                        int c = ci[k];
+                        int ec = colExp[c];
+                        colIdx[slot] = (uint8_t)(c - cb * T);
+                        v64[slot] = v[k];
+                        v32[slot] = f32_of(ldexp(v[k], -ec));
+                        v16[slot] = bf16_bits_of(ldexp(v[k], -ec));
+                    } else {
+                        colIdx[slot] = (uint8_t)T;
+                        v64[slot] = 0.0;
+                        v32[slot] = 0.0f;
+                        v16[slot] = 0;
+                    }
+                    j++;
+                }
+            }
+            pos += w * h;
             t++;
         }
         tileRowPtr[rb + 1] = t;
     }
     tileNnzOff[t] = pos;
-    free(cur);
     return ORA_OK;
 }
 

@@ -57,7 +57,7 @@ def test_cg_mixed_static_map_laplacian():
     assert oracle.true_residual(P.A, w.b, x) <= w.rtol
     assert abs(info["true_res"] - oracle.true_residual(P.A, w.b, x)) <= 1e-3 * w.rtol
     # precision census: every SpMV of the first pass reads the static map
-    per = np.bincount(mp, weights=np.diff(P.t.tileNnzOff), minlength=3).astype(np.int64)
+    per = np.bincount(mp, weights=P.t.tile_entries(), minlength=3).astype(np.int64)
     rec = info["iters_recursive"]
     rest = info["iters"] - rec
     want = per * rec + np.array([P.t.nnz * rest, 0, 0])

@@ -127,7 +127,7 @@ def test_precision_census():
     A, t = _setup((w.n, w.rp, w.ci, w.v), w.T)
     mp = W.tile_map(t.tile_rows(), t.tileColIdx, t.nrb, 1)
     r = oracle.cg(A, t, w.b, 1e-10, 3000, tile_map=mp)
-    per = np.bincount(mp, weights=np.diff(t.tileNnzOff), minlength=3)
+    per = np.bincount(mp, weights=t.tile_entries(), minlength=3)
     assert np.array_equal(r["prec_nnz"], (per * r["iters"]).astype(np.int64))
 
 

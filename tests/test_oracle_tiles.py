@@ -27,6 +27,39 @@ def _cases():
     yield "banded", W.banded_spd(9000, 6, band=300), 64
 
 
+def _check_slots(t, A):
+    """Slot invariants: every tile is a w x h rectangle over its nonempty rows; in each
+    row the real entries come first with strictly ascending local columns, then pads
+    (column T, value +0 in every stream); some row fills the width; the real entries
+    are exactly the CSR entries."""
+    T = t.T
+    h = np.array([bin(int(m)).count("1") for m in t.rowMask], np.int64)
+    assert np.all(h >= 1) and np.all(t.tileWidth >= 1)
+    assert np.array_equal(np.diff(t.tileNnzOff), h * t.tileWidth.astype(np.int64))
+    assert t.tileNnzOff[-1] == t.nslots and t.tileNnzOff[0] == 0
+    n_real = 0
+    last_rb = (t.n - 1) // T if t.n else -1
+    for tt in range(t.ntiles):
+        w, hh, off = int(t.tileWidth[tt]), int(h[tt]), int(t.tileNnzOff[tt])
+        if t.tile_rows()[tt] == last_rb and t.n % T:
+            assert int(t.rowMask[tt]) >> (t.n % T) == 0        # no rows past n
+        c = t.colIdx[off:off + w * hh].reshape(w, hh).astype(np.int64)
+        real = c < T
+        assert np.all(real[0])                                 # listed rows are nonempty
+        assert np.all(real[:-1] >= real[1:])                   # pads only after entries
+        assert np.any(real[-1])                                # the width is attained
+        cc = np.where(real, c, 10 ** 6)
+        assert np.all(np.diff(cc, axis=0)[real[1:]] > 0)       # ascending columns
+        pads = ~real.ravel()
+        sl = slice(off, off + w * hh)
+        assert np.all(c.ravel()[pads] == T)
+        assert np.all(t.v64[sl][pads].view(np.uint64) == 0)
+        assert np.all(t.v32[sl][pads].view(np.uint32) == 0) and np.all(t.v16[sl][pads] == 0)
+        n_real += int(real.sum())
+    assert n_real == A.rp[-1] == t.nnz
+    assert np.array_equal(t.tile_entries().sum(), t.nnz)
+
+
 @pytest.mark.parametrize("name,m,T", list(_cases()), ids=[c[0] for c in _cases()])
 def test_round_trip_and_invariants(name, m, T):
     A = _csr(m)
@@ -41,11 +74,7 @@ def test_round_trip_and_invariants(name, m, T):
     for rb in range(t.nrb):
         cbs = t.tileColIdx[t.tileRowPtr[rb]:t.tileRowPtr[rb + 1]]
         assert np.all(np.diff(cbs) > 0)
-    re = t.rowEnd.reshape(t.ntiles, T).astype(np.int64)
-    assert np.all(np.diff(re, axis=1) >= 0)
-    assert np.array_equal(re[:, -1], np.diff(t.tileNnzOff))
-    assert np.all(re[:, 0] >= 0) and np.all(t.colIdx < T)
-    assert t.tileNnzOff[-1] == A.rp[-1] == t.nnz
+    _check_slots(t, A)
     # tile count taken another way: distinct (row block, column block) pairs
     rows = np.repeat(np.arange(A.n), np.diff(A.rp))
     pairs = np.unique((rows // T) * ((A.n + T - 1) // T) + A.ci // T)
@@ -60,19 +89,16 @@ def test_value_streams_follow_column_scale():
     np.maximum.at(colmax, A.ci, np.abs(A.v))
     e = np.frexp(colmax)[1] - 1
     assert np.array_equal(t.colExp.astype(int), np.clip(e, -100, 100))
-    # every stored entry: locate it in CSR through the round trip order
-    back_cols = []
-    trow = t.tile_rows()
+    # every stored entry: its global column through the slots of its tile
+    back_cols, idx = [], []
     for tt in range(t.ntiles):
-        off, start = int(t.tileNnzOff[tt]), 0
-        for r in range(32):
-            end = int(t.rowEnd[tt * 32 + r])
-            for k in range(off + start, off + end):
-                back_cols.append(int(t.tileColIdx[tt]) * 32 + int(t.colIdx[k]))
-            start = end
-    j = np.array(back_cols)
-    scaled = np.ldexp(t.v64, -t.colExp[j].astype(int))
-    assert np.array_equal(t.v32, scaled.astype(np.float32))
+        for r, s in t.slots(tt):
+            if t.colIdx[s] < 32:
+                back_cols.append(int(t.tileColIdx[tt]) * 32 + int(t.colIdx[s]))
+                idx.append(s)
+    j, idx = np.array(back_cols), np.array(idx)
+    scaled = np.ldexp(t.v64[idx], -t.colExp[j].astype(int))
+    assert np.array_equal(t.v32[idx], scaled.astype(np.float32))
     smax = np.zeros(A.n)
     np.maximum.at(smax, j, np.abs(scaled))
     assert np.all((smax >= 1.0) & (smax < 2.0))  # each column's largest scaled entry is in [1, 2)
@@ -91,9 +117,11 @@ def test_empty_rows_and_columns():
     assert t.nrb == 2
     assert list(t.tileRowPtr) == [0, 2, 4]
     assert list(t.tileColIdx) == [0, 1, 0, 1]
-    re = t.rowEnd.reshape(-1, 16)
-    assert re[0, 3] == re[0, 2] and re[0, 5] == re[0, 4]       # empty local rows
-    assert list(re[3, 4:]) == [re[3, 3]] * 12                  # rows past n in the last block
+    m = [int(x) for x in t.rowMask]
+    assert (m[0] >> 3) & 1 == 0 and (m[0] >> 5) & 1 == 0        # empty local rows
+    assert m[0] == 0xFFFF & ~(1 << 3) & ~(1 << 5) and m[1] == 1   # row 0 reaches column 19
+    assert m[3] == 0xF and m[2] == 1 << 3                         # rows past n are absent
+    assert list(t.tileWidth) == [1, 1, 1, 1]
     back = t.to_csr()
     assert np.array_equal(back.ci, A.ci)
 
@@ -135,6 +163,15 @@ def _count_5pt(nx, ny, T):
     return nb * ny + 2 * (nb - 1) * ny + 2 * nb * (ny - 1)
 
 
+def _slots_5pt(nx, ny, T):
+    """Slots of the 5-point stencil with T | nx and T >= 3: a row block's own tile holds
+    x-1, x, x+1 (width 3 over all T rows; its first and last rows have two entries and
+    one pad each), the left / right tiles one entry each, the tiles of the lines above and
+    below one entry in every row."""
+    nb = nx // T
+    return nb * ny * 3 * T + 2 * (nb - 1) * ny + 2 * nb * (ny - 1) * T
+
+
 def _count_7pt(N, T):
     nb = N // T
     lines = N * N
@@ -144,10 +181,31 @@ def _count_7pt(N, T):
 def test_stencil_tile_counts_closed_form():
     t1 = oracle.Tiles(_csr(W.laplace2d_5pt(64)), 16)
     assert t1.ntiles == _count_5pt(64, 64, 16) == 1144        # the 64x64 Laplacian workload
+    assert t1.nslots == _slots_5pt(64, 64, 16)
+    assert t1.nslots - t1.nnz == 2 * (64 // 16) * 64           # two pads per own tile
     t2 = oracle.Tiles(_csr(W.laplace2d_5pt(96, 40)), 32)
     assert t2.ntiles == _count_5pt(96, 40, 32)
+    assert t2.nslots == _slots_5pt(96, 40, 32)
     t3 = oracle.Tiles(_csr(W.diffusion3d_7pt(32, 1)), 32)
     assert t3.ntiles == _count_7pt(32, 32)
     t4 = oracle.Tiles(_csr(W.diffusion3d_7pt(64, 1)), 32)
     assert t4.ntiles == _count_7pt(64, 32)
     assert _count_7pt(128, 32) == 423936                       # the 128^3 workload
+
+
+def test_slot_order_worked_example():
+    """A 4 x 4 tile worked out by hand from the slot definition: rows 0, 2, 3 are
+    nonempty (mask 0b1101, h = 3), row 3 is the longest (w = 3). Slot (k, j) at k*h + j
+    holds the k-th entry of the j-th nonempty row, else a pad (column 4):
+        k = 0: row 0 -> col 0, row 2 -> col 1, row 3 -> col 0
+        k = 1: row 0 -> col 2, row 2 -> pad,   row 3 -> col 1
+        k = 2: row 0 -> pad,   row 2 -> pad,   row 3 -> col 3"""
+    M = np.zeros((4, 4))
+    M[0, 0], M[0, 2] = 1.0, 2.0
+    M[2, 1] = 3.0
+    M[3, 0], M[3, 1], M[3, 3] = 4.0, 5.0, 6.0
+    t = oracle.Tiles(_csr(W.dense_to_csr(M)), 4)
+    assert t.ntiles == 1 and int(t.rowMask[0]) == 0b1101 and int(t.tileWidth[0]) == 3
+    assert list(t.colIdx) == [0, 1, 0, 2, 4, 1, 4, 4, 3]
+    assert list(t.v64) == [1.0, 3.0, 4.0, 2.0, 0.0, 5.0, 0.0, 0.0, 6.0]
+    assert t.nslots == 9 and t.nnz == 6
