@@ -105,15 +105,6 @@ def _workload(cfg):
     return W.workload(cfg)
 
 
-def _spmv_bytes(desc_n, ntiles, nrb, T, nnz_by_prec):
-    """Algorithmic bytes of one SpMV launch: the active value stream of every tile, one
-    local-column byte per entry, the tile's row ends (2T) and descriptor (column block 4,
-    entry offset 8, precision code 1), the row-block pointers, x read once, y written once."""
-    vals = 8 * nnz_by_prec[0] + 4 * nnz_by_prec[1] + 2 * nnz_by_prec[2]
-    nnz = sum(nnz_by_prec)
-    return vals + nnz + ntiles * (2 * T + 13) + 8 * (nrb + 1) + 16 * desc_n
-
-
 def _traffic_for(kernel_src_hash):
     """Per-launch DRAM bytes of the SpMV from the committed ncu summary, if it was taken
     on the current kernel source (else None)."""
@@ -207,7 +198,7 @@ def run_ours(args):
     import numpy as np
     import torch
 
-    from mixed_precision_sparse_gb300 import evocg
+    from mixed_precision_sparse_gb300 import evocg, spmv_run
     from mixed_precision_sparse_gb300 import workloads as W
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -309,7 +300,7 @@ def run_ours(args):
     # ---- the dominant kernel (the SpMV) timed alone on the same stream, CUDA events,
     # back-to-back launches (inputs > L2), with the seeded 40/40/20 mixed map and all-FP64
     trow, ex = G.tile_rows()
-    tnnz = np.diff(ex["tileNnzOff"])
+    tnnz = spmv_run.tile_entries(ex, G.T)
     peak, peak_kind = _peaks()
     xs = torch.from_numpy(np.random.default_rng(7).uniform(-1, 1, w.n)).to(dev)
     ys = torch.empty_like(xs)
@@ -329,7 +320,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1000.0 / reps
         per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
-        B = _spmv_bytes(w.n, G.ntiles, G.nrb, w.T, per)
+        B = spmv_run.spmv_bytes(w.n, G.ntiles, G.nrb, per)
         spmv[label] = {"us": us, "bytes": int(B), "gbs": B / us / 1e3,
                        "frac_of_peak": B / us / 1e3 / peak, "frac_of_8tbs": B / us / 1e3 / 8000.0}
     src_hash = _src_hash()

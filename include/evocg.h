@@ -66,8 +66,9 @@ typedef struct {
     int64_t nnz;          /* stored entries */
     int32_t tile_size;    /* T: tiles are T x T */
     int32_t map_kind;     /* which map the SpMV reads (EVOCG_MAP_*) */
-    int64_t bytes_index;  /* tileRowPtr + tileColIdx + tileNnzOff + rowEnd + colIdx */
-    int64_t bytes_v64, bytes_v32, bytes_v16, bytes_colexp;
+    int64_t bytes_index;  /* tileRowPtr + tileColIdx + tileNnzOff + rowMask + tileWidth + colIdx */
+    int64_t bytes_v64, bytes_v32, bytes_v16, bytes_colexp;   /* per value stream (slots) */
+    int64_t nslots;       /* slots of the value streams: entries plus row padding */
 } evocg_tiles_desc;
 
 typedef struct {
@@ -89,17 +90,21 @@ typedef struct {
     int restarts;          /* FP64-finish restarts taken */
     double rel_res;        /* last recursively updated ||r_k|| / ||r_0|| */
     double true_res;       /* ||b - A x|| / ||b|| recomputed in FP64 (all tiles FP64), or -1 */
-    int64_t prec_nnz[3];   /* stored entries processed per precision, summed over SpMVs */
+    int64_t prec_nnz[3];   /* stored entries (pads not counted) processed per precision,
+                              summed over SpMVs */
     int64_t ctrl_calls;    /* controller invocations */
 } evocg_solve_info;
 
 /*
  * Build the tile structure (EvoCG §3.3.1 Fig. 4(a) and §3.3.2): row blocks of
  * tile_size rows, the nonempty tile_size x tile_size tiles of each row block listed in
- * ascending column block (tileRowPtr / tileColIdx), inside a tile the entries row by
- * row with ascending column (one end offset per local row in rowEnd, one local column
- * per entry in colIdx), and three value streams over the same entries: FP64 a_ij, FP32
- * and BF16 of a_ij / s_j, where s_j = 2^e_j is the per-column factor of §3.3.2 with
+ * ascending column block (tileRowPtr / tileColIdx). Inside a tile: rowMask (bit r: local
+ * row r has entries in the tile), tileWidth w (its longest row) and w x h slots, h =
+ * popcount(rowMask), in slot-major order: slot (k, j) at tileNnzOff[t] + k*h + j holds the
+ * k-th entry (ascending column) of the j-th nonempty row, or a pad (local column T,
+ * value +0) when that row has k or fewer entries. One local column byte per slot
+ * (colIdx) and three value streams over the same slots: FP64 a_ij, FP32 and BF16 of
+ * a_ij / s_j, where s_j = 2^e_j is the per-column factor of §3.3.2 with
  * e_j = floor(log2 max_i |a_ij|) clamped to [-100, 100] (0 for an empty column). FP32 and
  * BF16 values are rounded once from FP64, to nearest with ties to even.
  *   n, row_ptr (n+1, int64), col_idx (row_ptr[n], int32, strictly ascending per row,
@@ -121,13 +126,14 @@ int evocg_tiles_info(evocg_tiles_t A, evocg_tiles_desc *d);
 
 /*
  * Copy the structure back to HOST arrays, for bit-exact layout checks. Sizes:
- * tileRowPtr nrb+1, tileColIdx ntiles, tileNnzOff ntiles+1, rowEnd ntiles*T,
- * colIdx / v64 / v32 / v16 nnz, colExp n. Any pointer may be NULL to skip that array.
- * Synchronises the device.
+ * tileRowPtr nrb+1, tileColIdx ntiles, tileNnzOff ntiles+1, rowMask ntiles,
+ * tileWidth ntiles, colIdx / v64 / v32 / v16 nslots, colExp n. Any pointer may be NULL to
+ * skip that array. Synchronises the device.
  */
 int evocg_tiles_export(evocg_tiles_t A, int64_t *tileRowPtr, int32_t *tileColIdx,
-                       int64_t *tileNnzOff, uint16_t *rowEnd, uint8_t *colIdx, double *v64,
-                       float *v32, uint16_t *v16, int8_t *colExp);
+                       int64_t *tileNnzOff, uint64_t *rowMask, uint8_t *tileWidth,
+                       uint8_t *colIdx, double *v64, float *v32, uint16_t *v16,
+                       int8_t *colExp);
 
 /*
  * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
@@ -158,15 +164,18 @@ enum {
     EVOCG_SPMV_REUSE_XCOPIES = 1, /* skip rounding x: reuse the FP32/BF16 copies of x made by
                                      the previous evocg_spmv / evocg_spmv_ex call on this
                                      handle; x must hold the same values as in that call */
-    EVOCG_SPMV_DIRECT = 2         /* run the direct kernel (every operand read from global
-                                     memory by the lanes) instead of the staged one (operands
-                                     copied into shared memory by bulk asynchronous copies).
-                                     For tiles of 32 and 64 both compute the same sums in the
-                                     same order; for tiles of 16 the direct kernel splits a row
-                                     block's tiles over two half-warps (same sums to rounding).
-                                     The staged kernel is the default when x is 16-byte
-                                     aligned and the tiles hold at least 12 entries on average
-                                     (the direct kernel is faster for sparser tiles) */
+    EVOCG_SPMV_DIRECT = 2,        /* run the direct kernel: a warp per row block, every operand
+                                     loaded by the lanes from global memory, one tile after
+                                     the other */
+    EVOCG_SPMV_STAGED = 4         /* run the staged kernel (the default where it can run): a
+                                     producer warp copies each tile's value slice and x segment
+                                     into shared memory by bulk asynchronous copies for two
+                                     consumer warps (needs 16-byte aligned x; the direct kernel
+                                     runs otherwise). Both kernels sum every row in ascending
+                                     column with the same arithmetic; for tiles of 32 and 64
+                                     they give the same bits; for tiles of 16 the direct kernel
+                                     splits a row block's tiles over two half-warps (same sums
+                                     to rounding). At most one of DIRECT, STAGED may be set */
 };
 
 /*

@@ -299,7 +299,7 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     if (!A) { H.release(); return fail(EVOCG_ENOMEM, "host allocation"); }
     cudaGetDevice(&A->device);
     A->sms = sms;
-    A->n = H.n; A->nrb = H.nrb; A->ntiles = H.ntiles; A->nnz = H.nnz; A->T = H.T;
+    A->n = H.n; A->nrb = H.nrb; A->ntiles = H.ntiles; A->nnz = H.nnz; A->nslots = H.nslots; A->T = H.T;
     A->diag_ok = H.diag_ok;
     cudaError_t e = cudaSuccess;
     auto up = [&](auto **dst, const auto *src, int64_t count) {
@@ -312,11 +312,12 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     up(&A->tileColIdx, H.tileColIdx, H.ntiles);
     up(&A->tileNnzOff, H.tileNnzOff, H.ntiles + 1);
     up(&A->tileRowIdx, H.tileRowIdx, H.ntiles);
-    up(&A->rowEnd, H.rowEnd, H.ntiles * H.T);
-    up(&A->colIdx, H.colIdx, H.nnz);
-    up(&A->v64, H.v64, H.nnz);
-    up(&A->v32, H.v32, H.nnz);
-    up(&A->v16, H.v16, H.nnz);
+    up(&A->rowMask, H.rowMask, H.ntiles);
+    up(&A->tileWidth, H.tileWidth, H.ntiles);
+    up(&A->colIdx, H.colIdx, H.nslots);
+    up(&A->v64, H.v64, H.nslots);
+    up(&A->v32, H.v32, H.nslots);
+    up(&A->v16, H.v16, H.nslots);
     up(&A->colExp, H.colExp, H.n);
     up(&A->dinv, H.dinv, H.n);
     // The staged kernel pays a fixed issue cost per batch of tiles and stages each tile's
@@ -325,7 +326,7 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     // on average at least kStagedMinEntries entries.
     constexpr int64_t kStagedMinEntries = 12;
     StagedLimits lim;
-    if (e == cudaSuccess && H.nrb > 0 && H.nnz >= kStagedMinEntries * H.ntiles && staged_limits(H.T, &lim)) {
+    if (e == cudaSuccess && H.nrb > 0 && H.nslots >= kStagedMinEntries * H.ntiles && staged_limits(H.T, &lim)) {
         const int grid = staged_grid_for(H.T, sms);
         if (grid > 0) {
             std::vector<int32_t> wr, wbt;
@@ -362,6 +363,12 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
         return code;
     }
     A->spmv_grid = spmv_grid_for(A->T, sms);
+    // Default kernel: the staged one where its plan exists and x is aligned, else the
+    // direct one; EVOCG_SPMV_KERNEL=direct selects the direct kernel for every SpMV of the
+    // matrices built afterwards.
+    A->spmv_kind = SPMV_KIND_AUTO;
+    if (const char *k = std::getenv("EVOCG_SPMV_KERNEL"))
+        if (!std::strcmp(k, "direct")) A->spmv_kind = SPMV_KIND_DIRECT;
     A->vec_grid = sms * 4 > kMaxBlocks ? kMaxBlocks : sms * 4;
     *out = A;
     return EVOCG_OK;
@@ -373,7 +380,7 @@ extern "C" int evocg_tiles_free(evocg_tiles_t A)
     cudaDeviceSynchronize();
     release_ws(A->ws);
     dfree(A->tileRowPtr); dfree(A->tileColIdx); dfree(A->tileNnzOff); dfree(A->tileRowIdx);
-    dfree(A->rowEnd); dfree(A->warpRb); dfree(A->warpBatch); dfree(A->batchTile);
+    dfree(A->rowMask); dfree(A->tileWidth); dfree(A->warpRb); dfree(A->warpBatch); dfree(A->batchTile);
     dfree(A->tileSlot); dfree(A->errw);
     dfree(A->colIdx); dfree(A->v64); dfree(A->v32); dfree(A->v16); dfree(A->colExp);
     dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16f);
@@ -387,18 +394,20 @@ extern "C" int evocg_tiles_info(evocg_tiles_t A, evocg_tiles_desc *d)
     if (!A || !d) return fail(EVOCG_EINVAL, "NULL argument");
     d->n = A->n; d->nrb = A->nrb; d->ntiles = A->ntiles; d->nnz = A->nnz; d->tile_size = A->T;
     d->map_kind = A->map_kind;
-    d->bytes_index = 8 * (A->nrb + 1) + 4 * A->ntiles + 8 * (A->ntiles + 1) +
-                     2 * A->ntiles * A->T + A->nnz;
-    d->bytes_v64 = 8 * A->nnz;
-    d->bytes_v32 = 4 * A->nnz;
-    d->bytes_v16 = 2 * A->nnz;
+    d->nslots = A->nslots;
+    d->bytes_index = 8 * (A->nrb + 1) + 4 * A->ntiles + 8 * (A->ntiles + 1) + 9 * A->ntiles +
+                     A->nslots;
+    d->bytes_v64 = 8 * A->nslots;
+    d->bytes_v32 = 4 * A->nslots;
+    d->bytes_v16 = 2 * A->nslots;
     d->bytes_colexp = A->n;
     return EVOCG_OK;
 }
 
 extern "C" int evocg_tiles_export(evocg_tiles_t A, int64_t *tileRowPtr, int32_t *tileColIdx,
-                                  int64_t *tileNnzOff, uint16_t *rowEnd, uint8_t *colIdx,
-                                  double *v64, float *v32, uint16_t *v16, int8_t *colExp)
+                                  int64_t *tileNnzOff, uint64_t *rowMask, uint8_t *tileWidth,
+                                  uint8_t *colIdx, double *v64, float *v32, uint16_t *v16,
+                                  int8_t *colExp)
 {
     if (!A) return fail(EVOCG_EINVAL, "NULL handle");
     CK(cudaDeviceSynchronize(), "synchronise");
@@ -409,11 +418,12 @@ extern "C" int evocg_tiles_export(evocg_tiles_t A, int64_t *tileRowPtr, int32_t 
     CK(dn(tileRowPtr, A->tileRowPtr, A->nrb + 1), "export tileRowPtr");
     CK(dn(tileColIdx, A->tileColIdx, A->ntiles), "export tileColIdx");
     CK(dn(tileNnzOff, A->tileNnzOff, A->ntiles + 1), "export tileNnzOff");
-    CK(dn(rowEnd, A->rowEnd, A->ntiles * A->T), "export rowEnd");
-    CK(dn(colIdx, A->colIdx, A->nnz), "export colIdx");
-    CK(dn(v64, A->v64, A->nnz), "export v64");
-    CK(dn(v32, A->v32, A->nnz), "export v32");
-    CK(dn(v16, A->v16, A->nnz), "export v16");
+    CK(dn(rowMask, A->rowMask, A->ntiles), "export rowMask");
+    CK(dn(tileWidth, A->tileWidth, A->ntiles), "export tileWidth");
+    CK(dn(colIdx, A->colIdx, A->nslots), "export colIdx");
+    CK(dn(v64, A->v64, A->nslots), "export v64");
+    CK(dn(v32, A->v32, A->nslots), "export v32");
+    CK(dn(v16, A->v16, A->nslots), "export v16");
     CK(dn(colExp, A->colExp, A->n), "export colExp");
     return EVOCG_OK;
 }
@@ -475,7 +485,10 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
 {
     g_err.clear();
     if (!A || (A->n > 0 && (!x || !y))) return fail(EVOCG_EINVAL, "NULL argument");
-    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT)) return fail(EVOCG_EINVAL, "unknown flags");
+    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED);
+    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED))
+        return fail(EVOCG_EINVAL, "unknown flags");
+    if (kflags & (kflags - 1)) return fail(EVOCG_EINVAL, "at most one kernel flag");
     if (A->n == 0) return EVOCG_OK;
     cudaStream_t s = (cudaStream_t)stream;
     const bool reuse = (flags & EVOCG_SPMV_REUSE_XCOPIES) != 0;
@@ -507,6 +520,7 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     S.map_kind = A->map_kind;
     S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
     S.direct = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
+    S.kind = (flags & EVOCG_SPMV_STAGED) ? SPMV_KIND_STAGED : 0;
     CK(launch_spmv(S, s), "launch spmv");
     if (!ydev) {
         int lost = 0;

@@ -46,14 +46,15 @@ enum { TK_SPMV = 0, TK_UPDATE = 1, TK_INIT = 2, TK_TRUE = 3 };
 
 // Everything the SpMV reads from the tile structure.
 struct TilesView {
-    int64_t n, nrb, ntiles;
+    int64_t n, nrb, ntiles, nslots;
     int T;
     const int64_t *tileRowPtr;
     const int32_t *tileColIdx;
-    const int64_t *tileNnzOff;
+    const int64_t *tileNnzOff;  // first slot of every tile (ntiles + 1)
     const int32_t *tileRowIdx;  // row block of each tile (device-side helper, not exported)
-    const uint16_t *rowEnd;
-    const uint8_t *colIdx;
+    const uint64_t *rowMask;    // nonempty local rows of every tile
+    const uint8_t *tileWidth;   // slots per nonempty row of every tile
+    const uint8_t *colIdx;      // local column of every slot (T: a pad)
     const double *v64;
     const float *v32;
     const uint16_t *v16;
@@ -68,7 +69,12 @@ struct TilesView {
     const uint16_t *tileSlot;
     int staged_grid;
     int *err;
+    int spmv_kind;     // kernel launch_spmv runs by default (SPMV_KIND_*)
 };
+
+// SpMV kernels: the direct kernel (warp per row block, global loads) and the staged kernel
+// (operands in shared memory by bulk asynchronous copies). AUTO: staged when it can run.
+enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_STAGED = 2 };
 
 constexpr uint16_t kDirectSlot = 0xFFFF;
 
@@ -81,7 +87,7 @@ struct StagedLimits {
 };
 bool staged_limits(int T, StagedLimits *out);
 
-// Worst-case stage bytes of a tile with m entries: the 16-byte cover of its value slice in
+// Worst-case stage bytes of a tile with m slots: the 16-byte cover of its value slice in
 // any precision (at most 8m + 8 bytes before rounding) followed by its x segment in FP64.
 #ifdef __CUDACC__
 __host__ __device__
@@ -117,13 +123,14 @@ struct SolveWS {
 struct evocg_tiles {
     int device = 0;
     int sms = 0;
-    int64_t n = 0, nrb = 0, ntiles = 0, nnz = 0;
+    int64_t n = 0, nrb = 0, ntiles = 0, nnz = 0, nslots = 0;
     int T = 0;
     int64_t *tileRowPtr = nullptr;
     int32_t *tileColIdx = nullptr;
     int64_t *tileNnzOff = nullptr;
     int32_t *tileRowIdx = nullptr;
-    uint16_t *rowEnd = nullptr;
+    uint64_t *rowMask = nullptr;
+    uint8_t *tileWidth = nullptr;
     uint8_t *colIdx = nullptr;
     double *v64 = nullptr;
     float *v32 = nullptr;
@@ -136,6 +143,7 @@ struct evocg_tiles {
     int64_t nbatches = 0;
     int staged_grid = 0;
     int *errw = nullptr;           // device error word (a lost stage wait)
+    int spmv_kind = 0;             // default SpMV kernel (SPMV_KIND_*)
     uint8_t *tilePrec = nullptr;   // per-tile map
     uint8_t *cbPrec = nullptr;     // per-column-block map
     int map_kind = EVOCG_MAP_PER_TILE;
@@ -151,9 +159,10 @@ struct evocg_tiles {
 
     evocg::TilesView view() const
     {
-        return evocg::TilesView{n, nrb, ntiles, T, tileRowPtr, tileColIdx, tileNnzOff, tileRowIdx,
-                                rowEnd, colIdx, v64, v32, v16, colExp, warpRb, warpBatch, batchTile,
-                                tileSlot, staged_grid, errw};
+        return evocg::TilesView{n, nrb, ntiles, nslots, T, tileRowPtr, tileColIdx, tileNnzOff,
+                                tileRowIdx, rowMask, tileWidth, colIdx, v64, v32, v16, colExp,
+                                warpRb, warpBatch, batchTile, tileSlot, staged_grid, errw,
+                                spmv_kind};
     }
 };
 
@@ -166,13 +175,14 @@ int cuda_fail(cudaError_t e, const char *what);
 
 // ---- tile builder (tile_build.cpp) ----
 struct HostTiles {
-    int64_t n = 0, nrb = 0, ntiles = 0, nnz = 0;
+    int64_t n = 0, nrb = 0, ntiles = 0, nnz = 0, nslots = 0;
     int T = 0;
     int64_t *tileRowPtr = nullptr;
     int32_t *tileColIdx = nullptr;
     int64_t *tileNnzOff = nullptr;
     int32_t *tileRowIdx = nullptr;
-    uint16_t *rowEnd = nullptr;
+    uint64_t *rowMask = nullptr;
+    uint8_t *tileWidth = nullptr;
     uint8_t *colIdx = nullptr;
     double *v64 = nullptr;
     float *v32 = nullptr;
@@ -201,17 +211,19 @@ struct SpmvLaunch {
     double *pq;
     double *partials;
     DevState *st;
-    int census;            // accumulate per-precision entry counts into st->census
+    int census;            // accumulate per-precision stored-entry counts (pads excluded) into st->census
     int gate;              // return at once when st->done is set (a stopped solve)
     int grid;              // grid of the direct kernel
-    int direct;            // 1: the direct kernel even when the staged one could run
+    int direct;            // 1: the direct kernel whatever the default
+    int kind;              // SPMV_KIND_*: a kernel other than the matrix's default (0: default)
 };
-// The staged kernel runs when the view has warp ranges and every x operand is 16-byte
-// aligned; otherwise the direct kernel.
+// Kernel choice: L.direct, else L.kind, else the matrix's default; the staged kernel only
+// when the view has its plan and every x operand is 16-byte aligned (else the direct one).
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
 cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s);
 int spmv_dot_partials(const SpmvLaunch &L);   // warps that write a p.q partial
 cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s);
+
 int staged_grid_for(int T, int sms);   // 0 if it cannot run
 int staged_warps_per_block(int T);      // consumer warps (the ones with rows) per block
 

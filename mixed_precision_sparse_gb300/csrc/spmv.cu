@@ -6,7 +6,9 @@
 // ascending column block, so every row is summed in column order. Lane l owns local row
 // l (T = 32), rows l and l+32 (T = 64), or, for T = 16, the two half-warps take
 // alternate tiles of the row block and are merged at the end. Each lane keeps its rows'
-// sums in registers for the whole row block: no cross-lane reduction at all.
+// sums in registers for the whole row block: no cross-lane reduction at all. In a tile,
+// a lane whose row is in the row mask reads its slots k*h + j (j = the mask's popcount
+// below its row) for k < w and skips pads (local column T).
 //
 // Arithmetic. An FP64 tile costs exactly one FP64 fused multiply-add per entry, the
 // floor for FP64 data. FP32 and BF16 tiles never touch the FP64 unit: their products
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(kSpmvThreads, kSpmvMinBlocks) spmv_kernel(Spmv
     const int64_t nwarps = (int64_t)gridDim.x * wpb;
     const int64_t wid = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     double dotp = 0.0;
-    unsigned long long cnt0 = 0, cnt1 = 0, cnt2 = 0;
+    unsigned cnt0 = 0, cnt1 = 0, cnt2 = 0;   // stored entries per precision (census)
 
     for (int64_t rb = wid; rb < A.nrb; rb += nwarps) {
         const int64_t t0 = A.tileRowPtr[rb], t1 = A.tileRowPtr[rb + 1];
@@ -59,43 +61,50 @@ __global__ void __launch_bounds__(kSpmvThreads, kSpmvMinBlocks) spmv_kernel(Spmv
         for (int64_t t = t0 + grp; t < t1; t += Gm::NG) {
             const int64_t cb = A.tileColIdx[t];
             const int64_t off = A.tileNnzOff[t];
+            const uint64_t msk = __ldg(reinterpret_cast<const unsigned long long *>(A.rowMask) + t);
+            const int w = (int)__ldg(A.tileWidth + t);
             const int prec = FORCE64 ? 0 : (int)__ldg(L.prec + (L.map_kind ? cb : t));
+            const int64_t h = __popcll(msk);
             const uint8_t *ci = A.colIdx + off;
             const int64_t xb = cb * T;
-            const uint16_t *re = A.rowEnd + t * T;
 #pragma unroll
             for (int rr = 0; rr < Gm::RPL; ++rr) {
                 const int r = gl + rr * Gm::G;
-                const int end = __ldg(re + r);
-                const int start = r ? (int)__ldg(re + r - 1) : 0;
+                if (!((msk >> r) & 1ull)) continue;          // no entry of my row here
+                const int64_t j = __popcll(msk & ((1ull << r) - 1ull));   // my slot column
                 if (prec == EVOCG_FP64) {
                     const double *vv = A.v64 + off;
                     const double *xs = L.x64 + xb;
                     double a = acc64[rr];
-#pragma unroll 4
-                    for (int k = start; k < end; ++k)
-                        a = fma(__ldg(vv + k), __ldg(xs + __ldg(ci + k)), a);
+                    for (int k = 0; k < w; ++k) {
+                        const int64_t s = (int64_t)k * h + j;
+                        const int c = __ldg(ci + s);
+                        if (c < T) { a = fma(__ldg(vv + s), __ldg(xs + c), a); ++cnt0; }
+                    }
                     acc64[rr] = a;
                 } else if (prec == EVOCG_FP32) {
                     const float *vv = A.v32 + off;
                     const float *xs = L.x32 + xb;
-#pragma unroll 4
-                    for (int k = start; k < end; ++k)
-                        accl[rr].add_prod(__ldg(vv + k), __ldg(xs + __ldg(ci + k)));
+                    for (int k = 0; k < w; ++k) {
+                        const int64_t s = (int64_t)k * h + j;
+                        const int c = __ldg(ci + s);
+                        if (c < T) { accl[rr].add_prod(__ldg(vv + s), __ldg(xs + c)); ++cnt1; }
+                    }
                 } else {
                     const uint16_t *vv = A.v16 + off;
                     const float *xs = L.x16f + xb;
-#pragma unroll 4
-                    for (int k = start; k < end; ++k)  // BF16 x BF16 is exact in FP32
-                        accl[rr].add(__fmul_rn(f32_from_bf16(__ldg(vv + k)), __ldg(xs + __ldg(ci + k))));
+                    for (int k = 0; k < w; ++k) {  // BF16 x BF16 is exact in FP32
+                        const int64_t s = (int64_t)k * h + j;
+                        const int c = __ldg(ci + s);
+                        if (c < T) {
+                            accl[rr].add(__fmul_rn(f32_from_bf16(__ldg(vv + s)), __ldg(xs + c)));
+                            ++cnt2;
+                        }
+                    }
                 }
             }
             any64 |= (prec == EVOCG_FP64);
             anylow |= (prec != EVOCG_FP64);
-            if (L.census && gl == 0) {
-                const unsigned long long c = __ldg(re + T - 1);
-                if (prec == 0) cnt0 += c; else if (prec == 1) cnt1 += c; else cnt2 += c;
-            }
         }
         if (Gm::NG == 2) {  // T = 16: fold the odd-tile half-warp into the even one
 #pragma unroll
@@ -132,9 +141,9 @@ __global__ void __launch_bounds__(kSpmvThreads, kSpmvMinBlocks) spmv_kernel(Spmv
             cnt2 += __shfl_xor_sync(0xffffffffu, cnt2, o);
         }
         if (lane == 0) {
-            if (cnt0) atomicAdd(&L.st->census[0], cnt0);
-            if (cnt1) atomicAdd(&L.st->census[1], cnt1);
-            if (cnt2) atomicAdd(&L.st->census[2], cnt2);
+            if (cnt0) atomicAdd(&L.st->census[0], (unsigned long long)cnt0);
+            if (cnt1) atomicAdd(&L.st->census[1], (unsigned long long)cnt1);
+            if (cnt2) atomicAdd(&L.st->census[2], (unsigned long long)cnt2);
         }
     }
     if (DOT) {   // this warp's p.q partial (lanes summed in a fixed tree)
@@ -183,27 +192,36 @@ static cudaError_t launch_T(const SpmvLaunch &L, cudaStream_t s)
     return cudaGetLastError();
 }
 
-static bool use_staged(const SpmvLaunch &L)
+static int chosen_kind(const SpmvLaunch &L)
 {
-    const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    return !L.direct && L.A.warpRb && L.A.staged_grid > 0 && al(L.x64) &&
-           (L.force64 || (al(L.x32) && al(L.x16f)));
+    if (L.direct) return SPMV_KIND_DIRECT;
+    const int k = L.kind ? L.kind : L.A.spmv_kind;
+    if (k == SPMV_KIND_STAGED || k == SPMV_KIND_AUTO) {
+        const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+        if (L.A.warpRb && L.A.staged_grid > 0 && al(L.x64) && (L.force64 || (al(L.x32) && al(L.x16f))))
+            return SPMV_KIND_STAGED;
+    }
+    return SPMV_KIND_DIRECT;
 }
 
 int spmv_dot_partials(const SpmvLaunch &L)
 {
-    if (use_staged(L)) return L.A.staged_grid * staged_warps_per_block(L.A.T);
-    return L.grid * (kSpmvThreads / 32);
+    switch (chosen_kind(L)) {
+    case SPMV_KIND_STAGED: return L.A.staged_grid * staged_warps_per_block(L.A.T);
+    default: return L.grid * (kSpmvThreads / 32);
+    }
 }
 
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
 {
-    if (use_staged(L)) {
-        SpmvLaunch S = L;
+    SpmvLaunch S = L;
+    switch (chosen_kind(L)) {
+    case SPMV_KIND_STAGED:
         S.grid = L.A.staged_grid;
         return launch_spmv_staged(S, s);
+    default:
+        return launch_spmv_direct(L, s);
     }
-    return launch_spmv_direct(L, s);
 }
 
 cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s)

@@ -6,14 +6,17 @@
 // order, in batches fixed at build time (a static plan: staged_plan.cpp). Lane l owns local
 // row l (rows l and l+32 for T = 64; lanes 16..31 idle in the arithmetic for T = 16) and
 // keeps its row sums in registers for the whole row block: no cross-lane reduction, so an
-// FP64 tile costs one FP64 fused multiply-add per entry and nothing more.
+// FP64 tile costs one FP64 fused multiply-add per entry and nothing more. Inside a tile the
+// slots are slot-major over the nonempty rows, so at every k the lanes read consecutive
+// slots; a lane finds its slot column with one popcount of the tile's row mask and runs
+// exactly the tile's width w, skipping pads (local column T).
 //
 // Staging. A warp holds S stages of shared memory; every tile of a batch has a fixed slot
 // in its stage, sized for FP64. For a batch, lane j issues two bulk asynchronous copies for
 // tile j: the tile's slice of the value stream its precision selects (the 16-byte aligned
 // cover of the slice: the same 32-byte sectors a plain load would fetch) and the x segment
-// of the tile's column block in that precision; one lane copies the batch's row-end table
-// and local-column bytes, which are contiguous. Copies land on the stage's mbarrier with
+// of the tile's column block in that precision; one lane copies the batch's local-column
+// bytes, which are contiguous. Copies land on the stage's mbarrier with
 // their byte count; the warp computes batch b while batches b+1 .. b+S-1 are in flight. So
 // a warp keeps kilobytes of reads in flight for a few instructions per tile, instead of a
 // dependent chain of global loads per tile. Matrix streams are read with an evict-first L2
@@ -49,24 +52,41 @@ template <int T>
 struct StCfg;
 template <>
 struct StCfg<16> : StParams<4, 3, 8, 512, 2560, 4> {};
-#ifndef EVOCG_ST32
-#define EVOCG_ST32 2, 2, 16, 768, 4096, 8
+// T = 32 (tuning constants, one macro each so a build can override them)
+#ifndef EVOCG_ST32_NC
+#define EVOCG_ST32_NC 2
+#endif
+#ifndef EVOCG_ST32_S
+#define EVOCG_ST32_S 2
+#endif
+#ifndef EVOCG_ST32_NB
+#define EVOCG_ST32_NB 16
+#endif
+#ifndef EVOCG_ST32_CB
+#define EVOCG_ST32_CB 768
+#endif
+#ifndef EVOCG_ST32_DB
+#define EVOCG_ST32_DB 4096
+#endif
+#ifndef EVOCG_ST32_MINB
+#define EVOCG_ST32_MINB 8
 #endif
 template <>
-struct StCfg<32> : StParams<EVOCG_ST32> {};
+struct StCfg<32> : StParams<EVOCG_ST32_NC, EVOCG_ST32_S, EVOCG_ST32_NB, EVOCG_ST32_CB, EVOCG_ST32_DB,
+                            EVOCG_ST32_MINB> {};
 template <>
 struct StCfg<64> : StParams<4, 2, 8, 1024, 8192, 2> {};
 
-// Stage layout (bytes from the stage base): header, per-tile info, row ends, local
-// columns, values + x segments. Block layout: full and empty mbarriers of every consumer
-// stage, then each consumer's S stages.
+// Stage layout (bytes from the stage base): header, per-tile info, local columns,
+// values + x segments. Block layout: full and empty mbarriers of every consumer stage,
+// then each consumer's S stages.
 template <int T>
 struct StLayout {
     using C = StCfg<T>;
     static constexpr int HDR = 0;                        // int64 tb, int32 nb, int32 direct
-    static constexpr int INFO = 16;                      // NB x uint4
-    static constexpr int RE = INFO + 16 * C::NB;         // NB x T x uint16
-    static constexpr int COL = RE + 2 * T * C::NB;       // CB bytes
+    static constexpr int INFO = 16;                      // NB x INFOB bytes
+    static constexpr int INFOB = T > 32 ? 32 : 16;       // uint4 (+ the high row mask)
+    static constexpr int COL = INFO + INFOB * C::NB;     // CB bytes
     static constexpr int DATA = COL + C::CB;             // DB bytes
     static constexpr int STAGE = (DATA + C::DB + 127) / 128 * 128;
     static constexpr int BARS = (2 * C::NC * C::S * 8 + 127) / 128 * 128;
@@ -191,7 +211,7 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
 
     const int n = (int)A.n;
     double dotp = 0.0;
-    unsigned long long cnt0 = 0, cnt1 = 0, cnt2 = 0;
+    unsigned cnt0 = 0, cnt1 = 0, cnt2 = 0;   // stored entries per precision (census)
 
     if (wib == C::NC) {
         // =============================== producer ===============================
@@ -206,39 +226,54 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
         const uint32_t wreg = region(c);
 
         // Descriptors: raw for round r + 1 (loaded two rounds ahead) and resolved, with the
-        // precision looked up, for round r (its precision load issued one round ahead), so
-        // the producer never waits on memory inside a round.
-        int64_t r_o0 = 0, r_o1 = 0, r_tb = 0;
-        int r_cb = 0, r_rb = 0, r_slot = 0, r_pt = 0, r_nb = 0;
+        // precision looked up, for round r (its precision load issued one round ahead); the
+        // first tiles of rounds r + 2 and r + 3 (the batch pointers the raw loads index by)
+        // are loaded one round before they are used. No load inside a round waits on
+        // another load of that round.
+        int64_t r_o0 = 0, r_tb = 0;
+        int r_cb = 0, r_rb = 0, r_slot = 0, r_pt = 0, r_nb = 0, r_w = 0;
+        uint64_t r_mask = 0;
         int64_t d_o0 = 0, d_tb = 0;
-        int d_m = 0, d_cb = 0, d_rb = 0, d_slot = 0, d_nb = 0, d_prec = 0;
+        int d_m = 0, d_cb = 0, d_rb = 0, d_slot = 0, d_nb = 0, d_prec = 0, d_w = 0;
+        uint64_t d_mask = 0;
+        auto batch_ptr = [&](int r) -> int64_t {   // first tile of round r (bEnd: past the end)
+            const int bb = bBeg + r;
+            return bb <= bEnd ? __ldg(A.batchTile + bb) : 0;
+        };
         auto resolve = [&]() {   // d <- raw
-            d_nb = r_nb; d_tb = r_tb; d_o0 = r_o0; d_m = (int)(r_o1 - r_o0);
-            d_cb = r_cb; d_rb = r_rb; d_slot = r_slot;
+            d_nb = r_nb; d_tb = r_tb; d_o0 = r_o0;
+            d_m = r_w * __popcll(r_mask);   // slots of the tile
+            d_cb = r_cb; d_rb = r_rb; d_slot = r_slot; d_w = r_w; d_mask = r_mask;
             if (FORCE64) d_prec = 0;
             else if (L.map_kind == EVOCG_MAP_PER_TILE) d_prec = r_pt;
             else d_prec = (i < r_nb) ? (int)__ldg(L.prec + r_cb) : 0;
         };
-        auto load_raw = [&](int r) {
-            const int bb = bBeg + r;
+        auto load_raw = [&](int r, int64_t tb0, int64_t tb1) {   // tb0, tb1: rounds r, r + 1
             r_nb = 0;
-            if (bb < bEnd) {
-                r_tb = __ldg(A.batchTile + bb);
-                r_nb = (int)(__ldg(A.batchTile + bb + 1) - r_tb);
+            if (bBeg + r < bEnd) {
+                r_tb = tb0;
+                r_nb = (int)(tb1 - tb0);
                 if (i < r_nb) {
                     const int64_t t = r_tb + i;
                     r_o0 = __ldg(A.tileNnzOff + t);
-                    r_o1 = __ldg(A.tileNnzOff + t + 1);
                     r_cb = __ldg(A.tileColIdx + t);
                     r_rb = __ldg(A.tileRowIdx + t);
                     r_slot = __ldg(A.tileSlot + t);
+                    r_mask = __ldg(reinterpret_cast<const unsigned long long *>(A.rowMask) + t);
+                    r_w = (int)__ldg(A.tileWidth + t);
                     r_pt = (!FORCE64 && L.map_kind == EVOCG_MAP_PER_TILE) ? (int)__ldg(L.prec + t) : 0;
                 }
             }
         };
-        load_raw(0);
-        resolve();
-        load_raw(1);
+        int64_t tbA, tbB;   // first tiles of rounds r + 2 and r + 3 at the end of round r
+        {
+            const int64_t p0 = batch_ptr(0), p1 = batch_ptr(1), p2 = batch_ptr(2);
+            tbA = p2;
+            tbB = batch_ptr(3);
+            load_raw(0, p0, p1);
+            resolve();
+            load_raw(1, p1, p2);
+        }
         bool lost = false;
         for (int r = 0; r < rounds && !lost; ++r) {
             const int st = r % C::S;
@@ -246,7 +281,8 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
             // loads are issued at the end of the round
             const int nb = d_nb;
             const int64_t tb = d_tb, o0 = d_o0;
-            const int m = d_m, cb = d_cb, rb = d_rb, slot = d_slot, prec = d_prec;
+            const int m = d_m, cb = d_cb, rb = d_rb, slot = d_slot, prec = d_prec, tw = d_w;
+            const uint64_t tmask = d_mask;
             const bool valid = i < nb;
             // wait until each consumer has released the stage this round refills
             bool timedout = false;
@@ -258,12 +294,6 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
                 break;
             }
             fence_proxy_async();
-            if (L.census) {
-                const unsigned cm = valid ? (unsigned)m : 0u;
-                cnt0 += __reduce_add_sync(kFull, prec == 0 ? cm : 0u);
-                cnt1 += __reduce_add_sync(kFull, prec == 1 ? cm : 0u);
-                cnt2 += __reduce_add_sync(kFull, prec == 2 ? cm : 0u);
-            }
             const uint32_t stg = wreg + (uint32_t)(st * Y::STAGE);     // consumer stage in sm
             const uint32_t srel = stg - wreg;                             // ... in its region
             const int slot0 = __shfl_sync(kFull, slot, 0, G);   // every lane takes part
@@ -286,15 +316,18 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
             const uint32_t xS = dOff + (uint32_t)(staged_slot_bytes(m, T) - 8 * T);
             const uint32_t colS = srel + Y::COL + (uint32_t)(o0 - colFirst);
             if (valid) {
+                const uint32_t pw = ((uint32_t)prec << 16) | ((uint32_t)tw << 18);
                 if (direct) {
                     *reinterpret_cast<int4 *>(sm + stg + Y::HDR) =
                         make_int4((int)(tb & 0xffffffff), (int)(tb >> 32), 1, 1);
                     *reinterpret_cast<uint4 *>(sm + stg + Y::INFO) =
-                        make_uint4(0u, (uint32_t)rb, (uint32_t)prec << 16, (uint32_t)m);
+                        make_uint4(0u, (uint32_t)rb, pw, (uint32_t)tmask);
                 } else {
-                    *reinterpret_cast<uint4 *>(sm + stg + Y::INFO + 16 * i) =
-                        make_uint4(valS | (xS << 16), (uint32_t)rb, colS | ((uint32_t)prec << 16),
-                                   (uint32_t)m);
+                    *reinterpret_cast<uint4 *>(sm + stg + Y::INFO + Y::INFOB * i) =
+                        make_uint4(valS | (xS << 16), (uint32_t)rb, colS | pw, (uint32_t)tmask);
+                    if (T > 32)
+                        *reinterpret_cast<uint32_t *>(sm + stg + Y::INFO + Y::INFOB * i + 16) =
+                            (uint32_t)(tmask >> 32);
                     if (!full_x) {  // the last column block of a matrix with T not dividing n
                         const int xb0 = cb * T;
                         if (prec == 0) {
@@ -315,7 +348,7 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
             __syncwarp();
             if (i == 0 && nb > 0) {
                 if (direct) mbar_arrive(full_bar(c, st));
-                else mbar_arrive_expect_tx(full_bar(c, st), (uint32_t)(txl + colBytes + nb * 2 * T));
+                else mbar_arrive_expect_tx(full_bar(c, st), (uint32_t)(txl + colBytes));
             }
             __syncwarp();
             if (valid && !direct) {
@@ -331,13 +364,13 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
                                                : reinterpret_cast<const unsigned char *>(L.x16f));
                     bulk_g2s(sbase + wreg + xS, xsrc + (size_t)cb * (size_t)xb, (uint32_t)xb, full_bar(c, st));
                 }
-                if (i == 0) {
+                if (i == 0)
                     bulk_g2s_hint(sbase + stg + Y::COL, A.colIdx + colFirst, (uint32_t)colBytes, full_bar(c, st), pol);
-                    bulk_g2s_hint(sbase + stg + Y::RE, A.rowEnd + tb * T, (uint32_t)(nb * 2 * T), full_bar(c, st), pol);
-                }
             }
             resolve();
-            load_raw(r + 2);
+            load_raw(r + 2, tbA, tbB);
+            tbA = tbB;
+            tbB = batch_ptr(r + 4);
         }
     } else {
         // =============================== consumer ===============================
@@ -391,65 +424,58 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
             cur_rb = rb;
             start_rb(rb);
         };
-        auto get_starts = [&](const int (&e)[RPL], int (&s)[RPL]) {
-            const int u1 = __shfl_up_sync(kFull, e[0], 1);
-            s[0] = lane ? u1 : 0;
-            if (RPL == 2) {
-                const int u2 = __shfl_up_sync(kFull, e[RPL - 1], 1);
-                const int l1 = __shfl_sync(kFull, e[0], 31);
-                s[RPL - 1] = lane ? u2 : l1;
-            }
-            if (!rowlane) s[0] = e[0];
-        };
+        const uint32_t ltm = (1u << lane) - 1u;   // lanes below mine
         // one tile's products for my rows, operands in my shared-memory region (32-bit
-        // offsets); the entry loop runs the warp's largest row count with predication
-        auto tile_staged = [&](uint4 inf, const int (&s)[RPL], const int (&e)[RPL]) {
+        // offsets): my slot column j = popcount of the row mask below my row; w slots at
+        // stride h = popcount of the mask; pads (column T) are skipped
+        auto tile_staged = [&](const uint4 inf, uint32_t mhi) {
             const int prec = (int)((inf.z >> 16) & 3u);
+            const int w = (int)((inf.z >> 18) & 127u);
             const uint32_t colo = wofs + (inf.z & 0xffffu), valo = wofs + (inf.x & 0xffffu);
             const uint32_t xo = wofs + (inf.x >> 16);
+            const uint32_t mlo = inf.w;
+            const uint32_t h = (uint32_t)(__popc(mlo) + (RPL == 2 ? __popc(mhi) : 0));
 #pragma unroll
             for (int q = 0; q < RPL; ++q) {
-                const int cnt = e[q] - s[q];
-                const int kmax = (int)__reduce_max_sync(kFull, (unsigned)cnt);
-                const uint32_t co = colo + (uint32_t)s[q];
+                const uint32_t mq = q ? mhi : mlo;
+                if (!((mq >> lane) & 1u)) continue;   // my row has no entry in this tile
+                const uint32_t j = (uint32_t)((q ? __popc(mlo) : 0) + __popc(mq & ltm));
                 if (prec == EVOCG_FP64) {
-                    const uint32_t vo = valo + 8u * (uint32_t)s[q];
                     double a = acc64[q];
-                    if (kmax == 1) {   // at most one entry per row: the common stencil tile
-                        if (cnt) {
-                            const uint32_t cc = sm[co];
-                            a = fma(*reinterpret_cast<const double *>(sm + vo),
-                                    *reinterpret_cast<const double *>(sm + xo + 8u * cc), a);
-                        }
-                    } else {
 #pragma unroll 1
-                        for (int k = 0; k < kmax; ++k)
-                            if (k < cnt) {
-                                const uint32_t cc = sm[co + k];
-                                a = fma(*reinterpret_cast<const double *>(sm + vo + 8u * k),
-                                        *reinterpret_cast<const double *>(sm + xo + 8u * cc), a);
-                            }
+                    for (int k = 0; k < w; ++k) {
+                        const uint32_t s = (uint32_t)k * h + j;
+                        const uint32_t cc = sm[colo + s];
+                        if (cc < (uint32_t)T) {
+                            a = fma(*reinterpret_cast<const double *>(sm + valo + 8u * s),
+                                    *reinterpret_cast<const double *>(sm + xo + 8u * cc), a);
+                            if (L.census) ++cnt0;
+                        }
                     }
                     acc64[q] = a;
                 } else if (prec == EVOCG_FP32) {
-                    const uint32_t vo = valo + 4u * (uint32_t)s[q];
 #pragma unroll 1
-                    for (int k = 0; k < kmax; ++k)
-                        if (k < cnt) {
-                            const uint32_t cc = sm[co + k];
-                            accl[q].add_prod(*reinterpret_cast<const float *>(sm + vo + 4u * k),
+                    for (int k = 0; k < w; ++k) {
+                        const uint32_t s = (uint32_t)k * h + j;
+                        const uint32_t cc = sm[colo + s];
+                        if (cc < (uint32_t)T) {
+                            accl[q].add_prod(*reinterpret_cast<const float *>(sm + valo + 4u * s),
                                              *reinterpret_cast<const float *>(sm + xo + 4u * cc));
+                            if (L.census) ++cnt1;
                         }
+                    }
                 } else {
-                    const uint32_t vo = valo + 2u * (uint32_t)s[q];
 #pragma unroll 1
-                    for (int k = 0; k < kmax; ++k)  // BF16 x BF16 is exact in FP32
-                        if (k < cnt) {
-                            const uint32_t cc = sm[co + k];
-                            const uint16_t h = *reinterpret_cast<const uint16_t *>(sm + vo + 2u * k);
-                            accl[q].add(__fmul_rn(f32_from_bf16(h),
+                    for (int k = 0; k < w; ++k) {  // BF16 x BF16 is exact in FP32
+                        const uint32_t s = (uint32_t)k * h + j;
+                        const uint32_t cc = sm[colo + s];
+                        if (cc < (uint32_t)T) {
+                            const uint16_t hb = *reinterpret_cast<const uint16_t *>(sm + valo + 2u * s);
+                            accl[q].add(__fmul_rn(f32_from_bf16(hb),
                                                   *reinterpret_cast<const float *>(sm + xo + 4u * cc)));
+                            if (L.census) ++cnt2;
                         }
+                    }
                 }
             }
             if (prec == EVOCG_FP64) any64 = true; else anylow = true;
@@ -458,19 +484,29 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
         auto tile_direct = [&](int64_t t, int prec) {
             const int64_t off = __ldg(A.tileNnzOff + t);
             const int xb0 = __ldg(A.tileColIdx + t) * T;
-            const uint16_t *re = A.rowEnd + t * T;
-            const uint8_t *ci = A.colIdx + off;
-            int e[RPL], s[RPL];
-            e[0] = rowlane ? (int)__ldg(re + lane) : 0;
-            if (RPL == 2) e[RPL - 1] = (int)__ldg(re + lane + 32);
-            get_starts(e, s);
+            const uint64_t msk = __ldg(reinterpret_cast<const unsigned long long *>(A.rowMask) + t);
+            const int w = (int)__ldg(A.tileWidth + t);
+            const int64_t h = __popcll(msk);
 #pragma unroll
             for (int q = 0; q < RPL; ++q) {
-                for (int k = s[q]; k < e[q]; ++k) {
-                    const int jx = xb0 + __ldg(ci + k);
-                    if (prec == EVOCG_FP64) acc64[q] = fma(__ldg(A.v64 + off + k), __ldg(L.x64 + jx), acc64[q]);
-                    else if (prec == EVOCG_FP32) accl[q].add_prod(__ldg(A.v32 + off + k), __ldg(L.x32 + jx));
-                    else accl[q].add(__fmul_rn(f32_from_bf16(__ldg(A.v16 + off + k)), __ldg(L.x16f + jx)));
+                const int r = lane + 32 * q;
+                if (!rowlane || !((msk >> r) & 1ull)) continue;
+                const int64_t j = __popcll(msk & ((1ull << r) - 1ull));
+                for (int k = 0; k < w; ++k) {
+                    const int64_t s = off + (int64_t)k * h + j;
+                    const int cc = __ldg(A.colIdx + s);
+                    if (cc >= T) continue;
+                    const int jx = xb0 + cc;
+                    if (prec == EVOCG_FP64) {
+                        acc64[q] = fma(__ldg(A.v64 + s), __ldg(L.x64 + jx), acc64[q]);
+                        if (L.census) ++cnt0;
+                    } else if (prec == EVOCG_FP32) {
+                        accl[q].add_prod(__ldg(A.v32 + s), __ldg(L.x32 + jx));
+                        if (L.census) ++cnt1;
+                    } else {
+                        accl[q].add(__fmul_rn(f32_from_bf16(__ldg(A.v16 + s)), __ldg(L.x16f + jx)));
+                        if (L.census) ++cnt2;
+                    }
                 }
             }
             if (prec == EVOCG_FP64) any64 = true; else anylow = true;
@@ -496,30 +532,17 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
                     tile_direct(tb, (int)((inf.z >> 16) & 3u));
                 } else {
                     const int nb = h.z;
-                    const uint32_t re = stg + Y::RE + 2u * (uint32_t)lane;   // my row's entry
                     uint4 inf = *reinterpret_cast<const uint4 *>(sm + info);
-                    int e[RPL], s[RPL];
-                    e[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re) : 0;
-                    if (RPL == 2) e[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 64u);
+                    uint32_t mhi = (T > 32) ? *reinterpret_cast<const uint32_t *>(sm + info + 16u) : 0u;
                     for (int jt = 0; jt < nb; ++jt) {
-                        // the next tile's descriptor and row ends load while this one computes
-                        uint4 infn = inf;
-                        int en[RPL];
-#pragma unroll
-                        for (int q = 0; q < RPL; ++q) en[q] = 0;
-                        if (jt + 1 < nb) {
-                            const uint32_t jn = (uint32_t)(jt + 1);
-                            infn = *reinterpret_cast<const uint4 *>(sm + info + 16u * jn);
-                            en[0] = rowlane ? (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn) : 0;
-                            if (RPL == 2)
-                                en[RPL - 1] = (int)*reinterpret_cast<const uint16_t *>(sm + re + 2u * T * jn + 64u);
-                        }
-                        get_starts(e, s);
+                        // the next tile's descriptor loads while this one computes
+                        const uint32_t ia = info + (uint32_t)(Y::INFOB * (jt + 1 < nb ? jt + 1 : jt));
+                        const uint4 infn = *reinterpret_cast<const uint4 *>(sm + ia);
+                        const uint32_t mhin = (T > 32) ? *reinterpret_cast<const uint32_t *>(sm + ia + 16u) : 0u;
                         goto_rb((int)inf.y);
-                        tile_staged(inf, s, e);
+                        tile_staged(inf, mhi);
                         inf = infn;
-#pragma unroll
-                        for (int q = 0; q < RPL; ++q) e[q] = en[q];
+                        mhi = mhin;
                     }
                 }
                 __syncwarp();
@@ -532,10 +555,17 @@ __global__ void __launch_bounds__(StCfg<T>::THREADS, StCfg<T>::MINB)
         }
     }
 
-    if (L.census && wib == C::NC && lane == 0) {
-        if (cnt0) atomicAdd(&L.st->census[0], cnt0);
-        if (cnt1) atomicAdd(&L.st->census[1], cnt1);
-        if (cnt2) atomicAdd(&L.st->census[2], cnt2);
+    if (L.census && wib < C::NC) {   // stored entries per precision, pads not counted
+        for (int o = 16; o; o >>= 1) {
+            cnt0 += __shfl_xor_sync(kFull, cnt0, o);
+            cnt1 += __shfl_xor_sync(kFull, cnt1, o);
+            cnt2 += __shfl_xor_sync(kFull, cnt2, o);
+        }
+        if (lane == 0) {
+            if (cnt0) atomicAdd(&L.st->census[0], (unsigned long long)cnt0);
+            if (cnt1) atomicAdd(&L.st->census[1], (unsigned long long)cnt1);
+            if (cnt2) atomicAdd(&L.st->census[2], (unsigned long long)cnt2);
+        }
     }
     if (DOT && wib < C::NC) {   // this consumer warp's p.q partial (fixed shuffle tree)
         for (int o = 16; o; o >>= 1) dotp += __shfl_xor_sync(kFull, dotp, o);

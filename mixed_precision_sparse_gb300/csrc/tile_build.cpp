@@ -2,15 +2,19 @@
 // blocks.
 //
 // Layout (EvoCG, "Self-Evolving Precision Control for Faster Conjugate Gradient",
-// §3.3.1 Fig. 4(a) and §3.3.2): CSR over row blocks of nonempty T x T tiles; inside a
-// tile the entries row by row in ascending column, with the end offset of every local
-// row (rowEnd) and one local column byte per entry (colIdx); three value streams over the
-// same entries (FP64 a_ij; FP32 and BF16 of a_ij / 2^e_j with the per-column exponent
-// e_j = floor(log2 max_i |a_ij|) clamped to [-100, 100]).
+// §3.3.1 Fig. 4(a) and §3.3.2): CSR over row blocks of nonempty T x T tiles. Inside a
+// tile: a mask of its nonempty local rows (rowMask), its width w = the longest row
+// (tileWidth), and w x h slots (h = nonempty rows) in slot-major order: slot (k, j) at
+// tileNnzOff[t] + k*h + j holds the k-th entry of the j-th nonempty row, or a pad
+// (local column T, value +0) when that row is shorter. One local column byte per slot
+// (colIdx) and three value streams over the same slots (FP64 a_ij; FP32 and BF16 of
+// a_ij / 2^e_j with the per-column exponent e_j = floor(log2 max_i |a_ij|) clamped to
+// [-100, 100]).
 //
-// Row-major order inside the tile (the paper stores the tile column-major) lets the SpMV
-// give each row to one lane and accumulate it in registers: no cross-lane FP64
-// reduction, which GB300's FP64 rate would make the bottleneck.
+// The SpMV gives each row to one lane and accumulates it in registers (no cross-lane
+// FP64 reduction, which GB300's FP64 rate would make the bottleneck); with slots in this
+// order the lanes of a warp read consecutive slots at every k, and the position of a
+// lane's slot is a popcount of the mask: no per-row offset table.
 #include <algorithm>
 #include <atomic>
 #include <climits>
@@ -26,9 +30,11 @@ namespace evocg {
 
 void HostTiles::release()
 {
-    delete[] tileRowPtr; delete[] tileColIdx; delete[] tileNnzOff; delete[] tileRowIdx; delete[] rowEnd;
-    delete[] colIdx; delete[] v64; delete[] v32; delete[] v16; delete[] colExp; delete[] dinv;
-    tileRowPtr = nullptr; tileColIdx = nullptr; tileNnzOff = nullptr; tileRowIdx = nullptr; rowEnd = nullptr;
+    delete[] tileRowPtr; delete[] tileColIdx; delete[] tileNnzOff; delete[] tileRowIdx; delete[] rowMask;
+    delete[] tileWidth; delete[] colIdx; delete[] v64; delete[] v32; delete[] v16; delete[] colExp;
+    delete[] dinv;
+    tileRowPtr = nullptr; tileColIdx = nullptr; tileNnzOff = nullptr; tileRowIdx = nullptr; rowMask = nullptr;
+    tileWidth = nullptr;
     colIdx = nullptr; v64 = nullptr; v32 = nullptr; v16 = nullptr; colExp = nullptr;
     dinv = nullptr;
 }
@@ -124,69 +130,104 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
             }
         });
         H.diag_ok = diag_bad.load() ? 0 : 1;
-        // --- pass 1: tiles per row block (distinct column blocks of its entries)
-        std::vector<int64_t> ntile_rb((size_t)nrb + 1, 0);
+        // --- pass 1: tiles and slots per row block. The entries of one tile row are a
+        // contiguous run of the CSR row (columns ascend), so a row block is walked once
+        // per tile with one cursor per row.
+        std::vector<int64_t> ntile_rb((size_t)nrb + 1, 0), nslot_rb((size_t)nrb + 1, 0);
+        auto walk = [&](int64_t rb, auto &&on_tile) {
+            const int64_t r0 = rb * T, r1 = std::min<int64_t>(n, r0 + T);
+            const int nr = (int)(r1 - r0);
+            int64_t cur[64], k1[64];
+            for (int r = 0; r < nr; ++r) cur[r] = rp[r0 + r];
+            for (;;) {
+                int32_t cb = INT32_MAX;  // smallest column block left in the row block
+                for (int r = 0; r < nr; ++r)
+                    if (cur[r] < rp[r0 + r + 1]) cb = std::min(cb, ci[cur[r]] / T);
+                if (cb == INT32_MAX) break;
+                uint64_t mask = 0;
+                int w = 0;
+                for (int r = 0; r < nr; ++r) {
+                    int64_t k = cur[r];
+                    while (k < rp[r0 + r + 1] && ci[k] / T == cb) ++k;
+                    k1[r] = k;
+                    if (k > cur[r]) mask |= 1ull << r;
+                    w = std::max(w, (int)(k - cur[r]));
+                }
+                on_tile(cb, mask, w, nr, cur, k1);
+                for (int r = 0; r < nr; ++r) cur[r] = k1[r];
+            }
+        };
         parallel_for(nrb, [&](int64_t a, int64_t b) {
-            std::vector<int32_t> cbs;
             for (int64_t rb = a; rb < b; ++rb) {
-                int64_t r0 = rb * T, r1 = std::min<int64_t>(n, r0 + T);
-                cbs.clear();
-                for (int64_t k = rp[r0]; k < rp[r1]; ++k) cbs.push_back(ci[k] / T);
-                std::sort(cbs.begin(), cbs.end());
-                ntile_rb[(size_t)rb] = (int64_t)(std::unique(cbs.begin(), cbs.end()) - cbs.begin());
+                int64_t nt = 0, ns = 0;
+                walk(rb, [&](int32_t, uint64_t mask, int w, int, const int64_t *, const int64_t *) {
+                    ++nt;
+                    ns += (int64_t)w * __builtin_popcountll(mask);
+                });
+                ntile_rb[(size_t)rb] = nt;
+                nslot_rb[(size_t)rb] = ns;
             }
         });
         H.tileRowPtr = new int64_t[(size_t)nrb + 1];
+        std::vector<int64_t> slot0((size_t)nrb + 1, 0);
         H.tileRowPtr[0] = 0;
-        for (int64_t rb = 0; rb < nrb; ++rb) H.tileRowPtr[rb + 1] = H.tileRowPtr[rb] + ntile_rb[(size_t)rb];
+        for (int64_t rb = 0; rb < nrb; ++rb) {
+            H.tileRowPtr[rb + 1] = H.tileRowPtr[rb] + ntile_rb[(size_t)rb];
+            slot0[(size_t)rb + 1] = slot0[(size_t)rb] + nslot_rb[(size_t)rb];
+        }
         H.ntiles = H.tileRowPtr[nrb];
-        const int64_t nt = H.ntiles;
+        H.nslots = slot0[(size_t)nrb];
+        const int64_t nt = H.ntiles, ns = H.nslots;
         H.tileColIdx = new int32_t[(size_t)std::max<int64_t>(nt, 1)];
         H.tileNnzOff = new int64_t[(size_t)nt + 1];
         H.tileRowIdx = new int32_t[(size_t)std::max<int64_t>(nt, 1)];
-        H.rowEnd = new uint16_t[(size_t)std::max<int64_t>(nt * T, 1)];
-        H.colIdx = new uint8_t[(size_t)std::max<int64_t>(nnz, 1)];
-        H.v64 = new double[(size_t)std::max<int64_t>(nnz, 1)];
-        H.v32 = new float[(size_t)std::max<int64_t>(nnz, 1)];
-        H.v16 = new uint16_t[(size_t)std::max<int64_t>(nnz, 1)];
-        H.tileNnzOff[nt] = nnz;
-        // --- pass 2: fill. The entries of row block rb occupy [rp[r0], rp[r1]) in the
-        // streams too (tiles only reorder them inside the row block).
+        H.rowMask = new uint64_t[(size_t)std::max<int64_t>(nt, 1)];
+        H.tileWidth = new uint8_t[(size_t)std::max<int64_t>(nt, 1)];
+        H.colIdx = new uint8_t[(size_t)std::max<int64_t>(ns, 1)];
+        H.v64 = new double[(size_t)std::max<int64_t>(ns, 1)];
+        H.v32 = new float[(size_t)std::max<int64_t>(ns, 1)];
+        H.v16 = new uint16_t[(size_t)std::max<int64_t>(ns, 1)];
+        H.tileNnzOff[nt] = ns;
+        // --- pass 2: fill the slots of every tile
         parallel_for(nrb, [&](int64_t a, int64_t b) {
-            std::vector<int64_t> cur((size_t)T);
             for (int64_t rb = a; rb < b; ++rb) {
-                const int64_t r0 = rb * T, r1 = std::min<int64_t>(n, r0 + T);
-                const int nr = (int)(r1 - r0);
-                for (int r = 0; r < nr; ++r) cur[(size_t)r] = rp[r0 + r];
-                int64_t pos = rp[r0];
-                for (int64_t t = H.tileRowPtr[rb]; t < H.tileRowPtr[rb + 1]; ++t) {
-                    int32_t cb = INT32_MAX;  // smallest column block left in the row block
-                    for (int r = 0; r < nr; ++r)
-                        if (cur[(size_t)r] < rp[r0 + r + 1]) cb = std::min(cb, ci[cur[(size_t)r]] / T);
+                int64_t t = H.tileRowPtr[rb], pos = slot0[(size_t)rb];
+                walk(rb, [&](int32_t cb, uint64_t mask, int w, int nr, const int64_t *k0,
+                             const int64_t *k1) {
+                    const int h = __builtin_popcountll(mask);
                     H.tileColIdx[t] = cb;
                     H.tileNnzOff[t] = pos;
                     H.tileRowIdx[t] = (int32_t)rb;
-                    const int64_t base = pos;
-                    for (int r = 0; r < T; ++r) {
-                        if (r < nr) {
-                            int64_t k = cur[(size_t)r];
-                            const int64_t kend = rp[r0 + r + 1];
-                            for (; k < kend && ci[k] / T == cb; ++k, ++pos) {
-                                const int32_t j = ci[k];
-                                const double s = std::ldexp(v[k], -(int)H.colExp[j]);
+                    H.rowMask[t] = mask;
+                    H.tileWidth[t] = (uint8_t)w;
+                    int j = 0;
+                    for (int r = 0; r < nr; ++r) {
+                        if (!((mask >> r) & 1)) continue;
+                        for (int k = 0; k < w; ++k) {
+                            const int64_t s = pos + (int64_t)k * h + j;
+                            const int64_t e = k0[r] + k;
+                            if (e < k1[r]) {
+                                const int32_t c = ci[e];
+                                const double sc = std::ldexp(v[e], -(int)H.colExp[c]);
                                 uint64_t sb;
-                                std::memcpy(&sb, &s, 8);
-                                H.colIdx[pos] = (uint8_t)(j - cb * T);
-                                H.v64[pos] = v[k];
-                                uint32_t b32 = rne_bits_from_f64<23>(sb);
-                                std::memcpy(&H.v32[pos], &b32, 4);
-                                H.v16[pos] = (uint16_t)rne_bits_from_f64<7>(sb);
+                                std::memcpy(&sb, &sc, 8);
+                                H.colIdx[s] = (uint8_t)(c - cb * T);
+                                H.v64[s] = v[e];
+                                const uint32_t b32 = rne_bits_from_f64<23>(sb);
+                                std::memcpy(&H.v32[s], &b32, 4);
+                                H.v16[s] = (uint16_t)rne_bits_from_f64<7>(sb);
+                            } else {  // pad: column T, +0 in every stream
+                                H.colIdx[s] = (uint8_t)T;
+                                H.v64[s] = 0.0;
+                                H.v32[s] = 0.0f;
+                                H.v16[s] = 0;
                             }
-                            cur[(size_t)r] = k;
                         }
-                        H.rowEnd[t * T + r] = (uint16_t)(pos - base);
+                        ++j;
                     }
-                }
+                    pos += (int64_t)w * h;
+                    ++t;
+                });
             }
         });
     } catch (const std::bad_alloc &) {

@@ -36,7 +36,7 @@ class TilesDesc(C.Structure):
     _fields_ = [("n", C.c_int64), ("nrb", C.c_int64), ("ntiles", C.c_int64), ("nnz", C.c_int64),
                 ("tile_size", C.c_int32), ("map_kind", C.c_int32), ("bytes_index", C.c_int64),
                 ("bytes_v64", C.c_int64), ("bytes_v32", C.c_int64), ("bytes_v16", C.c_int64),
-                ("bytes_colexp", C.c_int64)]
+                ("bytes_colexp", C.c_int64), ("nslots", C.c_int64)]
 
 
 class Ctrl(C.Structure):
@@ -88,7 +88,7 @@ def lib():
                 "evocg_tile_build": [i64, P, P, P, i32, C.POINTER(C.c_void_p)],
                 "evocg_tiles_free": [P],
                 "evocg_tiles_info": [P, C.POINTER(TilesDesc)],
-                "evocg_tiles_export": [P] + [P] * 9,
+                "evocg_tiles_export": [P] + [P] * 10,
                 "evocg_set_tile_precision": [P, P, i64, i32, P],
                 "evocg_get_tile_precision": [P, P, i64, P],
                 "evocg_spmv": [P, P, P, P],
@@ -159,6 +159,7 @@ class Tiles:
         d = TilesDesc()
         _check(lib().evocg_tiles_info(self.h, C.byref(d)))
         self.n, self.nrb, self.ntiles, self.nnz = d.n, d.nrb, d.ntiles, d.nnz
+        self.nslots = d.nslots
         self.T = d.tile_size
         self.desc = d
 
@@ -179,15 +180,17 @@ class Tiles:
             pass
 
     def export(self) -> dict:
+        ns = self.nslots
         out = dict(tileRowPtr=np.empty(self.nrb + 1, np.int64),
                    tileColIdx=np.empty(self.ntiles, np.int32),
                    tileNnzOff=np.empty(self.ntiles + 1, np.int64),
-                   rowEnd=np.empty(self.ntiles * self.T, np.uint16),
-                   colIdx=np.empty(self.nnz, np.uint8), v64=np.empty(self.nnz, np.float64),
-                   v32=np.empty(self.nnz, np.float32), v16=np.empty(self.nnz, np.uint16),
+                   rowMask=np.empty(self.ntiles, np.uint64),
+                   tileWidth=np.empty(self.ntiles, np.uint8),
+                   colIdx=np.empty(ns, np.uint8), v64=np.empty(ns, np.float64),
+                   v32=np.empty(ns, np.float32), v16=np.empty(ns, np.uint16),
                    colExp=np.empty(self.n, np.int8))
-        ks = ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowEnd", "colIdx", "v64", "v32", "v16",
-              "colExp"]
+        ks = ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowMask", "tileWidth", "colIdx", "v64",
+              "v32", "v16", "colExp"]
         _check(lib().evocg_tiles_export(self.h, *[_ptr(out[k]) for k in ks]))
         return out
 
@@ -218,6 +221,7 @@ def get_tile_precision(A: Tiles, stream=None):
 
 SPMV_REUSE_XCOPIES = 1
 SPMV_DIRECT = 2
+SPMV_STAGED = 4
 
 
 def spmv(A: Tiles, x, y, stream=None):

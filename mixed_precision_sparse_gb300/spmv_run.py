@@ -2,6 +2,7 @@
 
     python -m mixed_precision_sparse_gb300.spmv_run [--workloads 2,3,5] [--reps 50]
                                                     [--maps mixed,fp64] [--launches K]
+                                                    [--kernel default|staged|direct]
 
 For each workload: build the tile structure, set the seeded 40/40/20 per-tile map (or the
 all-FP64 map), and launch the SpMV kernel back to back on device-resident x and y (every
@@ -29,14 +30,21 @@ from mixed_precision_sparse_gb300 import evocg  # noqa: E402
 from mixed_precision_sparse_gb300 import workloads as W  # noqa: E402
 
 
-def spmv_bytes(G, nnz_by_prec):
-    """Algorithmic bytes of one SpMV launch on handle G given the stored entries per
-    precision: the active value stream of every tile, the index arrays the kernel reads
-    (as reported by evocg_tiles_info, minus the export-only entry offsets), x read once and
-    y written once."""
-    d = G.info()
+def spmv_bytes(n, ntiles, nrb, nnz_by_prec):
+    """Algorithmic bytes of one SpMV launch: the active value stream of every stored entry
+    (pads not counted), one local-column byte per entry, per tile its column block (4),
+    first slot (8), row mask (8), width (1) and precision code (1), the row-block
+    pointers, x read once and y written once."""
     vals = 8 * int(nnz_by_prec[0]) + 4 * int(nnz_by_prec[1]) + 2 * int(nnz_by_prec[2])
-    return vals + int(d.bytes_index) + 16 * int(d.n)
+    return vals + int(sum(nnz_by_prec)) + 22 * int(ntiles) + 8 * (int(nrb) + 1) + 16 * int(n)
+
+
+def tile_entries(ex, T):
+    """Stored entries (slots that are not pads) of every tile, from an export."""
+    real = (ex["colIdx"] < T).astype(np.int64)
+    c = np.concatenate([[0], np.cumsum(real)])
+    off = ex["tileNnzOff"]
+    return c[off[1:]] - c[off[:-1]]
 
 
 def main(argv=None):
@@ -47,8 +55,8 @@ def main(argv=None):
     ap.add_argument("--maps", default="mixed,fp64")
     ap.add_argument("--reps", type=int, default=50)
     ap.add_argument("--launches", type=int, default=0)
-    ap.add_argument("--direct", action="store_true",
-                    help="time the direct kernel instead of the staged one")
+    ap.add_argument("--kernel", default="default", choices=["default", "staged", "direct"],
+                    help="SpMV kernel to time (default: the library's choice)")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -57,7 +65,7 @@ def main(argv=None):
         w = W.workload(cfg)
         G = evocg.tile_build(w.n, w.rp, w.ci, w.v, w.T)
         trow, ex = G.tile_rows()
-        tnnz = np.diff(ex["tileNnzOff"])
+        tnnz = tile_entries(ex, G.T)
         x = torch.from_numpy(np.random.default_rng(7).uniform(-1, 1, w.n)).to(dev)
         y = torch.empty_like(x)
         for label in a.maps.split(","):
@@ -71,7 +79,8 @@ def main(argv=None):
                 mp = np.zeros(G.ntiles, np.uint8)
             evocg.set_tile_precision(G, mp)
             evocg.spmv(G, x, y)
-            flags = evocg.SPMV_REUSE_XCOPIES | (evocg.SPMV_DIRECT if a.direct else 0)
+            kflag = {"default": 0, "staged": evocg.SPMV_STAGED, "direct": evocg.SPMV_DIRECT}[a.kernel]
+            flags = evocg.SPMV_REUSE_XCOPIES | kflag
             if a.launches:
                 for _ in range(a.launches):
                     evocg.spmv_ex(G, x, y, flags)
@@ -89,9 +98,9 @@ def main(argv=None):
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1000.0 / a.reps
             per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
-            B = spmv_bytes(G, per)
+            B = spmv_bytes(G.n, G.ntiles, G.nrb, per)
             print(json.dumps({"workload": w.name, "map": label,
-                              "kernel": "direct" if a.direct else "staged", "n": w.n, "nnz": w.nnz,
+                              "kernel": a.kernel, "n": w.n, "nnz": w.nnz,
                               "ntiles": int(G.ntiles), "us": round(us, 2), "bytes": B,
                               "gbs": round(B / us / 1e3, 1)}), flush=True)
         G.free()

@@ -38,8 +38,9 @@ def test_layout_bit_exact(name, m, T):
     P = Pair(m, T)
     g = P.G.export()
     t = P.t
-    assert (P.G.ntiles, P.G.nnz) == (t.ntiles, t.nnz)
-    for k in ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowEnd", "colIdx", "v16", "colExp"]:
+    assert (P.G.ntiles, P.G.nnz, P.G.nslots) == (t.ntiles, t.nnz, t.nslots)
+    for k in ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowMask", "tileWidth", "colIdx", "v16",
+              "colExp"]:
         assert np.array_equal(g[k], getattr(t, k)), k
     assert np.array_equal(g["v64"].view(np.uint64), t.v64.view(np.uint64))
     assert np.array_equal(g["v32"].view(np.uint32), t.v32.view(np.uint32))
@@ -167,8 +168,8 @@ def test_spmv_parity_full_size(cfg):
     w = W.workload(cfg)
     P = Pair((w.n, w.rp, w.ci, w.v), w.T)
     g = P.G.export()
-    assert np.array_equal(g["tileRowPtr"], P.t.tileRowPtr)
-    assert np.array_equal(g["tileColIdx"], P.t.tileColIdx)
+    for k in ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowMask", "tileWidth", "colIdx"]:
+        assert np.array_equal(g[k], getattr(P.t, k)), k
     x = np.random.default_rng(cfg).uniform(-1, 1, P.n)
     _check_spmv(P, None, x, TOL64)
     _check_spmv(P, P.tile_map(cfg), x, TOLMIX)
@@ -178,7 +179,7 @@ def test_spmv_parity_full_size(cfg):
     ("dense_t32", W.dense_to_csr(np.random.default_rng(0).standard_normal((100, 100)) + 200 * np.eye(100)), 32),
     ("dense_t64", W.dense_to_csr(np.random.default_rng(1).standard_normal((200, 200)) + 300 * np.eye(200)), 64),
 ], ids=[c[0] for c in CASES] + ["dense_t32", "dense_t64"])
-def test_spmv_staged_equals_direct(name, m, T):
+def test_spmv_kernels_agree(name, m, T):
     """The staged kernel (operands copied to shared memory by bulk asynchronous copies) and
     the direct kernel sum the same products in the same order for T >= 32: identical bits.
     For T = 16 the direct kernel gives alternate tiles of a row block to the two half-warps
@@ -189,24 +190,27 @@ def test_spmv_staged_equals_direct(name, m, T):
     x = torch.from_numpy(rng.uniform(-1, 1, P.n) * 10.0 ** rng.uniform(-3, 3, P.n)).cuda()
     for mp in (np.zeros(P.t.ntiles, np.uint8), P.tile_map(1), P.tile_map(2, (0, 0, 1)), P.tile_map(3, (0, 1, 0))):
         evocg.set_tile_precision(P.G, mp)
-        ys = torch.full((P.n,), np.nan, dtype=torch.float64, device="cuda")
-        yd = torch.full((P.n,), np.nan, dtype=torch.float64, device="cuda")
-        evocg.spmv(P.G, x, ys)
-        evocg.spmv_ex(P.G, x, yd, evocg.SPMV_REUSE_XCOPIES | evocg.SPMV_DIRECT)
+        ys = {}
+        for k, flag in (("staged", evocg.SPMV_STAGED), ("direct", evocg.SPMV_DIRECT), ("default", 0)):
+            ys[k] = torch.full((P.n,), np.nan, dtype=torch.float64, device="cuda")
+            evocg.spmv_ex(P.G, x, ys[k], flag)
         torch.cuda.synchronize()
         want = oracle.mixed_spmv(P.A, P.t, mp, x.cpu().numpy())
+        den = P.abs_sum(mp, x.cpu().numpy())
+        assert torch.equal(ys["default"].view(torch.int64), ys["staged"].view(torch.int64))
         if T >= 32:
-            assert torch.equal(ys.view(torch.int64), yd.view(torch.int64))
+            assert torch.equal(ys["staged"].view(torch.int64), ys["direct"].view(torch.int64))
         else:
-            e2 = row_rel_err(ys.cpu().numpy(), yd.cpu().numpy(), P.abs_sum(mp, x.cpu().numpy()))
-            assert e2.max() <= 1e-12
-        err = row_rel_err(ys.cpu().numpy(), want, P.abs_sum(mp, x.cpu().numpy()))
-        assert err.max() <= (TOL64 if not mp.any() else TOLMIX)
+            assert row_rel_err(ys["staged"].cpu().numpy(), ys["direct"].cpu().numpy(), den).max() <= 1e-12
+        for k in ys:
+            err = row_rel_err(ys[k].cpu().numpy(), want, den)
+            assert err.max() <= (TOL64 if not mp.any() else TOLMIX), k
 
 
 def test_spmv_misaligned_x_uses_direct_kernel():
-    """An x that is not 16-byte aligned cannot be a bulk-copy source: the library runs the
-    direct kernel and the result is unchanged."""
+    """An x that is not 16-byte aligned cannot be a bulk-copy source: asked for the staged
+    kernel, the library runs the direct kernel and the result is unchanged; the default
+    kernel reads x element by element and takes it as is."""
     P = Pair(W.diffusion3d_7pt(16, 2), 32)
     mp = P.tile_map(4)
     evocg.set_tile_precision(P.G, mp)
@@ -216,7 +220,10 @@ def test_spmv_misaligned_x_uses_direct_kernel():
     assert xa.data_ptr() % 16 == 8 and xb.data_ptr() % 16 == 0
     ya = torch.empty(P.n, dtype=torch.float64, device="cuda")
     yb = torch.empty_like(ya)
-    evocg.spmv(P.G, xa, ya)
-    evocg.spmv(P.G, xb, yb)
+    yc = torch.empty_like(ya)
+    evocg.spmv_ex(P.G, xa, ya, evocg.SPMV_STAGED)
+    evocg.spmv_ex(P.G, xb, yb, evocg.SPMV_STAGED)
+    evocg.spmv(P.G, xa, yc)
     torch.cuda.synchronize()
     assert torch.equal(ya.view(torch.int64), yb.view(torch.int64))
+    assert torch.equal(ya.view(torch.int64), yc.view(torch.int64))
