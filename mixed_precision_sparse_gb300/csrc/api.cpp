@@ -634,6 +634,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     L.map_kind = A->map_kind;
     L.mlpW = w.mlpW; L.H1 = H1; L.H2 = H2; L.delta = (kind == EVOCG_CTRL_MLP) ? ctrl->delta : 0.0;
     L.st = w.st; L.vec_grid = A->vec_grid; L.spmv_grid = A->spmv_grid;
+    L.upd_grid = A->sms * kUpdMinBlocks > kMaxBlocks ? kMaxBlocks : A->sms * kUpdMinBlocks;
     L.cond = 0;
 
     // graph cache: the key is every launch parameter (the handle aside)

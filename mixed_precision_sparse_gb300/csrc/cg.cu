@@ -88,6 +88,18 @@ __device__ __forceinline__ void write_copies(const CgLaunch &L, int64_t j, doubl
     L.x16f[j] = __fmul_rn(f32_from_bf16(bf16_from_f64_rn(v)), s);
 }
 
+// The same for the pair j, j + 1 (j even): one 2-byte exponent load, 8-byte stores.
+__device__ __forceinline__ void write_copies2(const CgLaunch &L, int64_t j, double v0, double v1)
+{
+    const char2 e = *reinterpret_cast<const char2 *>(L.A.colExp + j);
+    const float s0 = pow2f(e.x), s1 = pow2f(e.y);
+    *reinterpret_cast<float2 *>(L.x32 + j) =
+        make_float2(__fmul_rn(f32_from_f64_rn(v0), s0), __fmul_rn(f32_from_f64_rn(v1), s1));
+    *reinterpret_cast<float2 *>(L.x16f + j) =
+        make_float2(__fmul_rn(f32_from_bf16(bf16_from_f64_rn(v0)), s0),
+                    __fmul_rn(f32_from_bf16(bf16_from_f64_rn(v1)), s1));
+}
+
 // Start (restart = 0) or FP64-finish restart (restart = 1, after q = A x in FP64):
 //   r = b (x = 0) or r = b - q; z = D^-1 r; p = z; rho = r.z; ||r||^2.
 template <int T>
@@ -166,7 +178,7 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
 // block), alpha = rho / sigma; then x += alpha p; r -= alpha q; z = D^-1 r; r.z and ||r||^2.
 // The last block appends the history entry, tests convergence and forms beta. A sigma that
 // is not finite and positive stops the solve with EVOCG_EBREAKDOWN.
-__global__ void __launch_bounds__(kVecThreads) cg_update_kernel(CgLaunch L, int npq)
+__global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(CgLaunch L, int npq)
 {
     DevState *st = L.st;
     if (st->done) {
@@ -197,46 +209,63 @@ __global__ void __launch_bounds__(kVecThreads) cg_update_kernel(CgLaunch L, int 
     }
     const double alpha = s_alpha;
     if (isnan(alpha)) return;   // every block saw the same sigma
-    const int64_t n = L.n, npairs = (n + 1) / 2;
+    const int64_t n = L.n, nfull = n / 2;   // whole pairs; an odd last entry separately
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    double rz = 0.0, rr = 0.0;
-    for (int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; pair < npairs; pair += stride) {
+    // Two pairs per thread and pass, every load issued before any arithmetic, and two sets
+    // of dot-product partials, so that neither the loads nor the FP64 pipe wait on one
+    // chain of fused multiply-adds.
+    double rz0 = 0.0, rr0 = 0.0, rz1 = 0.0, rr1 = 0.0;
+    auto pair_update = [&](int64_t j, double2 p, double2 q, double2 x, double2 r, double2 d,
+                           double &rz, double &rr) {
+        x.x = fma(alpha, p.x, x.x);
+        x.y = fma(alpha, p.y, x.y);
+        r.x = fma(-alpha, q.x, r.x);
+        r.y = fma(-alpha, q.y, r.y);
+        *reinterpret_cast<double2 *>(L.x + j) = x;
+        *reinterpret_cast<double2 *>(L.r + j) = r;
+        rr = fma(r.x, r.x, rr);
+        rr = fma(r.y, r.y, rr);
+        if (L.jacobi) {
+            double2 z;
+            z.x = d.x * r.x;
+            z.y = d.y * r.y;
+            *reinterpret_cast<double2 *>(L.z + j) = z;
+            rz = fma(r.x, z.x, rz);
+            rz = fma(r.y, z.y, rz);
+        }
+    };
+    auto ld2 = [](const double *a, int64_t j) { return *reinterpret_cast<const double2 *>(a + j); };
+    int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (; pair + stride < nfull; pair += 2 * stride) {
+        const int64_t ja = 2 * pair, jb = 2 * (pair + stride);
+        const double2 pa = ld2(L.p, ja), pb = ld2(L.p, jb);
+        const double2 qa = ld2(L.q, ja), qb = ld2(L.q, jb);
+        const double2 xa = ld2(L.x, ja), xb = ld2(L.x, jb);
+        const double2 ra = ld2(L.r, ja), rb = ld2(L.r, jb);
+        double2 da = make_double2(0.0, 0.0), db = da;
+        if (L.jacobi) { da = ld2(L.dinv, ja); db = ld2(L.dinv, jb); }
+        pair_update(ja, pa, qa, xa, ra, da, rz0, rr0);
+        pair_update(jb, pb, qb, xb, rb, db, rz1, rr1);
+    }
+    if (pair < nfull) {
         const int64_t j = 2 * pair;
-        if (j + 1 < n) {
-            const double2 p = *reinterpret_cast<const double2 *>(L.p + j);
-            const double2 q = *reinterpret_cast<const double2 *>(L.q + j);
-            double2 x = *reinterpret_cast<const double2 *>(L.x + j);
-            double2 r = *reinterpret_cast<const double2 *>(L.r + j);
-            x.x = fma(alpha, p.x, x.x);
-            x.y = fma(alpha, p.y, x.y);
-            r.x = fma(-alpha, q.x, r.x);
-            r.y = fma(-alpha, q.y, r.y);
-            *reinterpret_cast<double2 *>(L.x + j) = x;
-            *reinterpret_cast<double2 *>(L.r + j) = r;
-            rr = fma(r.x, r.x, rr);
-            rr = fma(r.y, r.y, rr);
-            if (L.jacobi) {
-                const double2 d = *reinterpret_cast<const double2 *>(L.dinv + j);
-                double2 z;
-                z.x = d.x * r.x;
-                z.y = d.y * r.y;
-                *reinterpret_cast<double2 *>(L.z + j) = z;
-                rz = fma(r.x, z.x, rz);
-                rz = fma(r.y, z.y, rz);
-            }
-        } else {
-            const double x = fma(alpha, L.p[j], L.x[j]);
-            const double r = fma(-alpha, L.q[j], L.r[j]);
-            L.x[j] = x;
-            L.r[j] = r;
-            rr = fma(r, r, rr);
-            if (L.jacobi) {
-                const double z = L.dinv[j] * r;
-                L.z[j] = z;
-                rz = fma(r, z, rz);
-            }
+        const double2 d = L.jacobi ? ld2(L.dinv, j) : make_double2(0.0, 0.0);
+        pair_update(j, ld2(L.p, j), ld2(L.q, j), ld2(L.x, j), ld2(L.r, j), d, rz0, rr0);
+    }
+    if ((n & 1) && blockIdx.x == 0 && threadIdx.x == 0) {   // odd last entry
+        const int64_t j = n - 1;
+        const double x = fma(alpha, L.p[j], L.x[j]);
+        const double r = fma(-alpha, L.q[j], L.r[j]);
+        L.x[j] = x;
+        L.r[j] = r;
+        rr1 = fma(r, r, rr1);
+        if (L.jacobi) {
+            const double z = L.dinv[j] * r;
+            L.z[j] = z;
+            rz1 = fma(r, z, rz1);
         }
     }
+    const double rz = rz0 + rz1, rr = rr0 + rr1;
     const double s_rz = block_sum_cg(rz);
     const double s_rr = block_sum_cg(rr);
     if (threadIdx.x == 0) {
@@ -297,8 +326,7 @@ __global__ void __launch_bounds__(kVecThreads) cg_pupdate_kernel(CgLaunch L)
                 p.x = fma(beta, p.x, z.x);
                 p.y = fma(beta, p.y, z.y);
                 *reinterpret_cast<double2 *>(L.p + j) = p;
-                write_copies(L, j, p.x);
-                write_copies(L, j + 1, p.y);
+                write_copies2(L, j, p.x, p.y);
                 const uint64_t a0 = abs_bits(p.x), a1 = abs_bits(p.y);
                 m = a0 > a1 ? a0 : a1;
             } else {
@@ -387,7 +415,7 @@ cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
     if (npq > kMaxPq) return cudaErrorInvalidConfiguration;
     e = launch_spmv(S, s);
     if (e != cudaSuccess) return e;
-    cg_update_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L, npq);
+    cg_update_kernel<<<L.upd_grid, kVecThreads, 0, s>>>(L, npq);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (L.T) {

@@ -14,6 +14,7 @@ namespace evocg {
 constexpr int kMaxBlocks = 2048;      // upper bound of any grid here (partials buffers)
 constexpr int kMaxPq = 16384;         // per-warp p.q partials of one SpMV (grid x warps)
 constexpr int kVecThreads = 256;      // threads per block of the vector kernels
+constexpr int kUpdMinBlocks = 3;      // resident blocks per SM of the CG update kernel (its grid)
 constexpr int kSpmvThreads = 256;     // threads per block of the SpMV
 constexpr int kSpmvMinBlocks = 4;     // resident blocks per SM the SpMV registers are budgeted for
 constexpr int kMlpHiddenMax = 64;
@@ -257,6 +258,7 @@ struct CgLaunch {
     double delta;
     DevState *st;
     int vec_grid, spmv_grid;
+    int upd_grid;          // grid of the update kernel (kUpdMinBlocks per SM)
     cudaGraphConditionalHandle cond;
     int use_cond;          // 1 inside the solve graph: the kernels drive its while node
 };
