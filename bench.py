@@ -194,6 +194,23 @@ def run_reference(args):
 # GPU arm
 # --------------------------------------------------------------------------------------
 
+def max_over_ranks(v, dist, device):
+    """The largest of the ranks' values (the job's clock is its slowest replica); v itself
+    on a single process (dist None)."""
+    if not dist:
+        return float(v)
+    import torch
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_seconds_per_solve(ms_per_step, world):
+    """Whole-job time per solve: every rank runs one solve per step (independent replicas),
+    so a step of ms_per_step milliseconds completes `world` solves."""
+    return ms_per_step / 1000.0 / world
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -248,13 +265,9 @@ def run_ours(args):
         torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, dev)
     info = infos[-1]
-    value = ms / 1000.0 / world      # seconds per solve for the whole job
+    value = job_seconds_per_solve(ms, world)
     launches = 0
     for inf in infos:
         # init + 3 kernels per iteration (+1 policy kernel per iteration with the MLP),
@@ -274,11 +287,7 @@ def run_ours(args):
                  for _ in range(e2e_steps)]
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if dist:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     h2d = 8 * w.n
     d2h = 8 * w.n + 8 * (e2e_infos[-1]["iters"] + 1)
 
