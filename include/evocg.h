@@ -81,6 +81,13 @@ typedef struct {
                               hidden1), b2, W3 (3 x hidden2), b3, packed in that order, each
                               W row-major (out, in), FP32 */
     double delta;          /* MLP: the floor of the segment norm in phi (EvoCG Eq. 8) */
+    uint8_t *map_log;      /* NULL, or a HOST or DEVICE buffer of map_log_rows x nrb bytes: row k
+                              receives the column-block map the SpMV of iteration k used, for the
+                              iterations of the controlled phase (k < map_log_rows; rows past
+                              the last such iteration are left as they were). The profiling run
+                              of EvoCG §3.4 interval reuse: log with kstar = 1, then choose the
+                              interval with evocg_kstar_select. Ignored for EVOCG_CTRL_STATIC */
+    int64_t map_log_rows;
 } evocg_ctrl;
 
 typedef struct {
@@ -238,6 +245,23 @@ int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, double rtol, int
  */
 int evocg_ctrl_decide(evocg_tiles_t A, const evocg_ctrl *ctrl, const double *p,
                       uint8_t *cb_prec, float *logits, void *stream);
+
+/*
+ * Choose the reuse interval K* of EvoCG §3.4 (interval reuse scheduling) from a per-iteration
+ * log of column-block decisions (rows x ncb bytes, HOST, codes 0/1/2, row k = the map of
+ * iteration k, as evocg_ctrl.map_log records it with kstar = 1). An upward transition is a
+ * block whose code drops from row k-1 to row k (a higher precision). Reusing the decisions
+ * of every K-th iteration puts row K*floor(k/K) in force at iteration k; the transition is
+ * delayed when that row's code for the block is above row k's. For K = 1, 2, 4, ... up to
+ * the largest power of two <= rows, fractions[i] receives (delayed upward transitions) /
+ * (upward transitions), 0 when there are none; *kstar receives the largest K whose fraction
+ * is below `limit` (the paper: 0.1); K = 1 always qualifies.
+ *   fractions: NULL or room for max_candidates doubles; *ncand (may be NULL) receives the
+ *   number of candidates examined. A host-only computation: no GPU is needed.
+ * Errors: EINVAL (NULL log or kstar with rows > 0, ncb < 1, rows < 0, a code above 2).
+ */
+int evocg_kstar_select(const uint8_t *map_log, int64_t rows, int64_t ncb, double limit,
+                       int *kstar, double *fractions, int max_candidates, int *ncand);
 
 /*
  * The device's FP64 -> FP32 and FP64 -> BF16 rounding (integer-pipe, round to nearest

@@ -102,10 +102,10 @@ void release_ws(SolveWS &w)
 {
     release_graphs(w);
     dfree(w.b); dfree(w.x); dfree(w.r); dfree(w.p); dfree(w.q); dfree(w.z); dfree(w.hist);
-    dfree(w.partials); dfree(w.pq); dfree(w.cbPrec); dfree(w.mlpW); dfree(w.st);
+    dfree(w.partials); dfree(w.pq); dfree(w.cbPrec); dfree(w.mlpW); dfree(w.st); dfree(w.logbuf);
     if (w.st_host) cudaFreeHost(w.st_host);
     w.st_host = nullptr;
-    w.cap_n = 0; w.cap_hist = 0; w.cap_ncb = 0; w.cap_mlp = 0;
+    w.cap_n = 0; w.cap_hist = 0; w.cap_ncb = 0; w.cap_mlp = 0; w.cap_log = 0;
 }
 
 int ensure_ws(evocg_tiles *A, int maxit)
@@ -613,9 +613,31 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
         return fail(EVOCG_EINVAL, "unknown controller kind");
     if (kind == EVOCG_CTRL_THRESHOLD && !(ctrl->eps >= 0.0))
         return fail(EVOCG_EINVAL, "threshold eps must be >= 0");
+    const bool logging = kind != EVOCG_CTRL_STATIC && ctrl->map_log && ctrl->map_log_rows > 0 && A->nrb > 0;
+    if (kind != EVOCG_CTRL_STATIC && ctrl->map_log_rows < 0)
+        return fail(EVOCG_EINVAL, "map_log_rows must be >= 0");
     int rc = ensure_ws(A, maxit);
     if (rc) return rc;
     SolveWS &w = A->ws;
+    // decision log: written on the device; a host log goes through a library buffer
+    uint8_t *dlog = nullptr;
+    const bool host_log = logging && !is_device_ptr(ctrl->map_log);
+    const int64_t log_bytes = logging ? ctrl->map_log_rows * A->nrb : 0;
+    if (logging) {
+        if (host_log) {
+            if (w.cap_log < log_bytes) {
+                release_graphs(w);   // the graphs hold the buffer's address
+                dfree(w.logbuf);
+                CK(dalloc(&w.logbuf, log_bytes), "cudaMalloc decision log");
+                w.cap_log = log_bytes;
+            }
+            CK(cudaMemcpy(w.logbuf, ctrl->map_log, (size_t)log_bytes, cudaMemcpyHostToDevice),
+               "copy decision log");   // rows the solve does not reach keep their contents
+            dlog = w.logbuf;
+        } else {
+            dlog = ctrl->map_log;
+        }
+    }
     int H1 = 0, H2 = 0;
     if (kind == EVOCG_CTRL_MLP) {
         rc = upload_mlp(A, ctrl, &H1, &H2);
@@ -635,6 +657,8 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     L.mlpW = w.mlpW; L.H1 = H1; L.H2 = H2; L.delta = (kind == EVOCG_CTRL_MLP) ? ctrl->delta : 0.0;
     L.st = w.st; L.vec_grid = A->vec_grid; L.spmv_grid = A->spmv_grid;
     L.upd_grid = A->sms * kUpdMinBlocks > kMaxBlocks ? kMaxBlocks : A->sms * kUpdMinBlocks;
+    L.map_log = dlog;
+    L.map_log_rows = logging ? ctrl->map_log_rows : 0;
     L.cond = 0;
 
     // graph cache: the key is every launch parameter (the handle aside)
@@ -684,6 +708,8 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
             // continue from the true residual with every tile in FP64
             CgLaunch R = L;
             R.ctrl = EVOCG_CTRL_STATIC;
+            R.map_log = nullptr;   // the FP64 finish is not the controlled phase
+            R.map_log_rows = 0;
             uint64_t rkey = key ^ 0x9E3779B97F4A7C15ull;
             if (use_graph && (!w.exec_rs || w.exec_rs_key != rkey)) {
                 if (w.exec_rs) { cudaGraphExecDestroy(w.exec_rs); w.exec_rs = nullptr; }
@@ -709,6 +735,8 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     CK(cudaMemcpyAsync(&lost, A->errw, sizeof(int), cudaMemcpyDeviceToHost, s), "read error word");
     if (n > 0) CK(cudaMemcpyAsync(x, w.x, bytes, cudaMemcpyDefault, s), "copy x");
     if (res_hist) CK(cudaMemcpyAsync(res_hist, w.hist, sizeof(double) * (size_t)(k + 1), cudaMemcpyDefault, s), "copy history");
+    if (host_log)
+        CK(cudaMemcpyAsync(ctrl->map_log, dlog, (size_t)log_bytes, cudaMemcpyDeviceToHost, s), "copy decision log");
     CK(cudaStreamSynchronize(s), "synchronise outputs");
     if (info) {
         info->status = H.status;

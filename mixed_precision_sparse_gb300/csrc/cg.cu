@@ -387,12 +387,35 @@ cudaError_t launch_cg_init(const CgLaunch &L, int restart, cudaStream_t s)
     }
 }
 
-// One loop body: [MLP controller] -> SpMV (+ p.q, alpha) -> update -> p-update.
+// Row k of the decision log = the column-block map the SpMV of iteration k reads (k = the
+// iterations done so far); nothing once the solve has stopped or past the log's rows.
+__global__ void __launch_bounds__(kVecThreads)
+    log_map_kernel(const uint8_t *__restrict__ cbPrec, uint8_t *__restrict__ log, int64_t ncb,
+                   int64_t rows, const DevState *st)
+{
+    if (st->done) return;
+    const int64_t k = st->k;
+    if (k < 0 || k >= rows) return;
+    uint8_t *row = log + k * ncb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < ncb;
+         i += (int64_t)gridDim.x * blockDim.x)
+        row[i] = cbPrec[i];
+}
+
+// One loop body: [MLP controller] -> [decision log] -> SpMV (+ p.q, alpha) -> update -> p-update.
 cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
 {
     cudaError_t e;
     if (!force64 && L.ctrl == EVOCG_CTRL_MLP) {
         e = launch_ctrl_mlp(L.A, L.p, L.mlpW, L.H1, L.H2, L.delta, L.cbPrec, nullptr, L.st, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (!force64 && L.ctrl != EVOCG_CTRL_STATIC && L.map_log) {
+        const int64_t ncb = L.A.nrb;
+        int64_t g = (ncb + kVecThreads - 1) / kVecThreads;
+        if (g > 1024) g = 1024;
+        log_map_kernel<<<(int)g, kVecThreads, 0, s>>>(L.cbPrec, L.map_log, ncb, L.map_log_rows, L.st);
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     SpmvLaunch S{};

@@ -106,6 +106,8 @@ struct SolveWS {
     double *partials = nullptr;       // 2 * kMaxBlocks
     double *pq = nullptr;             // kMaxPq per-warp p.q partials of the SpMV
     uint8_t *cbPrec = nullptr;        // controller decisions per column block
+    uint8_t *logbuf = nullptr;        // device copy of a host decision log
+    int64_t cap_log = 0;
     float *mlpW = nullptr;            // packed MLP weights on the device
     int64_t cap_mlp = 0;
     DevState *st = nullptr;
@@ -259,6 +261,8 @@ struct CgLaunch {
     DevState *st;
     int vec_grid, spmv_grid;
     int upd_grid;          // grid of the update kernel (kUpdMinBlocks per SM)
+    uint8_t *map_log;      // device decision log (NULL: none), map_log_rows x ncb
+    int64_t map_log_rows;
     cudaGraphConditionalHandle cond;
     int use_cond;          // 1 inside the solve graph: the kernels drive its while node
 };

@@ -42,7 +42,15 @@ class TilesDesc(C.Structure):
 class Ctrl(C.Structure):
     _fields_ = [("kind", C.c_int), ("kstar", C.c_int), ("eps", C.c_double),
                 ("hidden1", C.c_int), ("hidden2", C.c_int), ("weights", C.c_void_p),
-                ("delta", C.c_double)]
+                ("delta", C.c_double), ("map_log", C.c_void_p), ("map_log_rows", C.c_int64)]
+
+    def log_to(self, log) -> "Ctrl":
+        """Record the per-iteration column-block maps into `log` (rows x nrb uint8, a numpy
+        array or a CUDA tensor) during the next solves with this controller."""
+        self.map_log = _ptr(log)
+        self.map_log_rows = int(log.shape[0])
+        self._keep_log = log
+        return self
 
     @staticmethod
     def threshold(eps: float, kstar: int = 1) -> "Ctrl":
@@ -98,6 +106,8 @@ def lib():
                                    C.POINTER(SolveInfo), P],
                 "evocg_ctrl_decide": [P, C.POINTER(Ctrl), P, P, P, P],
                 "evocg_round": [P, i64, P, P, P],
+                "evocg_kstar_select": [P, i64, i64, dbl, C.POINTER(C.c_int), P, i32,
+                                       C.POINTER(C.c_int)],
                 "evocg_version": [],
             }
             for name, args in sig.items():
@@ -256,6 +266,18 @@ def ctrl_decide(A: Tiles, ctrl: Ctrl, p, cb_prec, logits=None, stream=None):
     _check(lib().evocg_ctrl_decide(A.h, C.byref(ctrl), _ptr(p), _ptr(cb_prec), _ptr(logits),
                                    _stream(stream)))
     return cb_prec
+
+
+def kstar_select(map_log, limit: float = 0.1):
+    """Reuse interval K* (EvoCG §3.4) from a (rows, nrb) host decision log: (K*, fractions of
+    delayed upward transitions for K = 1, 2, 4, ...)."""
+    log = _np(map_log, np.uint8)
+    rows, ncb = log.shape
+    ks, nc = C.c_int(), C.c_int()
+    frac = np.zeros(64)
+    _check(lib().evocg_kstar_select(_ptr(log), int(rows), int(ncb), float(limit), C.byref(ks),
+                                    _ptr(frac), 64, C.byref(nc)))
+    return ks.value, frac[: nc.value]
 
 
 def round_fp(x, out32=None, out16=None, stream=None):

@@ -58,6 +58,8 @@ def _load():
             lib.ora_tile_count.restype = i32
             lib.ora_tile_build.argtypes = [i64, P, P, P, i32] + [P] * 10
             lib.ora_tile_build.restype = i32
+            lib.ora_kstar_select.argtypes = [P, i64, i64, C.c_double, P, P, i32]
+            lib.ora_kstar_select.restype = i32
             lib.ora_mixed_spmv.argtypes = [i64, P, P, P, i32, P, P, P, P, P, P]
             lib.ora_ctrl_threshold.argtypes = [i64, i32, P, dbl, P]
             lib.ora_ctrl_mlp.argtypes = [i64, i32, P, i32, i32, P, P, P, P, P, P, dbl, P, P]
@@ -268,3 +270,15 @@ def cg(A: CSR, tiles: Tiles, b, rtol: float, maxit: int, jacobi: bool = False,
     return dict(status=st, x=x, iters=it, iters_rec=int(out[1]), restarts=int(out[2]),
                 hist=hist[: it + 1].copy(), rel_res=float(fout[0]), true_res=float(fout[1]),
                 prec_nnz=pn.copy())
+
+
+def kstar_select(log, limit: float = 0.1):
+    """Reuse interval of EvoCG §3.4 from a (rows, ncb) uint8 decision log: (K*, fractions of
+    delayed upward transitions for K = 1, 2, 4, ...)."""
+    log = _c(log, np.uint8)
+    rows, ncb = log.shape
+    ks = C.c_int()
+    frac = np.zeros(64)
+    nc = _load().ora_kstar_select(_p(log), int(rows), int(ncb), float(limit), C.byref(ks),
+                                  _p(frac), 64)
+    return ks.value, frac[:nc]

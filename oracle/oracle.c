@@ -567,3 +567,40 @@ int ora_cg_flat(int64_t n, const int64_t *rp, const int32_t *ci, const double *v
     return ora_cg(n, rp, ci, v, T, tileRowPtr, tileColIdx, colExp, b, x, rtol, maxit, jacobi,
                   &c, finish_fp64, hist, out, fout, prec_nnz);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Reuse interval K* (EvoCG §3.4, interval reuse scheduling).                */
+/* ------------------------------------------------------------------------ */
+
+/* For each candidate interval K = 1, 2, 4, ... (up to the largest power of two not above
+ * `rows`), count over every column block i and iteration k >= 1 the upward transitions
+ * (the block's code at k below its code at k-1: a higher precision) and, among them, those
+ * that reusing every K-th decision would delay: the decision in force at k is the one of
+ * iteration K*floor(k/K), and the transition is delayed when that decision's code is above
+ * the code at k. frac[K index] = delayed / upward (0 with no upward transition); *kstar =
+ * the largest K with frac below `limit` (1 if none is). Returns the number of candidates. */
+int ora_kstar_select(const uint8_t *log, int64_t rows, int64_t ncb, double limit,
+                     int *kstar, double *frac, int max_frac)
+{
+    int nc = 0;
+    *kstar = 1;
+    int64_t top = rows > 0 ? rows : 1;
+    for (int64_t K = 1; K <= top; K *= 2) {
+        int64_t up = 0, delayed = 0;
+        for (int64_t i = 0; i < ncb; ++i) {
+            for (int64_t k = 1; k < rows; ++k) {
+                int before = log[(k - 1) * ncb + i];
+                int now = log[k * ncb + i];
+                if (now >= before) continue;          /* not an upward transition */
+                up++;
+                int64_t start = k - (k % K);          /* the window's decision iteration */
+                if (log[start * ncb + i] > now) delayed++;
+            }
+        }
+        double f = (up == 0) ? 0.0 : (double)delayed / (double)up;
+        if (nc < max_frac) frac[nc] = f;
+        nc++;
+        if (f < limit && K > *kstar) *kstar = (int)K;
+    }
+    return nc;
+}
