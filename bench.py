@@ -119,10 +119,22 @@ def _traffic_for(kernel_src_hash):
 
 
 def _src_hash():
+    """Hash of what the SpMV kernels are built from: their sources and, from the internal
+    header, the structures they read (DevState, TilesView, StagedLimits and the stage-size
+    helper, SpmvLaunch); other declarations of the header do not change the kernel."""
+    import re
+    csrc = os.path.join(ROOT, "mixed_precision_sparse_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("spmv.cu", "spmv_staged.cu", "staged_plan.cpp", "fpconv.cuh", "evocg_internal.h"):
-        with open(os.path.join(ROOT, "mixed_precision_sparse_gb300", "csrc", name), "rb") as f:
+    for name in ("spmv.cu", "spmv_staged.cu", "staged_plan.cpp", "fpconv.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
+    with open(os.path.join(csrc, "evocg_internal.h")) as f:
+        hdr = f.read()
+    for pat in (r"struct DevState \{.*?\n\};", r"struct TilesView \{.*?\n\};",
+                r"struct StagedLimits \{.*?\n\};", r"inline int staged_slot_bytes.*?\n\}",
+                r"struct SpmvLaunch \{.*?\n\};", r"constexpr int k\w+ = [^;]*;"):
+        for m in re.findall(pat, hdr, flags=re.S):
+            h.update(m.encode())
     return h.hexdigest()
 
 
