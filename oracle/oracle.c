@@ -29,6 +29,10 @@
  *    h = its nonempty rows) and slot (k, j) holds the k-th entry of the j-th
  *    nonempty row, so that one lane per row reads consecutive slots. The
  *    inter-tile level is CSR over row blocks as in EvoCG Fig. 4(a).
+ *  - The reuse interval K* (EvoCG §3.4) is the largest of 1, 2, 4, ... for which fewer than
+ *    10% of the upward transitions in a per-iteration decision log would be delayed, a
+ *    transition at iteration k being delayed when the decision of iteration K*floor(k/K)
+ *    has a lower precision than iteration k's.
  *
  * Parity pins live in tests/test_oracle_*.py. The MLP controller is pinned only
  * through special cases and invariances (its weights are seeded, not trained):
