@@ -56,3 +56,18 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = type("A", (), dict(workload=1, warmup=1, steps=1, cpu_sample_iters=1, gpus=2))()
     assert bench.run_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
+    """The reference arm (the oracle on the host cores) prints one JSON line with the keys
+    the harness reads; a bounded sample of the 64 x 64 Laplacian solve keeps it quick."""
+    import json
+    monkeypatch.setenv("RANK", "0")
+    args = type("A", (), dict(workload=1, warmup=1, steps=2, cpu_sample_iters=3, gpus=1))()
+    assert bench.run_reference(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "s" and line["higher_is_better"] is False
+    assert line["metric"] == bench.METRIC and line["steps"] == 2 and line["warmup"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["value"] is None or line["value"] > 0
