@@ -67,7 +67,7 @@ def _load():
             lib.ora_true_residual.restype = dbl
             lib.ora_cg_flat.argtypes = ([i64, P, P, P, i32, P, P, P, P, P, dbl, i32, i32,
                                          i32, P, dbl, i32, i32, i32] + [P] * 6 +
-                                        [dbl, i32, P, P, P, P])
+                                        [dbl, i32, P, P, P, P, P, i64, P, i64])
             lib.ora_cg_flat.restype = i32
             _lib = lib
     return _lib
@@ -242,11 +242,16 @@ def true_residual(A: CSR, b, x) -> float:
 
 def cg(A: CSR, tiles: Tiles, b, rtol: float, maxit: int, jacobi: bool = False,
        ctrl: str = "static", tile_map=None, eps: float = 0.0, kstar: int = 1,
-       weights=None, delta: float = 1e-30, finish_fp64: bool = False):
-    """CG / Jacobi-PCG with a static map or an in-loop controller ('threshold', 'mlp').
+       weights=None, delta: float = 1e-30, finish_fp64: bool = False, replay=None,
+       log_rows: int = 0):
+    """CG / Jacobi-PCG with a static map, an in-loop controller ('threshold', 'mlp'), or a
+    replayed sequence of column-block maps ('replay': row k of `replay` at iteration k, the
+    last row past its end).
 
     Returns a dict: status, x, iters, iters_rec, restarts, hist (iters+1 entries),
-    rel_res (recursive), true_res (FP64 recomputed), prec_nnz (entries per precision).
+    rel_res (recursive), true_res (FP64 recomputed), prec_nnz (entries per precision), and
+    with log_rows > 0 `log`: the column-block map in force at each of the first log_rows
+    iterations of the controlled phase (rows it did not reach hold 255).
     """
     b = _c(b, np.float64)
     x = np.zeros(A.n, np.float64)
@@ -254,7 +259,11 @@ def cg(A: CSR, tiles: Tiles, b, rtol: float, maxit: int, jacobi: bool = False,
     out = np.zeros(3, np.int64)
     fout = np.zeros(2, np.float64)
     pn = np.zeros(3, np.int64)
-    kind = {"static": 0, "threshold": 1, "mlp": 2}[ctrl]
+    kind = {"static": 0, "threshold": 1, "mlp": 2, "replay": 3}[ctrl]
+    rp_log = None if replay is None else _c(replay, np.uint8)
+    if kind == 3 and (rp_log is None or rp_log.ndim != 2 or rp_log.shape[1] != tiles.nrb):
+        raise ValueError("replay needs a (rows, nrb) uint8 map log")
+    logo = np.full((max(int(log_rows), 0), tiles.nrb), 255, np.uint8) if log_rows > 0 else None
     tm = None if tile_map is None else _c(tile_map, np.uint8)
     if weights is not None:
         W = [_c(w, np.float32) for w in weights]
@@ -265,11 +274,16 @@ def cg(A: CSR, tiles: Tiles, b, rtol: float, maxit: int, jacobi: bool = False,
                              _p(tiles.tileColIdx), _p(tiles.colExp), _p(b), _p(x), float(rtol),
                              int(maxit), int(bool(jacobi)), kind, _p(tm), float(eps), int(kstar),
                              H1, H2, *[_p(w) for w in W], float(delta), int(bool(finish_fp64)),
-                             _p(hist), _p(out), _p(fout), _p(pn))
+                             _p(hist), _p(out), _p(fout), _p(pn), _p(rp_log),
+                             0 if rp_log is None else int(rp_log.shape[0]), _p(logo),
+                             0 if logo is None else int(logo.shape[0]))
     it = int(out[0])
-    return dict(status=st, x=x, iters=it, iters_rec=int(out[1]), restarts=int(out[2]),
-                hist=hist[: it + 1].copy(), rel_res=float(fout[0]), true_res=float(fout[1]),
-                prec_nnz=pn.copy())
+    res = dict(status=st, x=x, iters=it, iters_rec=int(out[1]), restarts=int(out[2]),
+               hist=hist[: it + 1].copy(), rel_res=float(fout[0]), true_res=float(fout[1]),
+               prec_nnz=pn.copy())
+    if logo is not None:
+        res["log"] = logo
+    return res
 
 
 def kstar_select(log, limit: float = 0.1):

@@ -412,13 +412,20 @@ void ora_ctrl_mlp(int64_t n, int T, const double *p, int H1, int H2,
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
-    int ctrl;            /* 0 = static map (tileMap, or all FP64 when NULL), 1 = threshold, 2 = MLP */
+    int ctrl;            /* 0 = static map (tileMap, or all FP64 when NULL), 1 = threshold,
+                            2 = MLP, 3 = replay: iteration k uses row k of `replay` (the last
+                            row past its end), a column-block map per row */
     const uint8_t *tileMap;
     double eps;          /* threshold rule */
     int kstar;           /* controller interval, >= 1 */
     int H1, H2;
     const float *W1, *b1, *W2, *b2, *W3, *b3;
     double delta;
+    const uint8_t *replay;   /* replayRows x ncb column-block codes (ctrl 3) */
+    int64_t replayRows;
+    uint8_t *logOut;         /* NULL, or logRows x ncb: row k = the column-block map in force
+                                at iteration k of the controlled phase (ctrl 1, 2, 3) */
+    int64_t logRows;
 } ora_ctrl_t;
 
 static double dot(int64_t n, const double *a, const double *b)
@@ -509,7 +516,11 @@ int ora_cg(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int
         double rho = dot(n, r, z);
         int converged = 0;
         while (k < maxit) {
-            if (!allfp64 && ctrl->ctrl != 0 && k % ctrl->kstar == 0) {
+            if (!allfp64 && ctrl->ctrl == 3) {
+                int64_t row = k < ctrl->replayRows ? k : ctrl->replayRows - 1;
+                for (int64_t cb = 0; cb < ncb; ++cb) cbp[cb] = ctrl->replay[row * ncb + cb];
+                for (int64_t t = 0; t < ntiles; ++t) map[t] = cbp[tileColIdx[t]];
+            } else if (!allfp64 && ctrl->ctrl != 0 && k % ctrl->kstar == 0) {
                 if (ctrl->ctrl == 1)
                     ora_ctrl_threshold(n, T, p, ctrl->eps, cbp);
                 else
@@ -517,6 +528,8 @@ int ora_cg(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int
                                  ctrl->b2, ctrl->W3, ctrl->b3, ctrl->delta, cbp, NULL);
                 for (int64_t t = 0; t < ntiles; ++t) map[t] = cbp[tileColIdx[t]];
             }
+            if (!allfp64 && ctrl->ctrl != 0 && ctrl->logOut && k < ctrl->logRows)
+                for (int64_t cb = 0; cb < ncb; ++cb) ctrl->logOut[k * ncb + cb] = cbp[cb];
             for (int64_t t = 0; t < ntiles; ++t) prec_nnz[map[t]] += tnnz[t];
             ora_mixed_spmv(n, rp, ci, v, T, colExp, tileRowPtr, tileColIdx, map, p, q);
             double sigma = dot(n, p, q);
@@ -562,12 +575,15 @@ int ora_cg_flat(int64_t n, const int64_t *rp, const int32_t *ci, const double *v
                 int ctrl_kind, const uint8_t *tileMap, double eps, int kstar,
                 int H1, int H2, const float *W1, const float *b1, const float *W2,
                 const float *b2, const float *W3, const float *b3, double delta,
-                int finish_fp64, double *hist, int64_t *out, double *fout, int64_t *prec_nnz)
+                int finish_fp64, double *hist, int64_t *out, double *fout, int64_t *prec_nnz,
+                const uint8_t *replay, int64_t replayRows, uint8_t *logOut, int64_t logRows)
 {
     ora_ctrl_t c;
     c.ctrl = ctrl_kind; c.tileMap = tileMap; c.eps = eps; c.kstar = kstar > 0 ? kstar : 1;
     c.H1 = H1; c.H2 = H2; c.W1 = W1; c.b1 = b1; c.W2 = W2; c.b2 = b2; c.W3 = W3; c.b3 = b3;
     c.delta = delta;
+    c.replay = replay; c.replayRows = replayRows; c.logOut = logOut; c.logRows = logRows;
+    if (ctrl_kind == 3 && (!replay || replayRows < 1)) return ORA_EINVAL;
     return ora_cg(n, rp, ci, v, T, tileRowPtr, tileColIdx, colExp, b, x, rtol, maxit, jacobi,
                   &c, finish_fp64, hist, out, fout, prec_nnz);
 }

@@ -196,3 +196,44 @@ def test_mlp_normalisation_invariance_and_delta():
     want = _forward_np(tiny, T, w, 1e-30)
     assert np.allclose(lc, want, atol=1e-12)
     assert not np.allclose(lc, la)
+
+
+# ---------------------------------------------------------------- decision log and replay
+
+@pytest.mark.parametrize("kind", ["threshold", "mlp"])
+def test_replaying_the_decision_log_reproduces_the_controlled_solve(kind):
+    """Row k of the oracle's decision log is the column-block map of iteration k: feeding the
+    log back as a fixed schedule must give the controlled solve again, bit for bit, and the
+    log weighted by each block's stored entries must give the solve's precision census."""
+    if kind == "threshold":
+        w = W.workload(2, scale=0.125)
+        kw = dict(ctrl="threshold", eps=w.eps)
+    else:
+        w = W.workload(3, scale=0.125)
+        kw = dict(ctrl="mlp", weights=W.mlp_weights(w.T, w.mlp_seed), delta=w.delta)
+    A, t = _setup((w.n, w.rp, w.ci, w.v), w.T)
+    ref = oracle.cg(A, t, w.b, w.rtol, w.maxit, jacobi=True, finish_fp64=True,
+                    log_rows=w.maxit, **kw)
+    rec = ref["iters_rec"]
+    log = ref["log"]
+    assert rec > 0 and np.all(log[:rec] <= 2) and np.all(log[rec:] == 255)
+    rep = oracle.cg(A, t, w.b, w.rtol, w.maxit, jacobi=True, finish_fp64=True,
+                    ctrl="replay", replay=log[:rec])
+    assert rep["iters"] == ref["iters"] and rep["iters_rec"] == rec
+    assert np.array_equal(rep["hist"].view(np.uint64), ref["hist"].view(np.uint64))
+    assert np.array_equal(rep["x"].view(np.uint64), ref["x"].view(np.uint64))
+    ent = np.zeros(t.nrb, np.int64)
+    np.add.at(ent, t.tileColIdx.astype(np.int64), t.tile_entries())
+    want = np.array([((log[:rec] == c) * ent[None, :]).sum() for c in range(3)], np.int64)
+    want[0] += (ref["iters"] - rec) * ent.sum()
+    assert np.array_equal(ref["prec_nnz"], want)
+
+
+def test_replay_of_an_all_fp64_log_is_the_fp64_solve():
+    w = W.workload(1)
+    A, t = _setup((w.n, w.rp, w.ci, w.v), w.T)
+    plain = oracle.cg(A, t, w.b, w.rtol, w.maxit)
+    rep = oracle.cg(A, t, w.b, w.rtol, w.maxit, ctrl="replay",
+                    replay=np.zeros((3, t.nrb), np.uint8))     # shorter than the solve
+    assert rep["iters"] == plain["iters"]
+    assert np.array_equal(rep["hist"].view(np.uint64), plain["hist"].view(np.uint64))
