@@ -143,6 +143,22 @@ int evocg_tiles_export(evocg_tiles_t A, int64_t *tileRowPtr, int32_t *tileColIdx
                        int8_t *colExp);
 
 /*
+ * The tile layout of evocg_tile_build computed on the HOST only, without a GPU: the same
+ * builder, its arrays written to caller buffers (sizes as in evocg_tiles_export: tileRowPtr
+ * nrb+1, tileColIdx / tileNnzOff(+1) / rowMask / tileWidth ntiles, colIdx / v64 / v32 / v16
+ * nslots, colExp n), for inspecting a layout or checking it where no device is present.
+ *   n, row_ptr, col_idx, vals, tile_size: as evocg_tile_build (HOST arrays).
+ *   ntiles, nslots: receive the sizes (either may be NULL). Every array pointer may be NULL;
+ *   a call with all of them NULL only sizes the layout (the builder runs on every call).
+ * Errors: as evocg_tile_build (EINVAL, ENOMEM); no device is touched.
+ */
+int evocg_tile_layout_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                           const double *vals, int tile_size, int64_t *ntiles, int64_t *nslots,
+                           int64_t *tileRowPtr, int32_t *tileColIdx, int64_t *tileNnzOff,
+                           uint64_t *rowMask, uint8_t *tileWidth, uint8_t *colIdx, double *v64,
+                           float *v32, uint16_t *v16, int8_t *colExp);
+
+/*
  * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
  *   map: host or device, len = ntiles (PER_TILE) or nrb (PER_COLBLOCK).
  * The SpMV and static-map solves read the map set last. Errors: EINVAL on a wrong length

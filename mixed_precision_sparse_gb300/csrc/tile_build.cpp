@@ -240,3 +240,34 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
 }
 
 }  // namespace evocg
+
+extern "C" int evocg_tile_layout_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                                      const double *vals, int tile_size, int64_t *ntiles,
+                                      int64_t *nslots, int64_t *tileRowPtr, int32_t *tileColIdx,
+                                      int64_t *tileNnzOff, uint64_t *rowMask, uint8_t *tileWidth,
+                                      uint8_t *colIdx, double *v64, float *v32, uint16_t *v16,
+                                      int8_t *colExp)
+{
+    evocg::set_error("");
+    evocg::HostTiles H;
+    std::string err;
+    const int rc = evocg::build_host_tiles(n, row_ptr, col_idx, vals, tile_size, &H, &err);
+    if (rc) return evocg::fail(rc, err);
+    if (ntiles) *ntiles = H.ntiles;
+    if (nslots) *nslots = H.nslots;
+    auto put = [](auto *dst, const auto *src, int64_t count) {
+        if (dst && count > 0) std::memcpy(dst, src, sizeof(*dst) * (size_t)count);
+    };
+    put(tileRowPtr, H.tileRowPtr, H.nrb + 1);
+    put(tileColIdx, H.tileColIdx, H.ntiles);
+    put(tileNnzOff, H.tileNnzOff, H.ntiles + 1);
+    put(rowMask, H.rowMask, H.ntiles);
+    put(tileWidth, H.tileWidth, H.ntiles);
+    put(colIdx, H.colIdx, H.nslots);
+    put(v64, H.v64, H.nslots);
+    put(v32, H.v32, H.nslots);
+    put(v16, H.v16, H.nslots);
+    put(colExp, H.colExp, H.n);
+    H.release();
+    return EVOCG_OK;
+}

@@ -108,6 +108,8 @@ def lib():
                 "evocg_round": [P, i64, P, P, P],
                 "evocg_kstar_select": [P, i64, i64, dbl, C.POINTER(C.c_int), P, i32,
                                        C.POINTER(C.c_int)],
+                "evocg_tile_layout_host": [i64, P, P, P, i32, C.POINTER(C.c_int64),
+                                           C.POINTER(C.c_int64)] + [P] * 10,
                 "evocg_version": [],
             }
             for name, args in sig.items():
@@ -215,6 +217,29 @@ def tile_build(n, row_ptr, col_idx, vals, tile_size: int) -> Tiles:
     _check(lib().evocg_tile_build(int(n), _ptr(rp), _ptr(ci), _ptr(v), int(tile_size),
                                   C.byref(h)))
     return Tiles(h.value)
+
+
+def tile_layout_host(n, row_ptr, col_idx, vals, tile_size: int) -> dict:
+    """The tile layout evocg_tile_build would make, computed on the host (no GPU): a dict of
+    the arrays evocg_tiles_export returns, plus ntiles and nslots."""
+    rp, ci, v = _np(row_ptr, np.int64), _np(col_idx, np.int32), _np(vals, np.float64)
+    nt, ns = C.c_int64(), C.c_int64()
+    nul = [None] * 10
+    _check(lib().evocg_tile_layout_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), int(tile_size),
+                                        C.byref(nt), C.byref(ns), *nul))
+    T = int(tile_size)
+    nrb = (int(n) + T - 1) // T
+    out = dict(tileRowPtr=np.empty(nrb + 1, np.int64), tileColIdx=np.empty(nt.value, np.int32),
+               tileNnzOff=np.empty(nt.value + 1, np.int64), rowMask=np.empty(nt.value, np.uint64),
+               tileWidth=np.empty(nt.value, np.uint8), colIdx=np.empty(ns.value, np.uint8),
+               v64=np.empty(ns.value, np.float64), v32=np.empty(ns.value, np.float32),
+               v16=np.empty(ns.value, np.uint16), colExp=np.empty(int(n), np.int8))
+    ks = ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowMask", "tileWidth", "colIdx", "v64",
+          "v32", "v16", "colExp"]
+    _check(lib().evocg_tile_layout_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), T, None, None,
+                                        *[_ptr(out[k]) for k in ks]))
+    out["ntiles"], out["nslots"] = nt.value, ns.value
+    return out
 
 
 def set_tile_precision(A: Tiles, prec_map, map_kind: int = MAP_PER_TILE, stream=None):
