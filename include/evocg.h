@@ -159,6 +159,20 @@ int evocg_tile_layout_host(int64_t n, const int64_t *row_ptr, const int32_t *col
                            float *v32, uint16_t *v16, int8_t *colExp);
 
 /*
+ * The staged SpMV's static work plan for a matrix, computed on the HOST only (no GPU), for
+ * inspection: the same builder and planner evocg_tile_build runs, for `warps` consumer
+ * warps (the library plans for its grid times the consumer warps of a block).
+ *   *nbatches receives the number of batches; *valid 1 when the plan passes the checks the
+ *   library applies before using it (warp ranges tiling the row blocks, batches covering
+ *   each warp's tiles in order, every batch inside a stage), 0 when the library would run
+ *   the direct kernel instead. Either pointer may be NULL.
+ * Errors: as evocg_tile_build; EINVAL for warps < 1 or a tile size without a staged kernel.
+ */
+int evocg_staged_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                           const double *vals, int tile_size, int64_t warps, int64_t *nbatches,
+                           int *valid);
+
+/*
  * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
  *   map: host or device, len = ntiles (PER_TILE) or nrb (PER_COLBLOCK).
  * The SpMV and static-map solves read the map set last. Errors: EINVAL on a wrong length

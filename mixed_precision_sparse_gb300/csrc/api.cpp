@@ -333,7 +333,8 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
             std::vector<int64_t> bt;
             std::vector<uint16_t> slot;
             staged_plan(H, (int64_t)grid * lim.warps_per_block, lim, &wr, &wbt, &bt, &slot);
-            bool small = true;   // the kernel uses 32-bit entry offsets inside a warp
+            bool small = staged_plan_ok(H, (int64_t)grid * lim.warps_per_block, lim, wr, wbt, bt, slot);
+            // the kernel uses 32-bit entry offsets inside a warp
             for (size_t w = 0; w + 1 < wr.size() && small; ++w)
                 small = H.tileNnzOff[H.tileRowPtr[wr[w + 1]]] - H.tileNnzOff[H.tileRowPtr[wr[w]]] <
                         (1ll << 28) - 64;

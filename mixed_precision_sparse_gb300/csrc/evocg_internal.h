@@ -230,10 +230,14 @@ cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s);
 int staged_grid_for(int T, int sms);   // 0 if it cannot run
 int staged_warps_per_block(int T);      // consumer warps (the ones with rows) per block
 
-// Host: the staged SpMV plan for `warps` warps (api.cpp).
+// Host: the staged SpMV plan for `warps` warps (staged_plan.cpp), and its check against
+// what the kernel assumes of it.
 void staged_plan(const HostTiles &H, int64_t warps, const StagedLimits &lim,
                  std::vector<int32_t> *warpRb, std::vector<int32_t> *warpBatch,
                  std::vector<int64_t> *batchTile, std::vector<uint16_t> *tileSlot);
+bool staged_plan_ok(const HostTiles &H, int64_t warps, const StagedLimits &lim,
+                    const std::vector<int32_t> &wr, const std::vector<int32_t> &wbt,
+                    const std::vector<int64_t> &bt, const std::vector<uint16_t> &slot);
 cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, float *x16f,
                            int grid, cudaStream_t s);
 cudaError_t launch_round(const double *x, int64_t n, float *o32, uint16_t *o16, cudaStream_t s);

@@ -110,6 +110,8 @@ def lib():
                                        C.POINTER(C.c_int)],
                 "evocg_tile_layout_host": [i64, P, P, P, i32, C.POINTER(C.c_int64),
                                            C.POINTER(C.c_int64)] + [P] * 10,
+                "evocg_staged_plan_host": [i64, P, P, P, i32, i64, C.POINTER(C.c_int64),
+                                           C.POINTER(C.c_int)],
                 "evocg_version": [],
             }
             for name, args in sig.items():
@@ -240,6 +242,15 @@ def tile_layout_host(n, row_ptr, col_idx, vals, tile_size: int) -> dict:
                                         *[_ptr(out[k]) for k in ks]))
     out["ntiles"], out["nslots"] = nt.value, ns.value
     return out
+
+
+def staged_plan_host(n, row_ptr, col_idx, vals, tile_size: int, warps: int):
+    """(batches, valid) of the staged SpMV's plan for `warps` consumer warps, on the host."""
+    rp, ci, v = _np(row_ptr, np.int64), _np(col_idx, np.int32), _np(vals, np.float64)
+    nb, ok = C.c_int64(), C.c_int()
+    _check(lib().evocg_staged_plan_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), int(tile_size),
+                                        int(warps), C.byref(nb), C.byref(ok)))
+    return nb.value, bool(ok.value)
 
 
 def set_tile_precision(A: Tiles, prec_map, map_kind: int = MAP_PER_TILE, stream=None):

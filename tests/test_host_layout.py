@@ -64,3 +64,25 @@ def test_host_builder_rejects_bad_input():
     ci2[1], ci2[2] = ci2[2], ci2[1]
     with pytest.raises(evocg.EvocgError):
         evocg.tile_layout_host(n, rp, ci2, v, 16)                # columns ascending per row
+
+
+@pytest.mark.parametrize("name,m,T", list(_cases()), ids=[c[0] for c in _cases()])
+@pytest.mark.parametrize("warps", [1, 7, 2432])
+def test_staged_plan_passes_its_checks(name, m, T, warps):
+    """The staged SpMV's plan, built as the library builds it, passes the checks the library
+    applies before using it, for one warp, a few warps, and the 128^3 solve's 2432 consumer
+    warps (more warps than row blocks leaves warps without work)."""
+    n, rp, ci, v = m
+    nb, ok = evocg.staged_plan_host(n, rp, ci, v, T, warps)
+    assert ok and nb >= (1 if n > 0 else 0)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3])
+def test_staged_plan_of_the_stencil_workloads(cfg):
+    w = W.workload(cfg)
+    for warps in (1216 * 2, 152 * 4 * 4):   # the T = 32 and T = 16 kernels' consumer warps
+        nb, ok = evocg.staged_plan_host(w.n, w.rp, w.ci, w.v, w.T, warps)
+        assert ok and nb > 0
+    if cfg == 2:   # the 128^3 solve's plan: 65,294 batches of at most 16 tiles
+        nb, _ = evocg.staged_plan_host(w.n, w.rp, w.ci, w.v, w.T, 2432)
+        assert 423936 / 16 <= nb <= 423936
