@@ -143,7 +143,8 @@ int evocg_tiles_export(evocg_tiles_t A, int64_t *tileRowPtr, int32_t *tileColIdx
                        int8_t *colExp);
 
 /*
- * The tile layout of evocg_tile_build computed on the HOST only, without a GPU: the same
+ * The tile layout of evocg_tile_build (EvoCG §3.3.1 Fig. 4(a), §3.3.2, with the slot-major
+ * tile interior described there) computed on the HOST only, without a GPU: the same
  * builder, its arrays written to caller buffers (sizes as in evocg_tiles_export: tileRowPtr
  * nrb+1, tileColIdx / tileNnzOff(+1) / rowMask / tileWidth ntiles, colIdx / v64 / v32 / v16
  * nslots, colExp n), for inspecting a layout or checking it where no device is present.
@@ -160,7 +161,9 @@ int evocg_tile_layout_host(int64_t n, const int64_t *row_ptr, const int32_t *col
 
 /*
  * The staged SpMV's static work plan for a matrix, computed on the HOST only (no GPU), for
- * inspection: the same builder and planner evocg_tile_build runs, for `warps` consumer
+ * inspection. The paper has no counterpart: the plan belongs to this library's SpMV kernel
+ * (batches of tiles staged in shared memory). The same builder and planner evocg_tile_build
+ * runs, for `warps` consumer
  * warps (the library plans for its grid times the consumer warps of a block).
  *   *nbatches receives the number of batches; *valid 1 when the plan passes the checks the
  *   library applies before using it (warp ranges tiling the row blocks, batches covering

@@ -86,3 +86,10 @@ def test_staged_plan_of_the_stencil_workloads(cfg):
     if cfg == 2:   # the 128^3 solve's plan: 65,294 batches of at most 16 tiles
         nb, _ = evocg.staged_plan_host(w.n, w.rp, w.ci, w.v, w.T, 2432)
         assert 423936 / 16 <= nb <= 423936
+
+
+def test_empty_matrix():
+    z64, z32, zf = np.zeros(1, np.int64), np.zeros(0, np.int32), np.zeros(0)
+    h = evocg.tile_layout_host(0, z64, z32, zf, 16)
+    assert (h["ntiles"], h["nslots"]) == (0, 0) and list(h["tileRowPtr"]) == [0]
+    assert evocg.staged_plan_host(0, z64, z32, zf, 32, 4) == (0, True)
