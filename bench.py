@@ -45,7 +45,8 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi SM clock and throttle reasons, sampled every 200 ms in the background."""
+    """nvidia-smi SM clock and throttle reasons, sampled every 200 ms in the background; the
+    timed region starts once the first sample has arrived (at most 3 s of waiting)."""
 
     def __init__(self, index: int):
         self.index = index
@@ -62,6 +63,9 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            t0 = time.time()
+            while not self.lines and self.proc.poll() is None and time.time() - t0 < 3.0:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
