@@ -163,8 +163,7 @@ int upload_mlp(evocg_tiles *A, const evocg_ctrl *c, int *H1, int *H2)
     return EVOCG_OK;
 }
 
-int build_graph(evocg_tiles *A, CgLaunch L, int restart, cudaGraph_t *graph_out,
-                cudaGraphExec_t *exec_out)
+int build_graph(CgLaunch L, int restart, cudaGraph_t *graph_out, cudaGraphExec_t *exec_out)
 {
     cudaStream_t cs = nullptr;
     CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking), "cudaStreamCreate (capture)");
@@ -672,7 +671,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     if (use_graph && (!w.exec || w.exec_key != key)) {
         if (w.exec) { cudaGraphExecDestroy(w.exec); w.exec = nullptr; }
         if (w.graph) { cudaGraphDestroy(w.graph); w.graph = nullptr; }
-        rc = build_graph(A, L, 0, &w.graph, &w.exec);
+        rc = build_graph(L, 0, &w.graph, &w.exec);
         if (rc) return rc;
         w.exec_key = key;
     }
@@ -715,7 +714,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
             if (use_graph && (!w.exec_rs || w.exec_rs_key != rkey)) {
                 if (w.exec_rs) { cudaGraphExecDestroy(w.exec_rs); w.exec_rs = nullptr; }
                 if (w.graph_rs) { cudaGraphDestroy(w.graph_rs); w.graph_rs = nullptr; }
-                rc = build_graph(A, R, 1, &w.graph_rs, &w.exec_rs);
+                rc = build_graph(R, 1, &w.graph_rs, &w.exec_rs);
                 if (rc) return rc;
                 w.exec_rs_key = rkey;
             }
