@@ -1,0 +1,51 @@
+"""The C ABI from a plain C program: tests/c_abi_host.c is compiled with gcc as C99 against
+include/evocg.h, linked to libevocg.so, and run on the host (it calls only the entry points
+that need no GPU). Its printed results are checked against the oracle and hand counts."""
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_sparse_gb300 import build
+from mixed_precision_sparse_gb300 import workloads as W
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+@pytest.fixture(scope="module")
+def c_output():
+    lib = build.build()
+    libdir = os.path.dirname(lib)
+    os.makedirs(build.OUT_DIR, exist_ok=True)
+    exe = os.path.join(build.OUT_DIR, "c_abi_host")   # the library's own build directory
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                           "-I", os.path.join(ROOT, "include"), os.path.join(HERE, "c_abi_host.c"),
+                           "-o", exe, "-L", libdir, "-levocg", f"-Wl,-rpath,{libdir}"])
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0, out.stdout + out.stderr
+    return {ln.split()[0]: ln.split()[1:] for ln in out.stdout.splitlines()}
+
+
+def test_layout_from_c_matches_the_oracle(c_output):
+    n, rp, ci, v = W.laplace2d_5pt(20)
+    t = oracle.Tiles(oracle.CSR(n, rp, ci, v), 16)
+    got = dict(zip(c_output["layout"][0::2], map(int, c_output["layout"][1::2])))
+    assert got["ntiles"] == t.ntiles and got["nslots"] == t.nslots and got["nnz"] == t.nnz
+    assert got["tiles_in_last_rowblock"] == int(t.tileRowPtr[-1] - t.tileRowPtr[-2])
+    assert got["widest"] == int(t.tileWidth.max())
+    assert int(c_output["rows_in_masks"][0]) == sum(bin(int(m)).count("1") for m in t.rowMask)
+
+
+def test_plan_and_kstar_from_c(c_output):
+    assert c_output["plan"][2:] == ["valid", "1"] and int(c_output["plan"][1]) > 0
+    ks = c_output["kstar"]
+    assert ks[0] == "1" and ks[2] == "4"
+    assert [float(f) for f in ks[4:8]] == [0.0, 1.0, 1.0, 1.0]
+    assert oracle.kstar_select(np.array([2, 2, 2, 1, 1, 0, 0, 0], np.uint8).reshape(-1, 1))[0] == 1
+
+
+def test_error_message_reaches_c(c_output):
+    assert "tile_size" in " ".join(c_output["error"])
