@@ -160,6 +160,43 @@ int evocg_tile_layout_host(int64_t n, const int64_t *row_ptr, const int32_t *col
                            float *v32, uint16_t *v16, int8_t *colExp);
 
 /*
+ * The Tile-CSC layout of EvoCG §3.3.1 Fig. 4(a) and §3.3.2 Fig. 4(b), written from this
+ * library's tile builder on the HOST (no GPU): the inter-tile CSR over row blocks
+ * (tileRowPtr nrb+1, tileColIdx ntiles: tiles of a row block in ascending column block) and
+ * inside every tile a CSC. Tile t's entries start at tileNnzOff[t] (ntiles+1 entries) in the
+ * padded streams; colPtr[t*(T+1) + c] .. colPtr[t*(T+1) + c + 1] is the range of local column
+ * c relative to that start (colPtr: ntiles x (T+1), uint16); a column's entries are in
+ * ascending row and rowIdx (nnz_p bytes) holds each entry's row relative to the row block's
+ * first row. With pad = 2 (the paper's padding of every column to a multiple of two) a
+ * column with an odd number of entries ends with one sentinel-marked zero: rowIdx = T (the
+ * row index "R" of Fig. 4(b)) and +0 in the three value streams; pad = 1 stores no sentinel.
+ * v64 / v32 / v16 (nnz_p each): a_ij, and a_ij / s_j rounded once to FP32 / BF16 (s_j =
+ * 2^colExp[j], colExp: n bytes), the same bits the SpMV reads.
+ *   n, row_ptr, col_idx, vals, tile_size: as evocg_tile_build (HOST arrays).
+ *   ntiles, nnz_p: receive the sizes (either may be NULL). Every array pointer may be NULL; a
+ *   call with all of them NULL only sizes the layout.
+ * Errors: as evocg_tile_build; EINVAL for pad other than 1 or 2. No device is touched.
+ */
+int evocg_tile_csc_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                        const double *vals, int tile_size, int pad, int64_t *ntiles,
+                        int64_t *nnz_p, int64_t *tileRowPtr, int32_t *tileColIdx,
+                        int64_t *tileNnzOff, uint16_t *colPtr, uint8_t *rowIdx, double *v64,
+                        float *v32, uint16_t *v16, int8_t *colExp);
+
+/*
+ * The same Tile-CSC arrays as evocg_tile_csc_host, written from the DEVICE-resident
+ * structure of a handle: the arrays the SpMV kernels read are copied back and rewritten as
+ * Tile-CSC on the host, so a bit-exact comparison checks what the GPU computes with. Sizes
+ * as in evocg_tile_csc_host (ntiles from evocg_tiles_info); *nnz_p receives the padded
+ * length (may be NULL); every array pointer may be NULL. Synchronises the device.
+ * Errors: EINVAL (NULL handle, pad other than 1 or 2), ENOMEM, ECUDA.
+ */
+int evocg_tiles_export_csc(evocg_tiles_t A, int pad, int64_t *nnz_p, int64_t *tileRowPtr,
+                           int32_t *tileColIdx, int64_t *tileNnzOff, uint16_t *colPtr,
+                           uint8_t *rowIdx, double *v64, float *v32, uint16_t *v16,
+                           int8_t *colExp);
+
+/*
  * The staged SpMV's static work plan for a matrix, computed on the HOST only (no GPU), for
  * inspection. The paper has no counterpart: the plan belongs to this library's SpMV kernel
  * (batches of tiles staged in shared memory). The same builder and planner evocg_tile_build
@@ -207,7 +244,7 @@ enum {
     EVOCG_SPMV_DIRECT = 2,        /* run the direct kernel: a warp per row block, every operand
                                      loaded by the lanes from global memory, one tile after
                                      the other */
-    EVOCG_SPMV_STAGED = 4         /* run the staged kernel (the default where it can run): a
+    EVOCG_SPMV_STAGED = 4,        /* run the staged kernel (the default where it can run): a
                                      producer warp copies each tile's value slice and x segment
                                      into shared memory by bulk asynchronous copies for two
                                      consumer warps (needs 16-byte aligned x; the direct kernel
@@ -215,7 +252,13 @@ enum {
                                      column with the same arithmetic; for tiles of 32 and 64
                                      they give the same bits; for tiles of 16 the direct kernel
                                      splits a row block's tiles over two half-warps (same sums
-                                     to rounding). At most one of DIRECT, STAGED may be set */
+                                     to rounding). At most one of DIRECT, STAGED, PANEL may be
+                                     set */
+    EVOCG_SPMV_PANEL = 8          /* run the panel kernel (tiles of 16 or 32): a warp streams the
+                                     tile descriptors of consecutive row blocks and keeps several
+                                     tiles' loads in flight; single-entry tiles take one lane
+                                     each. Low-precision products are summed in FP32 pairs and
+                                     folded into the FP64 row sum once per row */
 };
 
 /*

@@ -347,6 +347,28 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
             }
         }
     }
+    // panel SpMV plan (tiles of 16 or 32)
+    if (e == cudaSuccess && H.nrb > 0) {
+        int variant = 0;
+        if (const char *v = std::getenv("EVOCG_PANEL_VARIANT")) variant = std::atoi(v);
+        if (variant < 0 || variant >= kPanelVariants) variant = 0;
+        const int pg = panel_grid_for(H.T, sms, variant);
+        if (pg > 0) {
+            std::vector<uint4> pd;
+            std::vector<int64_t> wrec;
+            std::vector<int32_t> wpan;
+            std::string why;
+            const int64_t warps = (int64_t)pg * (kPanelThreads / 32);
+            if (panel_plan(H, warps, &pd, &wrec, &wpan, &why) &&
+                panel_plan_ok(H, warps, pd, wrec, wpan, &why)) {
+                A->panel_variant = variant;
+                up(&A->pdesc, pd.data(), (int64_t)pd.size());
+                up(&A->warpRec, wrec.data(), (int64_t)wrec.size());
+                up(&A->warpPanel, wpan.data(), (int64_t)wpan.size());
+                A->panel_grid = pg;
+            }
+        }
+    }
     if (e == cudaSuccess) e = dalloc(&A->errw, 1);
     if (e == cudaSuccess) e = cudaMemset(A->errw, 0, sizeof(int));
     H.release();
@@ -367,8 +389,10 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     // direct one; EVOCG_SPMV_KERNEL=direct selects the direct kernel for every SpMV of the
     // matrices built afterwards.
     A->spmv_kind = SPMV_KIND_AUTO;
-    if (const char *k = std::getenv("EVOCG_SPMV_KERNEL"))
+    if (const char *k = std::getenv("EVOCG_SPMV_KERNEL")) {
         if (!std::strcmp(k, "direct")) A->spmv_kind = SPMV_KIND_DIRECT;
+        if (!std::strcmp(k, "panel")) A->spmv_kind = SPMV_KIND_PANEL;
+    }
     A->vec_grid = sms * 4 > kMaxBlocks ? kMaxBlocks : sms * 4;
     *out = A;
     return EVOCG_OK;
@@ -381,7 +405,7 @@ extern "C" int evocg_tiles_free(evocg_tiles_t A)
     release_ws(A->ws);
     dfree(A->tileRowPtr); dfree(A->tileColIdx); dfree(A->tileNnzOff); dfree(A->tileRowIdx);
     dfree(A->rowMask); dfree(A->tileWidth); dfree(A->warpRb); dfree(A->warpBatch); dfree(A->batchTile);
-    dfree(A->tileSlot); dfree(A->errw);
+    dfree(A->tileSlot); dfree(A->errw); dfree(A->pdesc); dfree(A->warpRec); dfree(A->warpPanel);
     dfree(A->colIdx); dfree(A->v64); dfree(A->v32); dfree(A->v16); dfree(A->colExp);
     dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16f);
     dfree(A->xstage); dfree(A->ystage);
@@ -485,8 +509,8 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
 {
     g_err.clear();
     if (!A || (A->n > 0 && (!x || !y))) return fail(EVOCG_EINVAL, "NULL argument");
-    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED);
-    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED))
+    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED | EVOCG_SPMV_PANEL);
+    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED | EVOCG_SPMV_PANEL))
         return fail(EVOCG_EINVAL, "unknown flags");
     if (kflags & (kflags - 1)) return fail(EVOCG_EINVAL, "at most one kernel flag");
     if (A->n == 0) return EVOCG_OK;
@@ -520,7 +544,7 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     S.map_kind = A->map_kind;
     S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
     S.direct = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
-    S.kind = (flags & EVOCG_SPMV_STAGED) ? SPMV_KIND_STAGED : 0;
+    S.kind = (flags & EVOCG_SPMV_STAGED) ? SPMV_KIND_STAGED : (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : 0;
     CK(launch_spmv(S, s), "launch spmv");
     if (!ydev) {
         int lost = 0;

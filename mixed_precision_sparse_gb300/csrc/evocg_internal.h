@@ -20,6 +20,8 @@ constexpr int kSpmvMinBlocks = 4;     // resident blocks per SM the SpMV registe
 constexpr int kMlpHiddenMax = 64;
 constexpr int kStages = 5;            // tile slots per warp in the SpMV's shared-memory ring
 constexpr int kSlack = 16;            // bytes past the end of every staged array
+constexpr int kPanelThreads = 128;    // threads per block of the panel SpMV
+constexpr int kPanelVariants = 4;     // (tiles issued together, blocks per SM) variants built
 
 // Device-resident solver state; one per handle. Written by the last block of each
 // reducing kernel, read by every block of the next kernel.
@@ -71,11 +73,18 @@ struct TilesView {
     int staged_grid;
     int *err;
     int spmv_kind;     // kernel launch_spmv runs by default (SPMV_KIND_*)
+    // panel SpMV: descriptor stream, first record and first panel of every warp (warps + 1
+    // entries each), and the grid the plan was made for (0: no plan)
+    const uint4 *pdesc;
+    const int64_t *warpRec;
+    const int32_t *warpPanel;
+    int panel_grid;
+    int panel_variant;
 };
 
 // SpMV kernels: the direct kernel (warp per row block, global loads) and the staged kernel
 // (operands in shared memory by bulk asynchronous copies). AUTO: staged when it can run.
-enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_STAGED = 2 };
+enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_STAGED = 2, SPMV_KIND_PANEL = 3 };
 
 constexpr uint16_t kDirectSlot = 0xFFFF;
 
@@ -145,6 +154,11 @@ struct evocg_tiles {
     uint16_t *tileSlot = nullptr;
     int64_t nbatches = 0;
     int staged_grid = 0;
+    uint4 *pdesc = nullptr;        // panel SpMV plan (see TilesView)
+    int64_t *warpRec = nullptr;
+    int32_t *warpPanel = nullptr;
+    int panel_grid = 0;
+    int panel_variant = 0;
     int *errw = nullptr;           // device error word (a lost stage wait)
     int spmv_kind = 0;             // default SpMV kernel (SPMV_KIND_*)
     uint8_t *tilePrec = nullptr;   // per-tile map
@@ -165,7 +179,7 @@ struct evocg_tiles {
         return evocg::TilesView{n, nrb, ntiles, nslots, T, tileRowPtr, tileColIdx, tileNnzOff,
                                 tileRowIdx, rowMask, tileWidth, colIdx, v64, v32, v16, colExp,
                                 warpRb, warpBatch, batchTile, tileSlot, staged_grid, errw,
-                                spmv_kind};
+                                spmv_kind, pdesc, warpRec, warpPanel, panel_grid, panel_variant};
     }
 };
 
@@ -226,6 +240,13 @@ cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
 cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s);
 int spmv_dot_partials(const SpmvLaunch &L);   // warps that write a p.q partial
 cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s);
+cudaError_t launch_spmv_panel(const SpmvLaunch &L, cudaStream_t s);
+int panel_grid_for(int T, int sms, int variant);   // 0 if no panel kernel exists for T
+bool panel_plan(const HostTiles &H, int64_t warps, std::vector<uint4> *desc,
+                std::vector<int64_t> *warpRec, std::vector<int32_t> *warpPanel, std::string *why);
+bool panel_plan_ok(const HostTiles &H, int64_t warps, const std::vector<uint4> &desc,
+                   const std::vector<int64_t> &warpRec, const std::vector<int32_t> &warpPanel,
+                   std::string *why);
 
 int staged_grid_for(int T, int sms);   // 0 if it cannot run
 int staged_warps_per_block(int T);      // consumer warps (the ones with rows) per block

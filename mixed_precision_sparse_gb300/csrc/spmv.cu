@@ -196,6 +196,7 @@ static int chosen_kind(const SpmvLaunch &L)
 {
     if (L.direct) return SPMV_KIND_DIRECT;
     const int k = L.kind ? L.kind : L.A.spmv_kind;
+    if (k == SPMV_KIND_PANEL && L.A.pdesc && L.A.panel_grid > 0) return SPMV_KIND_PANEL;
     if (k == SPMV_KIND_STAGED || k == SPMV_KIND_AUTO) {
         const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
         if (L.A.warpRb && L.A.staged_grid > 0 && al(L.x64) && (L.force64 || (al(L.x32) && al(L.x16f))))
@@ -208,6 +209,7 @@ int spmv_dot_partials(const SpmvLaunch &L)
 {
     switch (chosen_kind(L)) {
     case SPMV_KIND_STAGED: return L.A.staged_grid * staged_warps_per_block(L.A.T);
+    case SPMV_KIND_PANEL: return L.A.panel_grid * (kPanelThreads / 32);
     default: return L.grid * (kSpmvThreads / 32);
     }
 }
@@ -219,6 +221,8 @@ cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
     case SPMV_KIND_STAGED:
         S.grid = L.A.staged_grid;
         return launch_spmv_staged(S, s);
+    case SPMV_KIND_PANEL:
+        return launch_spmv_panel(S, s);
     default:
         return launch_spmv_direct(L, s);
     }

@@ -112,6 +112,9 @@ def lib():
                                            C.POINTER(C.c_int64)] + [P] * 10,
                 "evocg_staged_plan_host": [i64, P, P, P, i32, i64, C.POINTER(C.c_int64),
                                            C.POINTER(C.c_int)],
+                "evocg_tile_csc_host": [i64, P, P, P, i32, i32, C.POINTER(C.c_int64),
+                                        C.POINTER(C.c_int64)] + [P] * 9,
+                "evocg_tiles_export_csc": [P, i32, C.POINTER(C.c_int64)] + [P] * 9,
                 "evocg_version": [],
             }
             for name, args in sig.items():
@@ -212,6 +215,44 @@ class Tiles:
         ex = self.export()
         return np.repeat(np.arange(self.nrb, dtype=np.int64), np.diff(ex["tileRowPtr"])), ex
 
+    def export_csc(self, pad: int = 1) -> dict:
+        """The device-resident structure rewritten as EvoCG's Tile-CSC (evocg_tiles_export_csc)."""
+        nzp = C.c_int64()
+        _check(lib().evocg_tiles_export_csc(self.h, int(pad), C.byref(nzp), *[None] * 9))
+        out = _csc_arrays(self.n, self.T, self.ntiles, nzp.value)
+        _check(lib().evocg_tiles_export_csc(self.h, int(pad), None, *[_ptr(out[k]) for k in _CSC_KEYS]))
+        out["ntiles"], out["nnz_p"] = self.ntiles, nzp.value
+        return out
+
+
+_CSC_KEYS = ["tileRowPtr", "tileColIdx", "tileNnzOff", "colPtr", "rowIdx", "v64", "v32", "v16",
+             "colExp"]
+
+
+def _csc_arrays(n, T, ntiles, nnz_p):
+    nrb = (int(n) + T - 1) // T
+    return dict(tileRowPtr=np.empty(nrb + 1, np.int64), tileColIdx=np.empty(ntiles, np.int32),
+                tileNnzOff=np.empty(ntiles + 1, np.int64),
+                colPtr=np.empty((ntiles, T + 1), np.uint16), rowIdx=np.empty(nnz_p, np.uint8),
+                v64=np.empty(nnz_p, np.float64), v32=np.empty(nnz_p, np.float32),
+                v16=np.empty(nnz_p, np.uint16), colExp=np.empty(int(n), np.int8))
+
+
+def tile_csc_host(n, row_ptr, col_idx, vals, tile_size: int, pad: int = 1) -> dict:
+    """EvoCG's Tile-CSC written by the library's builder on the host (no GPU): a dict of
+    tileRowPtr, tileColIdx, tileNnzOff, colPtr (ntiles x (T+1)), rowIdx, v64, v32, v16,
+    colExp, plus ntiles and nnz_p."""
+    rp, ci, v = _np(row_ptr, np.int64), _np(col_idx, np.int32), _np(vals, np.float64)
+    nt, nzp = C.c_int64(), C.c_int64()
+    T = int(tile_size)
+    _check(lib().evocg_tile_csc_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), T, int(pad),
+                                     C.byref(nt), C.byref(nzp), *[None] * 9))
+    out = _csc_arrays(n, T, nt.value, nzp.value)
+    _check(lib().evocg_tile_csc_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), T, int(pad), None, None,
+                                     *[_ptr(out[k]) for k in _CSC_KEYS]))
+    out["ntiles"], out["nnz_p"] = nt.value, nzp.value
+    return out
+
 
 def tile_build(n, row_ptr, col_idx, vals, tile_size: int) -> Tiles:
     rp, ci, v = _np(row_ptr, np.int64), _np(col_idx, np.int32), _np(vals, np.float64)
@@ -268,6 +309,7 @@ def get_tile_precision(A: Tiles, stream=None):
 SPMV_REUSE_XCOPIES = 1
 SPMV_DIRECT = 2
 SPMV_STAGED = 4
+SPMV_PANEL = 8
 
 
 def spmv(A: Tiles, x, y, stream=None):

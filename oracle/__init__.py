@@ -54,10 +54,10 @@ def _load():
             lib.ora_csr_check.argtypes = [i64, P, P, P]
             lib.ora_csr_check.restype = i32
             lib.ora_col_exp.argtypes = [i64, P, P, P, P]
-            lib.ora_tile_count.argtypes = [i64, P, P, i32, P, P, P]
-            lib.ora_tile_count.restype = i32
-            lib.ora_tile_build.argtypes = [i64, P, P, P, i32] + [P] * 10
-            lib.ora_tile_build.restype = i32
+            lib.ora_tile_csc_count.argtypes = [i64, P, P, i32, i32, P, P, P]
+            lib.ora_tile_csc_count.restype = i32
+            lib.ora_tile_csc_build.argtypes = [i64, P, P, P, i32, i32] + [P] * 9
+            lib.ora_tile_csc_build.restype = i32
             lib.ora_kstar_select.argtypes = [P, i64, i64, C.c_double, P, P, i32]
             lib.ora_kstar_select.restype = i32
             lib.ora_mixed_spmv.argtypes = [i64, P, P, P, i32, P, P, P, P, P, P]
@@ -129,42 +129,41 @@ def col_exp(A: CSR):
 
 
 class Tiles:
-    """The oracle's own tile layout (arrays named as in the GPU library's export).
+    """The Tile-CSC layout of EvoCG §3.3 (Fig. 4): CSR over row blocks of T x T tiles
+    (tileRowPtr, tileColIdx), and inside every tile a CSC: colPtr[t] (T + 1 offsets from
+    the tile's first entry tileNnzOff[t]), rowIdx (row within the row block; T is the
+    sentinel of a pad), and the FP64 / FP32 / BF16 value streams over the same entries.
+    pad = 2 pads every column to even length as the paper does; pad = 1 stores no pads."""
 
-    Inside tile t: rowMask[t] marks its nonempty local rows, tileWidth[t] = w is its
-    longest row, and slot (k, j) at tileNnzOff[t] + k*h + j (h = nonempty rows) holds
-    the k-th entry of the j-th nonempty row or a pad (local column T, value +0)."""
-
-    def __init__(self, A: CSR, T: int):
+    def __init__(self, A: CSR, T: int, pad: int = 1):
         lib = _load()
-        nt, nz, ns = C.c_int64(), C.c_int64(), C.c_int64()
-        st = lib.ora_tile_count(A.n, _p(A.rp), _p(A.ci), int(T), C.byref(nt), C.byref(nz),
-                                C.byref(ns))
+        nt, nz, nzp = C.c_int64(), C.c_int64(), C.c_int64()
+        st = lib.ora_tile_csc_count(A.n, _p(A.rp), _p(A.ci), int(T), int(pad), C.byref(nt),
+                                    C.byref(nz), C.byref(nzp))
         if st != OK:
             raise ValueError(f"tile count failed: status {st}")
-        self.n, self.T = A.n, int(T)
+        self.n, self.T, self.pad = A.n, int(T), int(pad)
         self.nrb = (A.n + T - 1) // T
-        self.ntiles, self.nnz, self.nslots = nt.value, nz.value, ns.value
+        self.ntiles, self.nnz, self.nnz_p = nt.value, nz.value, nzp.value
         self.tileRowPtr = np.empty(self.nrb + 1, np.int64)
         self.tileColIdx = np.empty(max(self.ntiles, 1), np.int32)
         self.tileNnzOff = np.empty(self.ntiles + 1, np.int64)
-        self.rowMask = np.empty(max(self.ntiles, 1), np.uint64)
-        self.tileWidth = np.empty(max(self.ntiles, 1), np.uint8)
-        self.colIdx = np.empty(max(self.nslots, 1), np.uint8)
-        self.v64 = np.empty(max(self.nslots, 1), np.float64)
-        self.v32 = np.empty(max(self.nslots, 1), np.float32)
-        self.v16 = np.empty(max(self.nslots, 1), np.uint16)
+        self.colPtr = np.empty((max(self.ntiles, 1), T + 1), np.uint16)
+        self.rowIdx = np.empty(max(self.nnz_p, 1), np.uint8)
+        self.v64 = np.empty(max(self.nnz_p, 1), np.float64)
+        self.v32 = np.empty(max(self.nnz_p, 1), np.float32)
+        self.v16 = np.empty(max(self.nnz_p, 1), np.uint16)
         self.colExp = np.empty(max(A.n, 1), np.int8)
-        st = lib.ora_tile_build(A.n, _p(A.rp), _p(A.ci), _p(A.v), int(T), _p(self.tileRowPtr),
-                                _p(self.tileColIdx), _p(self.tileNnzOff), _p(self.rowMask),
-                                _p(self.tileWidth), _p(self.colIdx), _p(self.v64), _p(self.v32),
-                                _p(self.v16), _p(self.colExp))
+        st = lib.ora_tile_csc_build(A.n, _p(A.rp), _p(A.ci), _p(A.v), int(T), int(pad),
+                                    _p(self.tileRowPtr), _p(self.tileColIdx), _p(self.tileNnzOff),
+                                    _p(self.colPtr), _p(self.rowIdx), _p(self.v64), _p(self.v32),
+                                    _p(self.v16), _p(self.colExp))
         if st != OK:
             raise ValueError(f"tile build failed: status {st}")
         self.tileColIdx = self.tileColIdx[: self.ntiles]
-        self.rowMask, self.tileWidth = self.rowMask[: self.ntiles], self.tileWidth[: self.ntiles]
-        self.colIdx, self.v64 = self.colIdx[: self.nslots], self.v64[: self.nslots]
-        self.v32, self.v16 = self.v32[: self.nslots], self.v16[: self.nslots]
+        self.colPtr = self.colPtr[: self.ntiles]
+        self.rowIdx, self.v64 = self.rowIdx[: self.nnz_p], self.v64[: self.nnz_p]
+        self.v32, self.v16 = self.v32[: self.nnz_p], self.v16[: self.nnz_p]
         self.colExp = self.colExp[: A.n]
 
     def tile_rows(self):
@@ -172,17 +171,17 @@ class Tiles:
         return np.repeat(np.arange(self.nrb, dtype=np.int64), np.diff(self.tileRowPtr))
 
     def tile_entries(self):
-        """Stored entries (slots that are not pads) of every tile."""
-        real = (self.colIdx < self.T).astype(np.int64)
+        """Stored entries (not sentinels) of every tile."""
+        real = (self.rowIdx < self.T).astype(np.int64)
         c = np.concatenate([[0], np.cumsum(real)])
         return c[self.tileNnzOff[1:]] - c[self.tileNnzOff[:-1]]
 
-    def slots(self, t):
-        """(local row, slot index) of every slot of tile t, slot order."""
-        m = int(self.rowMask[t])
-        rows = [r for r in range(self.T) if (m >> r) & 1]
-        h, w, off = len(rows), int(self.tileWidth[t]), int(self.tileNnzOff[t])
-        return [(rows[j], off + k * h + j) for k in range(w) for j in range(h)]
+    def entries(self, t):
+        """(local row, local column, stream index) of every entry of tile t in storage
+        order, sentinels included (local row T)."""
+        off, cp = int(self.tileNnzOff[t]), self.colPtr[t]
+        return [(int(self.rowIdx[off + e]), c, off + e)
+                for c in range(self.T) for e in range(int(cp[c]), int(cp[c + 1]))]
 
     def to_csr(self) -> CSR:
         """Rebuild CSR (FP64 stream) from the layout: the round-trip check."""
@@ -190,11 +189,11 @@ class Tiles:
         rows, cols, vals = [], [], []
         trow = self.tile_rows()
         for t in range(self.ntiles):
-            for r, s in self.slots(t):
-                if self.colIdx[s] == T:
+            for r, c, s in self.entries(t):
+                if r == T:
                     continue
                 rows.append(trow[t] * T + r)
-                cols.append(int(self.tileColIdx[t]) * T + int(self.colIdx[s]))
+                cols.append(int(self.tileColIdx[t]) * T + c)
                 vals.append(self.v64[s])
         rows, cols, vals = np.array(rows, np.int64), np.array(cols, np.int64), np.array(vals)
         order = np.lexsort((cols, rows))

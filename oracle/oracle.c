@@ -24,11 +24,13 @@
  *  - A low-precision tile multiplies RN(a_ij / s_j) by RN(x_j) (the x entry rounded
  *    to the tile's own format) and scales the product by s_j. Both factors have at
  *    most 24 significant bits, so the FP64 product is exact.
- *  - Intra-tile order is slot-major over the tile's nonempty rows: a row mask
- *    names them, the tile is padded to a w x h rectangle (w = its longest row,
- *    h = its nonempty rows) and slot (k, j) holds the k-th entry of the j-th
- *    nonempty row, so that one lane per row reads consecutive slots. The
- *    inter-tile level is CSR over row blocks as in EvoCG Fig. 4(a).
+ *  - Tiles are square, T x T (R = C = T), as the workloads fix them. Inside a tile the
+ *    layout is EvoCG's CSC (§3.3.2, Fig. 4(b)): colPtr of length T+1 relative to the
+ *    tile's first entry, rowIdx relative to the row block's first row, entries of a
+ *    column in ascending row. Padding of a column to even length with the sentinel
+ *    row index T ("R" in Fig. 4(b)) and zero values is a build parameter, pad = 2
+ *    (the paper) or pad = 1 (no padding). The N/C entries of Fig. 4(a) are read as
+ *    placeholders: there is no padding of the tile list.
  *  - The reuse interval K* (EvoCG §3.4) is the largest of 1, 2, 4, ... for which fewer than
  *    10% of the upward transitions in a per-iteration decision log would be delayed, a
  *    transition at iteration k being delayed when the decision of iteration K*floor(k/K)
@@ -154,132 +156,149 @@ void ora_col_exp(int64_t n, const int64_t *rp, const int32_t *ci, const double *
 }
 
 /* ------------------------------------------------------------------------ */
-/* Tile layout (EvoCG §3.3.1 and Fig. 4(a): CSR over row blocks of tiles;    */
-/* §3.3.2: three value streams over one set of indices).                     */
+/* Tile-CSC layout (EvoCG §3.3.1 and Fig. 4(a): CSR over row blocks of       */
+/* tiles; §3.3.2 and Fig. 4(b): each tile stored as CSC, three value streams */
+/* over one set of indices, columns padded to even length with a sentinel    */
+/* row index).                                                               */
 /* ------------------------------------------------------------------------ */
 
-/* Entries of local row r of row block rb that fall in column block cb: the
- * half-open CSR range [*k0, *k1). cur[r] is where the row's scan stands. */
-static void row_range_in_block(const int64_t *rp, const int32_t *ci, int64_t row,
-                               int64_t cur, int64_t cb, int T, int64_t *k0, int64_t *k1)
+/* One stored entry of a row block: its global column, its row within the block, and
+ * its index in the CSR arrays. */
+typedef struct {
+    int32_t col;
+    int32_t lrow;
+    int64_t k;
+} ora_entry;
+
+/* Column-major order inside a row block: by column, then by row. */
+static int entry_col_row(const void *a, const void *b)
 {
-    int64_t k = cur;
-    *k0 = k;
-    while (k < rp[row + 1] && ci[k] / T == cb) k++;
-    *k1 = k;
+    const ora_entry *x = (const ora_entry *)a, *y = (const ora_entry *)b;
+    if (x->col != y->col) return x->col < y->col ? -1 : 1;
+    return (x->lrow > y->lrow) - (x->lrow < y->lrow);
 }
 
-/* Smallest column block still unvisited among the rows of a row block, or -1. */
-static int64_t next_col_block(const int64_t *rp, const int32_t *ci, int64_t r0, int64_t nr,
-                              const int64_t *cur, int T)
+/* The entries of row block rb (rows rb*T .. rb*T + T - 1), sorted column-major into
+ * buf; returns how many there are. */
+static int64_t row_block_entries(int64_t n, const int64_t *rp, const int32_t *ci, int T,
+                                 int64_t rb, ora_entry *buf)
 {
-    int64_t cbmin = -1;
-    for (int64_t r = 0; r < nr; ++r)
-        if (cur[r] < rp[r0 + r + 1]) {
-            int64_t cb = ci[cur[r]] / T;
-            if (cbmin < 0 || cb < cbmin) cbmin = cb;
+    int64_t r0 = rb * T, r1 = (r0 + T < n) ? r0 + T : n, m = 0;
+    for (int64_t i = r0; i < r1; ++i)
+        for (int64_t k = rp[i]; k < rp[i + 1]; ++k) {
+            buf[m].col = ci[k];
+            buf[m].lrow = (int32_t)(i - r0);
+            buf[m].k = k;
+            m++;
         }
-    return cbmin;
+    qsort(buf, (size_t)m, sizeof(ora_entry), entry_col_row);
+    return m;
 }
 
-/* Count the nonempty T x T tiles, the stored entries and the slots of the layout
- * below (entries plus the padding that makes every tile a w x h rectangle). */
-int ora_tile_count(int64_t n, const int64_t *rp, const int32_t *ci, int T,
-                   int64_t *ntiles_out, int64_t *nnz_out, int64_t *nslots_out)
+/* Largest number of entries of one row block (the size of the sort buffer). */
+static int64_t max_row_block_entries(int64_t n, const int64_t *rp, int T)
 {
-    if (T < 1 || T > 64 || n < 0) return ORA_EINVAL;
-    int64_t nrb = (n + T - 1) / T, ntiles = 0, nslots = 0;
-    int64_t cur[64];
+    int64_t best = 0;
+    for (int64_t r0 = 0; r0 < n; r0 += T) {
+        int64_t r1 = (r0 + T < n) ? r0 + T : n;
+        if (rp[r1] - rp[r0] > best) best = rp[r1] - rp[r0];
+    }
+    return best;
+}
+
+/* Entries a column of c stored entries occupies: c, rounded up to a multiple of pad
+ * (pad = 2 is the paper's padding to a multiple of two; pad = 1 stores no padding). */
+static int64_t padded(int64_t c, int pad) { return (c + pad - 1) / pad * pad; }
+
+/* Count the nonempty T x T tiles, the stored entries, and the entries of the padded
+ * streams (stored entries plus sentinels). */
+int ora_tile_csc_count(int64_t n, const int64_t *rp, const int32_t *ci, int T, int pad,
+                       int64_t *ntiles_out, int64_t *nnz_out, int64_t *nnzp_out)
+{
+    if (T < 1 || T > 64 || n < 0 || (pad != 1 && pad != 2)) return ORA_EINVAL;
+    int64_t nrb = (n + T - 1) / T, ntiles = 0, nnzp = 0;
+    ora_entry *buf = (ora_entry *)malloc(sizeof(ora_entry) * (size_t)(max_row_block_entries(n, rp, T) + 1));
+    if (!buf) return ORA_ENOMEM;
     for (int64_t rb = 0; rb < nrb; ++rb) {
-        int64_t r0 = rb * T, nr = (n - r0 < T) ? n - r0 : T;
-        for (int64_t r = 0; r < nr; ++r) cur[r] = rp[r0 + r];
-        for (;;) {
-            int64_t cb = next_col_block(rp, ci, r0, nr, cur, T);
-            if (cb < 0) break;
-            int64_t h = 0, w = 0;
-            for (int64_t r = 0; r < nr; ++r) {
-                int64_t k0, k1;
-                row_range_in_block(rp, ci, r0 + r, cur[r], cb, T, &k0, &k1);
-                if (k1 > k0) h++;
-                if (k1 - k0 > w) w = k1 - k0;
-                cur[r] = k1;
-            }
-            nslots += w * h;
+        int64_t m = row_block_entries(n, rp, ci, T, rb, buf);
+        for (int64_t e = 0; e < m;) {
+            int64_t cb = buf[e].col / T;
             ntiles++;
+            while (e < m && buf[e].col / T == cb) {      /* the columns of tile (rb, cb) */
+                int64_t c0 = e;
+                while (e < m && buf[e].col == buf[c0].col) e++;
+                nnzp += padded(e - c0, pad);
+            }
         }
     }
+    free(buf);
     *ntiles_out = ntiles;
     *nnz_out = (n > 0) ? rp[n] : 0;
-    *nslots_out = nslots;
+    *nnzp_out = nnzp;
     return ORA_OK;
 }
 
-/* Fill the layout. Inter-tile level (EvoCG Fig. 4(a)): CSR over row blocks, the
- * tiles of a row block in ascending column block. Inside a tile:
- *   rowMask[t]  bit r set when local row r has at least one entry in the tile;
- *   tileWidth[t] w = the largest number of entries of one local row in the tile;
- *   the tile's h = popcount(rowMask[t]) nonempty rows, ascending, are numbered
- *   j = 0..h-1, and slot (k, j), k = 0..w-1, sits at tileNnzOff[t] + k*h + j: it
- *   holds the k-th entry (ascending column) of row j, or, when that row has k or
- *   fewer entries, a pad: local column T (one past the last column, like the
- *   sentinel row index of EvoCG Fig. 4(b)) and value +0 in all three streams.
- * tileNnzOff counts slots; colIdx and the value streams have one element per slot. */
-int ora_tile_build(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int T,
-                   int64_t *tileRowPtr, int32_t *tileColIdx, int64_t *tileNnzOff,
-                   uint64_t *rowMask, uint8_t *tileWidth, uint8_t *colIdx, double *v64,
-                   float *v32, uint16_t *v16, int8_t *colExp)
+/* Fill the Tile-CSC layout.
+ * Inter-tile level (EvoCG §3.3.1, Fig. 4(a)): row block rb holds tiles
+ * tileRowPtr[rb] .. tileRowPtr[rb+1]-1, listed in ascending column block tileColIdx.
+ * Intra-tile level (EvoCG §3.3.2, Fig. 4(b)): tile t's entries start at tileNnzOff[t] in
+ * the padded streams (tileNnzOff has ntiles+1 entries); colPtr[t*(T+1) + c] .. [c+1] is
+ * the range of local column c relative to that start (colPtr[t*(T+1)] = 0); inside a
+ * column the entries are in ascending row and rowIdx holds each entry's row relative to
+ * the row block's first row. With pad = 2 a column with an odd count gets one more
+ * entry: rowIdx = T (the sentinel row index R of Fig. 4(b), one past the last row) and
+ * +0 in all three value streams. v64 holds a_ij; v32 and v16 hold a_ij / s_j rounded
+ * once to FP32 / BF16, with s_j = 2^colExp[j]. */
+int ora_tile_csc_build(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int T,
+                       int pad, int64_t *tileRowPtr, int32_t *tileColIdx, int64_t *tileNnzOff,
+                       uint16_t *colPtr, uint8_t *rowIdx, double *v64, float *v32, uint16_t *v16,
+                       int8_t *colExp)
 {
-    if (T < 1 || T > 64 || n < 0) return ORA_EINVAL;
+    if (T < 1 || T > 64 || n < 0 || (pad != 1 && pad != 2)) return ORA_EINVAL;
     ora_col_exp(n, rp, ci, v, colExp);
     int64_t nrb = (n + T - 1) / T, t = 0, pos = 0;
-    int64_t cur[64], k0[64], k1[64];
+    ora_entry *buf = (ora_entry *)malloc(sizeof(ora_entry) * (size_t)(max_row_block_entries(n, rp, T) + 1));
+    if (!buf) return ORA_ENOMEM;
     tileRowPtr[0] = 0;
     for (int64_t rb = 0; rb < nrb; ++rb) {
-        int64_t r0 = rb * T, nr = (n - r0 < T) ? n - r0 : T;
-        for (int64_t r = 0; r < nr; ++r) cur[r] = rp[r0 + r];
-        for (;;) {
-            int64_t cb = next_col_block(rp, ci, r0, nr, cur, T);
-            if (cb < 0) break;
-            uint64_t mask = 0;
-            int64_t h = 0, w = 0;
-            for (int64_t r = 0; r < nr; ++r) {
-                row_range_in_block(rp, ci, r0 + r, cur[r], cb, T, &k0[r], &k1[r]);
-                if (k1[r] > k0[r]) { mask |= (uint64_t)1 << r; h++; }
-                if (k1[r] - k0[r] > w) w = k1[r] - k0[r];
-                cur[r] = k1[r];
-            }
+        int64_t m = row_block_entries(n, rp, ci, T, rb, buf);
+        for (int64_t e = 0; e < m;) {
+            int64_t cb = buf[e].col / T;
+            uint16_t *cp = colPtr + t * (T + 1);
             tileColIdx[t] = (int32_t)cb;
             tileNnzOff[t] = pos;
-            rowMask[t] = mask;
-            tileWidth[t] = (uint8_t)w;
-            for (int64_t kk = 0; kk < w; ++kk) {
-                int64_t j = 0;
-                for (int64_t r = 0; r < nr; ++r) {
-                    if (!((mask >> r) & 1)) continue;
-                    int64_t slot = pos + kk * h + j;
-                    if (k0[r] + kk < k1[r]) {
-                        int64_t k = k0[r] + kk;
-                        int c = ci[k];
-                        int ec = colExp[c];
-                        colIdx[slot] = (uint8_t)(c - cb * T);
-                        v64[slot] = v[k];
-                        v32[slot] = f32_of(ldexp(v[k], -ec));
-                        v16[slot] = bf16_bits_of(ldexp(v[k], -ec));
-                    } else {
-                        colIdx[slot] = (uint8_t)T;
-                        v64[slot] = 0.0;
-                        v32[slot] = 0.0f;
-                        v16[slot] = 0;
-                    }
-                    j++;
+            int64_t local = 0;              /* entries of this tile so far, pads included */
+            int64_t next_col = 0;           /* local columns below it have their pointer set */
+            while (e < m && buf[e].col / T == cb) {
+                int64_t c = buf[e].col - cb * T;
+                for (; next_col <= c; ++next_col) cp[next_col] = (uint16_t)local;
+                int64_t c0 = e;
+                while (e < m && buf[e].col == buf[c0].col) {
+                    int64_t k = buf[e].k;
+                    int ec = colExp[ci[k]];
+                    rowIdx[pos + local] = (uint8_t)buf[e].lrow;
+                    v64[pos + local] = v[k];
+                    v32[pos + local] = f32_of(ldexp(v[k], -ec));
+                    v16[pos + local] = bf16_bits_of(ldexp(v[k], -ec));
+                    local++;
+                    e++;
+                }
+                if (padded(e - c0, pad) > e - c0) {   /* sentinel-marked zero */
+                    rowIdx[pos + local] = (uint8_t)T;
+                    v64[pos + local] = 0.0;
+                    v32[pos + local] = 0.0f;
+                    v16[pos + local] = 0;
+                    local++;
                 }
             }
-            pos += w * h;
+            for (; next_col <= T; ++next_col) cp[next_col] = (uint16_t)local;
+            pos += local;
             t++;
         }
         tileRowPtr[rb + 1] = t;
     }
     tileNnzOff[t] = pos;
+    free(buf);
     return ORA_OK;
 }
 

@@ -5,6 +5,7 @@ import pytest
 
 import oracle
 from helpers import Pair, row_rel_err
+from test_host_layout import same_csc
 from mixed_precision_sparse_gb300 import evocg
 from mixed_precision_sparse_gb300 import workloads as W
 
@@ -33,17 +34,13 @@ def _small_cases():
 CASES = _small_cases()
 
 
+@pytest.mark.parametrize("pad", [1, 2])
 @pytest.mark.parametrize("name,m,T", CASES, ids=[c[0] for c in CASES])
-def test_layout_bit_exact(name, m, T):
+def test_layout_bit_exact(name, m, T, pad):
+    """The device-resident structure, copied back and written as EvoCG's Tile-CSC, equals the
+    oracle's independent Tile-CSC bit for bit (both paddings)."""
     P = Pair(m, T)
-    g = P.G.export()
-    t = P.t
-    assert (P.G.ntiles, P.G.nnz, P.G.nslots) == (t.ntiles, t.nnz, t.nslots)
-    for k in ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowMask", "tileWidth", "colIdx", "v16",
-              "colExp"]:
-        assert np.array_equal(g[k], getattr(t, k)), k
-    assert np.array_equal(g["v64"].view(np.uint64), t.v64.view(np.uint64))
-    assert np.array_equal(g["v32"].view(np.uint32), t.v32.view(np.uint32))
+    same_csc(P.G.export_csc(pad), oracle.Tiles(P.A, T, pad))
 
 
 def test_rounding_bit_exact():
@@ -164,12 +161,11 @@ def test_spmv_rejects_bad_maps():
 
 @pytest.mark.parametrize("cfg", [2, 3, 5, 4])
 def test_spmv_parity_full_size(cfg):
-    """Full-size workloads in the benchmark's launch configuration: every row checked."""
+    """Full-size workloads in the benchmark's launch configuration: the uploaded structure
+    against the oracle's Tile-CSC, then every row of the SpMV."""
     w = W.workload(cfg)
     P = Pair((w.n, w.rp, w.ci, w.v), w.T)
-    g = P.G.export()
-    for k in ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowMask", "tileWidth", "colIdx"]:
-        assert np.array_equal(g[k], getattr(P.t, k)), k
+    same_csc(P.G.export_csc(1), P.t)
     x = np.random.default_rng(cfg).uniform(-1, 1, P.n)
     _check_spmv(P, None, x, TOL64)
     _check_spmv(P, P.tile_map(cfg), x, TOLMIX)

@@ -1,6 +1,8 @@
-"""The library's host tile builder against the oracle's, bit for bit, without a GPU
-(evocg_tile_layout_host: the builder evocg_tile_build runs before it uploads). The GPU suite
-checks the uploaded copy the same way."""
+"""The library's tile builder against the oracle's, bit for bit, without a GPU: the Tile-CSC
+of EvoCG Fig. 4 written from the library's builder (evocg_tile_csc_host) equals the oracle's
+independent Tile-CSC builder for both paddings; the library's own slot-major interior
+(evocg_tile_layout_host, the arrays the SpMV kernels read) holds exactly the CSR entries. The
+GPU suite checks the uploaded copy the same way (evocg_tiles_export_csc)."""
 import numpy as np
 import pytest
 
@@ -28,28 +30,69 @@ def _lib():
     build.build()
 
 
-def _same(h, t):
-    assert (h["ntiles"], h["nslots"]) == (t.ntiles, t.nslots)
-    for k in ["tileRowPtr", "tileColIdx", "tileNnzOff", "rowMask", "tileWidth", "colIdx", "v16",
-              "colExp"]:
+def same_csc(h, t):
+    """Library Tile-CSC arrays h against the oracle's Tiles t, bit for bit."""
+    assert (h["ntiles"], h["nnz_p"]) == (t.ntiles, t.nnz_p)
+    for k in ["tileRowPtr", "tileColIdx", "tileNnzOff", "colPtr", "rowIdx", "v16", "colExp"]:
         assert np.array_equal(h[k], getattr(t, k)), k
     assert np.array_equal(h["v64"].view(np.uint64), t.v64.view(np.uint64))
     assert np.array_equal(h["v32"].view(np.uint32), t.v32.view(np.uint32))
 
 
+@pytest.mark.parametrize("pad", [1, 2])
 @pytest.mark.parametrize("name,m,T", list(_cases()), ids=[c[0] for c in _cases()])
-def test_host_builder_equals_oracle(name, m, T):
+def test_host_tile_csc_equals_oracle(name, m, T, pad):
     n, rp, ci, v = m
-    _same(evocg.tile_layout_host(n, rp, ci, v, T), oracle.Tiles(oracle.CSR(n, rp, ci, v), T))
+    same_csc(evocg.tile_csc_host(n, rp, ci, v, T, pad), oracle.Tiles(oracle.CSR(n, rp, ci, v), T, pad))
 
 
 @pytest.mark.parametrize("cfg", [2, 4])
-def test_host_builder_equals_oracle_full_size(cfg):
-    """The 128^3 diffusion (stencil tiles) and the 4M banded workload (sparse 64 x 64 tiles
-    with second levels)."""
+def test_host_tile_csc_equals_oracle_full_size(cfg):
+    """The 128^3 diffusion (stencil tiles) and the 4M banded workload (sparse 64 x 64 tiles)."""
     w = W.workload(cfg)
-    _same(evocg.tile_layout_host(w.n, w.rp, w.ci, w.v, w.T),
-          oracle.Tiles(oracle.CSR(w.n, w.rp, w.ci, w.v), w.T))
+    same_csc(evocg.tile_csc_host(w.n, w.rp, w.ci, w.v, w.T, 1),
+             oracle.Tiles(oracle.CSR(w.n, w.rp, w.ci, w.v), w.T, 1))
+
+
+def test_host_tile_csc_fig4b():
+    """The library reproduces the Fig. 4(b) fragment (colPtr 0, 4, 6 ... x, x+2; column 0
+    padded with the sentinel row index R) from its own builder."""
+    from test_oracle_tiles import fig4b_matrix
+    g, T, (n, rp, ci, v) = fig4b_matrix()
+    h = evocg.tile_csc_host(n, rp, ci, v, T, int(g["pad"]))
+    assert list(h["colPtr"][0][:3]) == [int(s) for s in g["colPtr_head"].split()]
+    assert list(h["colPtr"][0][-2:]) == [int(s) for s in g["colPtr_tail"].split()]
+    assert list(h["rowIdx"]) == [int(s) for s in g["rowIdx"].split()]
+
+
+def slot_layout_holds_the_csr(h, n, rp, ci, v, T):
+    """The kernels' slot-major interior (row mask, width, w x h slots, pads at local column T)
+    rebuilt into CSR with numpy equals the input; every pad is +0 in all three streams."""
+    rows, cols, vals = [], [], []
+    trow = np.repeat(np.arange(len(h["tileRowPtr"]) - 1), np.diff(h["tileRowPtr"]))
+    for t in range(h["ntiles"]):
+        m, w, off = int(h["rowMask"][t]), int(h["tileWidth"][t]), int(h["tileNnzOff"][t])
+        rr = [r for r in range(T) if (m >> r) & 1]
+        assert h["tileNnzOff"][t + 1] - off == w * len(rr)
+        for k in range(w):
+            for j, r in enumerate(rr):
+                s = off + k * len(rr) + j
+                if h["colIdx"][s] == T:
+                    assert h["v64"][s] == 0 and h["v32"][s] == 0 and h["v16"][s] == 0
+                    continue
+                rows.append(trow[t] * T + r)
+                cols.append(int(h["tileColIdx"][t]) * T + int(h["colIdx"][s]))
+                vals.append(h["v64"][s])
+    rows, cols, vals = np.array(rows), np.array(cols), np.array(vals)
+    o = np.lexsort((cols, rows))
+    assert np.array_equal(cols[o], ci) and np.array_equal(vals[o].view(np.uint64), np.asarray(v).view(np.uint64))
+    assert np.array_equal(np.searchsorted(rows[o], np.arange(n + 1)), rp)
+
+
+@pytest.mark.parametrize("name,m,T", list(_cases()), ids=[c[0] for c in _cases()])
+def test_slot_layout_holds_the_csr(name, m, T):
+    n, rp, ci, v = m
+    slot_layout_holds_the_csr(evocg.tile_layout_host(n, rp, ci, v, T), n, rp, ci, v, T)
 
 
 def test_host_builder_rejects_bad_input():
