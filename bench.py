@@ -1,12 +1,13 @@
 """Benchmark: CG time-to-solution of the tile-wise mixed-precision solver on one GB300.
 
-Workload (default): 3D 7-point variable-coefficient diffusion on a 128^3 grid (n = 2,097,152,
-nnz = 14,581,760), face coefficients 10^U[-2,2], b ~ U[-1,1], 32 x 32 tiles, Jacobi-PCG,
-rtol 1e-8, in-loop threshold controller (eps = rtol), FP64 finish. A step is one full solve
-(every stage of the hot path: controller, mixed SpMV with fused p.q, fused updates, the
-graph-driven loop and the FP64 true-residual check), inputs resident in HBM.
+Workload (default): Q1 bilinear 9-point anisotropic diffusion on a 4096 x 4096 grid
+(n = 16,777,216, nnz = 150,945,796; the largest single-GPU configuration), ratio 1e3 rotated
+30 degrees, b ~ U[-1,1], 32 x 32 tiles, Jacobi-PCG, rtol 1e-8, maxit 5000, the seeded
+40/40/20 FP64/FP32/BF16 per-tile map, FP64 finish. A step is one full solve (mixed SpMV with
+fused p.q, fused updates, the graph-driven loop and the FP64 true-residual check), inputs
+resident in HBM. `--workload N` selects another of the five configurations.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload N]
 
 N > 1 runs N independent replicas (one solve per rank per step, weak scaling); launch it
 with torch.distributed.run. `--impl reference` times the CPU oracle on the host cores on a
@@ -123,22 +124,14 @@ def _traffic_for(kernel_src_hash):
 
 
 def _src_hash():
-    """Hash of what the SpMV kernels are built from: their sources and, from the internal
-    header, the structures they read (DevState, TilesView, StagedLimits and the stage-size
-    helper, SpmvLaunch); other declarations of the header do not change the kernel."""
-    import re
+    """Hash of what the SpMV kernels are built from: the kernel sources, the host planner and
+    builder whose layout they read, and the internal header."""
     csrc = os.path.join(ROOT, "mixed_precision_sparse_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("spmv.cu", "spmv_staged.cu", "staged_plan.cpp", "fpconv.cuh"):
+    for name in ("spmv_panel.cu", "panel_plan.cpp", "tile_build.cpp", "spmv.cu", "fpconv.cuh",
+                 "evocg_internal.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
-    with open(os.path.join(csrc, "evocg_internal.h")) as f:
-        hdr = f.read()
-    for pat in (r"struct DevState \{.*?\n\};", r"struct TilesView \{.*?\n\};",
-                r"struct StagedLimits \{.*?\n\};", r"inline int staged_slot_bytes.*?\n\}",
-                r"struct SpmvLaunch \{.*?\n\};", r"constexpr int k\w+ = [^;]*;"):
-        for m in re.findall(pat, hdr, flags=re.S):
-            h.update(m.encode())
     return h.hexdigest()
 
 
@@ -157,15 +150,26 @@ def _oracle_iterations(cfg):
     return None
 
 
+def default_sample_iters(w):
+    """Oracle iterations for about 10-20 s of single-core CPU work (the oracle runs at roughly
+    25 ns per stored entry and iteration)."""
+    return max(2, min(40, int(round(15.0 / (2.6e-8 * max(w.nnz, 1))))))
+
+
 def oracle_sample(w, sample_iters):
-    """Time `sample_iters` iterations of the oracle's solve of workload w (single thread).
-    Returns seconds per iteration."""
+    """Time `sample_iters` iterations of the oracle's solve of workload w (single thread), with
+    the workload's own map or controller. Returns seconds per iteration."""
     import oracle
+    from mixed_precision_sparse_gb300 import workloads as W
     A = oracle.CSR(w.n, w.rp, w.ci, w.v)
     t = oracle.Tiles(A, w.T)
     kw = dict(jacobi=w.jacobi)
     if w.ctrl == "threshold":
         kw.update(ctrl="threshold", eps=w.eps)
+    elif w.ctrl == "mlp":
+        kw.update(ctrl="mlp", weights=W.mlp_weights(w.T, w.mlp_seed), delta=w.delta)
+    else:
+        kw.update(tile_map=W.tile_map(t.tile_rows(), t.tileColIdx, t.nrb, w.map_seed))
     t0 = time.perf_counter()
     r = oracle.cg(A, t, w.b, 0.0, sample_iters, **kw)
     el = time.perf_counter() - t0
@@ -178,7 +182,7 @@ def run_reference(args):
         return 0
     w = _workload(args.workload)
     iters_full = _oracle_iterations(args.workload)
-    sample = args.cpu_sample_iters
+    sample = args.cpu_sample_iters or max(1, default_sample_iters(w) // 2)
     times = []
     for _ in range(args.warmup):
         oracle_sample(w, 1)
@@ -225,6 +229,90 @@ def job_seconds_per_solve(ms_per_step, world):
     """Whole-job time per solve: every rank runs one solve per step (independent replicas),
     so a step of ms_per_step milliseconds completes `world` solves."""
     return ms_per_step / 1000.0 / world
+
+
+def spmv_measure(G, w, dev, stream, peak, reps=50, cold_reps=10):
+    """SpMV alone on workload w's structure G: microseconds per launch warm and with L2
+    flushed, algorithmic bytes, GB/s and fractions of the peak, for the seeded 40/40/20 map
+    and the all-FP64 map (the latter also against the FP64 pipe's rate)."""
+    import numpy as np
+    import torch
+
+    from mixed_precision_sparse_gb300 import evocg, spmv_run
+    from mixed_precision_sparse_gb300 import workloads as W
+    trow, ex = G.tile_rows()
+    tnnz = spmv_run.tile_entries(ex, G.T)
+    xs = torch.from_numpy(np.random.default_rng(7).uniform(-1, 1, w.n)).to(dev)
+    ys = torch.empty_like(xs)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (128 << 20)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    out = {}
+    for label, mp in (("mixed_40_40_20", W.tile_map(trow, ex["tileColIdx"], G.nrb, 12345)),
+                      ("fp64", np.zeros(G.ntiles, np.uint8))):
+        evocg.set_tile_precision(G, mp)
+        evocg.spmv(G, xs, ys)
+        for _ in range(5):
+            evocg.spmv_ex(G, xs, ys, evocg.SPMV_REUSE_XCOPIES)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            evocg.spmv_ex(G, xs, ys, evocg.SPMV_REUSE_XCOPIES)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1000.0 / reps
+        cold = []
+        for _ in range(cold_reps):
+            flush.fill_(1.0)
+            e0.record(stream)
+            evocg.spmv_ex(G, xs, ys, evocg.SPMV_REUSE_XCOPIES)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            cold.append(e0.elapsed_time(e1) * 1000.0)
+        per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
+        B = spmv_run.spmv_bytes(w.n, G.ntiles, G.nrb, per, G.T)
+        cus = statistics.median(cold)
+        out[label] = {"us": us, "bytes": int(B), "gbs": B / us / 1e3,
+                      "frac_of_peak": B / us / 1e3 / peak, "frac_of_8tbs": B / us / 1e3 / 8000.0,
+                      "cold": {"us": cus, "gbs": B / cus / 1e3, "frac_of_peak": B / cus / 1e3 / peak}}
+    # all-FP64: one FP64 fused multiply-add per stored entry, against the FP64 pipe's rate
+    out["fp64"]["fp64_fma_per_s"] = int(per.sum()) / (out["fp64"]["us"] * 1e-6)
+    return out
+
+
+def extra_workload(cfg, dev, stream, peak, steps=3):
+    """The solve and the SpMV of another configuration, outside the timed region."""
+    import torch
+
+    from mixed_precision_sparse_gb300 import evocg
+    from mixed_precision_sparse_gb300 import workloads as W
+    w = _workload(cfg)
+    G = evocg.tile_build(w.n, w.rp, w.ci, w.v, w.T)
+    ctrl = None
+    if w.ctrl == "threshold":
+        ctrl = evocg.Ctrl.threshold(w.eps, w.kstar)
+    elif w.ctrl == "mlp":
+        ctrl = evocg.Ctrl.mlp(W.mlp_weights(w.T, w.mlp_seed), w.kstar, w.delta)
+    else:
+        trow, ex = G.tile_rows()
+        evocg.set_tile_precision(G, W.tile_map(trow, ex["tileColIdx"], G.nrb, w.map_seed))
+    b = torch.from_numpy(w.b).to(dev)
+    x = torch.empty_like(b)
+    info = evocg.cg_solve(G, b, x, w.rtol, w.maxit, w.jacobi, ctrl, True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        info = evocg.cg_solve(G, b, x, w.rtol, w.maxit, w.jacobi, ctrl, True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    tts = e0.elapsed_time(e1) / 1000.0 / steps
+    spmv = spmv_measure(G, w, dev, stream, peak)
+    G.free()
+    return {"tts_s": tts, "iters": info["iters"], "status": info["status"],
+            "true_res": info["true_res"], "spmv": spmv}
 
 
 def run_ours(args):
@@ -322,47 +410,34 @@ def run_ours(args):
     fp64_solve = {"s": fp64_s, "iters": fp64_info["iters"], "true_res": fp64_info["true_res"],
                   "mixed_over_fp64": value * world / fp64_s}
 
-    # ---- the dominant kernel (the SpMV) timed alone on the same stream, CUDA events,
-    # back-to-back launches (inputs > L2), with the seeded 40/40/20 mixed map and all-FP64
-    trow, ex = G.tile_rows()
-    tnnz = spmv_run.tile_entries(ex, G.T)
+    # ---- the dominant kernel (the SpMV) timed alone on the solve's stream with CUDA events,
+    # with the seeded 40/40/20 mixed map and all-FP64: warm (back-to-back launches; every
+    # launch streams more than L2 on the large workloads) and cold (L2 flushed by writing a
+    # buffer of twice its size before each launch, each launch timed on its own)
     peak, peak_kind = _peaks()
-    xs = torch.from_numpy(np.random.default_rng(7).uniform(-1, 1, w.n)).to(dev)
-    ys = torch.empty_like(xs)
-    spmv = {}
-    for label, mp in (("mixed_40_40_20", W.tile_map(trow, ex["tileColIdx"], G.nrb, 12345)),
-                      ("fp64", np.zeros(G.ntiles, np.uint8))):
-        evocg.set_tile_precision(G, mp)
-        evocg.spmv(G, xs, ys)
-        reps = 50
-        for _ in range(5):
-            evocg.spmv_ex(G, xs, ys, evocg.SPMV_REUSE_XCOPIES)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(reps):
-            evocg.spmv_ex(G, xs, ys, evocg.SPMV_REUSE_XCOPIES)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1000.0 / reps
-        per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
-        B = spmv_run.spmv_bytes(w.n, G.ntiles, G.nrb, per)
-        spmv[label] = {"us": us, "bytes": int(B), "gbs": B / us / 1e3,
-                       "frac_of_peak": B / us / 1e3 / peak, "frac_of_8tbs": B / us / 1e3 / 8000.0}
+    spmv = spmv_measure(G, w, dev, stream, peak)
     src_hash = _src_hash()
     traffic = _traffic_for(src_hash)
     mixed = spmv["mixed_40_40_20"]
     roofline = {"bound": "hbm", "achieved": mixed["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": mixed["frac_of_peak"], "traffic": traffic,
-                "kernel": "spmv_staged_kernel<32> (bulk-copy staged, mixed 40/40/20 map)", "peak_kind": peak_kind,
-                "frac_of_8tbs": mixed["frac_of_8tbs"], "bytes_per_launch": mixed["bytes"],
-                "us_per_launch": mixed["us"], "fp64_map": spmv["fp64"]}
+                "kernel": "spmv_panel_kernel (panel-streaming, cp.async-staged; mixed 40/40/20 map)",
+                "peak_kind": peak_kind, "frac_of_8tbs": mixed["frac_of_8tbs"],
+                "bytes_per_launch": mixed["bytes"], "us_per_launch": mixed["us"],
+                "bytes_rule": "Tile-CSC algorithmic bytes: active value stream + 1 row-index "
+                              "byte per entry + 2(T+1)+12 bytes per tile + x and y once",
+                "cold_l2": {k: spmv[k]["cold"] for k in spmv}, "fp64_map": spmv["fp64"]}
+    extra = {}
+    if args.workload != 2 and not args.no_extra:
+        extra["diffusion3d_7pt_128cubed"] = extra_workload(2, dev, stream, peak)
 
     # ---- CPU oracle on the host cores, a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        sec_it, _ = oracle_sample(w, args.cpu_sample_iters)
+        ns = args.cpu_sample_iters or default_sample_iters(w)
+        sec_it, _ = oracle_sample(w, ns)
         cpu = {"value": sec_it * info["iters"], "unit": "s", "cores": 1, "kind": "oracle",
-               "sample": f"first {args.cpu_sample_iters} iterations of the same solve, "
+               "sample": f"first {ns} iterations of the same solve, "
                          f"seconds/iteration x the GPU solve's {info['iters']} iterations"}
 
     # what one iteration streams (the SpMV's algorithmic bytes with the map in force plus the
@@ -399,6 +474,7 @@ def run_ours(args):
             "gpu_launches": launches,
             "roofline": roofline,
             "cpu_baseline": cpu,
+            "other_workloads": extra,
         }
         print(json.dumps(line), flush=True)
     G.free()
@@ -410,12 +486,14 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2)
-    ap.add_argument("--cpu-sample-iters", type=int, default=8)
+    ap.add_argument("--workload", type=int, default=5)
+    ap.add_argument("--cpu-sample-iters", type=int, default=0,
+                    help="oracle iterations per CPU sample (0: about 10-20 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the 128^3 workload's summary")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -281,7 +281,8 @@ int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int flags, void *
  *   x, y: DEVICE pointers, n FP64 each, not overlapping. n must be at most 1,048,576
  *   (EINVAL otherwise, with a message naming the limit).
  * The first call on a device looks up that array's device address (cudaGetSymbolAddress),
- * once per device; make that first call before any stream capture. Every call shares the
+ * once per device and CUDA context (again after a cudaDeviceReset, which loads the library's
+ * module anew); make that first call before any stream capture. Every call shares the
  * one array and overwrites all of it that it reads, so no state carries over between calls,
  * but calls that may overlap on the GPU (concurrent streams, or several handles at once)
  * race on it: order them. Asynchronous on `stream`.

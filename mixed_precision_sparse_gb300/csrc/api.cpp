@@ -359,8 +359,9 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
             std::vector<int32_t> wpan;
             std::string why;
             const int64_t warps = (int64_t)pg * (kPanelThreads / 32);
-            if (panel_plan(H, warps, &pd, &wrec, &wpan, &why) &&
-                panel_plan_ok(H, warps, pd, wrec, wpan, &why)) {
+            const int sb = panel_stage_bytes(variant);
+            if (panel_plan(H, warps, sb, &pd, &wrec, &wpan, &why) &&
+                panel_plan_ok(H, warps, sb, pd, wrec, wpan, &why)) {
                 A->panel_variant = variant;
                 up(&A->pdesc, pd.data(), (int64_t)pd.size());
                 up(&A->warpRec, wrec.data(), (int64_t)wrec.size());

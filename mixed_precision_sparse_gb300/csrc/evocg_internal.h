@@ -242,9 +242,10 @@ int spmv_dot_partials(const SpmvLaunch &L);   // warps that write a p.q partial
 cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s);
 cudaError_t launch_spmv_panel(const SpmvLaunch &L, cudaStream_t s);
 int panel_grid_for(int T, int sms, int variant);   // 0 if no panel kernel exists for T
-bool panel_plan(const HostTiles &H, int64_t warps, std::vector<uint4> *desc,
+int panel_stage_bytes(int variant);                // shared-memory stage of one warp
+bool panel_plan(const HostTiles &H, int64_t warps, int stage_bytes, std::vector<uint4> *desc,
                 std::vector<int64_t> *warpRec, std::vector<int32_t> *warpPanel, std::string *why);
-bool panel_plan_ok(const HostTiles &H, int64_t warps, const std::vector<uint4> &desc,
+bool panel_plan_ok(const HostTiles &H, int64_t warps, int stage_bytes, const std::vector<uint4> &desc,
                    const std::vector<int64_t> &warpRec, const std::vector<int32_t> &warpPanel,
                    std::string *why);
 

@@ -7,6 +7,7 @@
 // under a fixed memory budget) forbid allocations they did not plan. For those callers
 // this file holds the scratch in a fixed array that is part of the loaded module: it is
 // reserved once, when the library is loaded on a device, and never grows.
+#include <cuda.h>   // CUcontext; the driver call is reached through the runtime's entry point table
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -27,23 +28,58 @@ static __device__ __align__(256) float g_noalloc_scratch[2 * kNoAllocMaxN];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-float *g_scratch_ptr[kMaxDevices] = {};
+// The scratch's device address, looked up once per device and context: the module (and with
+// it the array) is loaded again in a new context, for instance after cudaDeviceReset, so an
+// address is only reused while the context it was looked up in is still the current one.
+struct ScratchAddr {
+    CUcontext ctx;
+    float *ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch on the current device, looked up once per device.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+
+int current_context(CUcontext *out)
+{
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000,
+                                                               cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f) {
+            cudaGetLastError();
+            return evocg::fail(EVOCG_ECUDA, "cuCtxGetCurrent is not available from the CUDA runtime");
+        }
+        fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    }
+    *out = nullptr;
+    if (fn(out) != CUDA_SUCCESS) return evocg::fail(EVOCG_ECUDA, "cuCtxGetCurrent failed");
+    return EVOCG_OK;
+}
+
+// Device address of the scratch in the current device's current context, looked up with
+// cudaGetSymbolAddress on the first call in that context.
 int scratch_for_current_device(float **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return evocg::cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return evocg::fail(EVOCG_EDEVICE, "device index out of range");
+    e = cudaSetDevice(dev);   // binds the device's primary context to this thread
+    if (e != cudaSuccess) return evocg::cuda_fail(e, "cudaSetDevice");
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    CUcontext ctx = nullptr;
+    int rc = current_context(&ctx);
+    if (rc) return rc;
+    if (!g_scratch[dev].ptr || g_scratch[dev].ctx != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return evocg::cuda_fail(e, "cudaGetSymbolAddress (allocation-free SpMV scratch)");
-        g_scratch_ptr[dev] = static_cast<float *>(p);
+        g_scratch[dev].ptr = static_cast<float *>(p);
+        g_scratch[dev].ctx = ctx;
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_scratch[dev].ptr;
     return EVOCG_OK;
 }
 

@@ -8,18 +8,19 @@
 // by one per tile (slot offset, width, column block, row mask). Lane l owns row l of the
 // current panel and keeps its sums in registers: no cross-lane reduction of any row.
 //
-// Staging. Each warp owns one shared-memory stage. A panel's tiles are cut at run time into
-// batches that fit it (the cut depends on the precisions, hence on the map): for a batch the
-// lanes issue asynchronous global-to-shared copies (cp.async, 16 bytes per lane and
-// instruction) of the 16-byte cover of the batch's local-column bytes, of every tile's value
-// slice in the stream its precision selects, and of every tile's x segment in that
-// precision; single-entry tiles (one row, width one: the panel-edge tiles of stencils, most
-// of a stencil's tiles by count) copy just their value and x entry. The warp then waits for
-// its own copies (cp.async.wait_group: a hardware wait on the issuing threads' copies, no
-// polling) and computes the batch from shared memory. The next panel's descriptors and their
-// precisions are loaded while the current panel is in flight. Registers no longer bound the
-// bytes in flight, so an SM holds many warps with kilobytes in flight each. A tile too large
-// for the stage on its own is computed from global memory level by level.
+// Staging. Each warp owns one shared-memory stage. A panel's tiles come in batches planned on
+// the host (panel_plan.cpp: every tile sized for FP64, so the plan holds for any precision
+// map), each tile with a fixed stage offset. For a batch the lanes issue asynchronous
+// global-to-shared copies (cp.async): a tile's value slice in the stream its precision
+// selects (16 bytes per lane and instruction; the builder aligns every tile with more than one
+// slot to 8 slots and pads it to a multiple of 8, so slices are whole 16-byte chunks in every
+// stream), its local-column bytes (8 per lane) and its x segment in that precision (one entry
+// per lane); single-entry tiles (one row, width one: the panel-edge tiles of stencils, most of
+// a stencil's tiles by count) copy just their value and x entry, one lane each. The warp then
+// waits for its own copies (cp.async.wait_group: a hardware wait on the issuing threads'
+// copies, no polling) and computes the batch from shared memory. The next panel's descriptors
+// and their precisions are loaded while the current panel is in flight. A tile too large for
+// the stage on its own is computed from global memory level by level.
 //
 // Arithmetic. On GB300 the FP64 unit issues about two operations per clock per SM, so FP64
 // instructions go only where the data is FP64: one fused multiply-add per FP64 entry. FP32
@@ -38,7 +39,6 @@ namespace evocg {
 namespace {
 
 constexpr unsigned kAll = 0xffffffffu;
-constexpr int kSingleBytes = 16;   // stage bytes of a single-entry tile: value word, x entry
 
 __device__ __forceinline__ unsigned lanemask_lt()
 {
@@ -117,37 +117,17 @@ __device__ __forceinline__ void acc_prod(float &s, float &c, float a, float b)
     c = __fadd_rn(c, e);
 }
 
-__device__ __forceinline__ int vsize(int pr) { return pr == EVOCG_FP64 ? 8 : pr == EVOCG_FP32 ? 4 : 2; }
-__device__ __forceinline__ int xsize(int pr) { return pr == EVOCG_FP64 ? 8 : 4; }
+// Record flags (panel_plan.cpp): single-entry tile, first tile of a batch, tile computed from
+// global memory.
+constexpr unsigned kSingleBit = 1u << 26, kBatchBit = 1u << 27, kDirectBit = 1u << 28;
 
-// 16-byte chunks of the cover of slots [s0, s0 + m) in a stream of elements of sz bytes.
-__device__ __forceinline__ int cover16(int64_t s0, int m, int sz)
-{
-    return (int)((((s0 + m) * sz + 15) & ~(int64_t)15) - ((s0 * sz) & ~(int64_t)15)) >> 4;
-}
-
-__device__ __forceinline__ int scan_incl(int v, int lane)
-{
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(kAll, v, o);
-        if (lane >= o) v += t;
-    }
-    return v;
-}
-
-// Record layout (panel_plan.cpp): header {tiles, panel, first slot lo, hi}; tile {slot offset
-// from the panel's first slot, w | single-entry column << 8 | stored entries << 16, column
-// block, row mask}. SB: stage bytes per warp; MB: blocks per SM the registers are sized for.
-template <int R, int C, bool FORCE64, bool DOT, int SB, int MB>
+// Record layout and batches: panel_plan.cpp. SB: stage bytes per warp (the plan's); MB: blocks
+// per SM the registers are sized for; IL: panels interleaved over the warps.
+template <int R, int C, bool FORCE64, bool DOT, int SB, int MB, bool IL>
 __global__ void __launch_bounds__(kPanelThreads, MB) spmv_panel_kernel(SpmvLaunch L)
 {
     static_assert(R == 16 || R == 32, "panel rows");
     static_assert(C == R, "this kernel reads tiles as wide as the panel is tall");
-    // stage: single-entry slots, then local columns, then value covers and x segments
-    constexpr int kColSt = 32 * kSingleBytes;
-    constexpr int kData = SB - kColSt - 32;   // bytes for columns (+32 of alignment) and data
-    static_assert(SB % 16 == 0 && kData >= 1024, "stage size");
     extern __shared__ __align__(16) unsigned char smem_raw[];
     if ((DOT || L.gate) && L.st->done) return;
     const TilesView &A = L.A;
@@ -156,9 +136,15 @@ __global__ void __launch_bounds__(kPanelThreads, MB) spmv_panel_kernel(SpmvLaunc
     const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + wib;
     const uint32_t st0 = smem_addr(smem_raw + (size_t)wib * SB);
     const unsigned ltm = lanemask_lt();
-    const int p_end = A.warpPanel[wid + 1];
-    int p = A.warpPanel[wid];
-    int64_t rec = A.warpRec[wid];
+    // Panels of this warp: a contiguous range of the plan (IL = false), or every nwarps-th
+    // panel from wid (IL = true: all warps sweep one window of the matrix together). Panel
+    // q's header record is at q + tileRowPtr[q].
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t pstep = IL ? nwarps : 1;
+    const int64_t p_end = IL ? A.nrb : A.warpPanel[wid + 1];
+    int64_t p = IL ? wid : A.warpPanel[wid];
+    int64_t rec = IL ? (p < p_end ? p + A.tileRowPtr[p] : 0) : A.warpRec[wid];
+    int64_t tr_next = (IL && p + pstep < p_end) ? __ldg(A.tileRowPtr + p + pstep) : 0;
     double dotp = 0.0;
     unsigned cnt0 = 0, cnt1 = 0, cnt2 = 0;
     uint4 win = make_uint4(0u, 0u, 0u, 0u);
@@ -170,12 +156,13 @@ __global__ void __launch_bounds__(kPanelThreads, MB) spmv_panel_kernel(SpmvLaunc
             wprec = L.map_kind ? (int)__ldg(L.prec + (int)win.z) : (int)__ldcs(L.prec + (rec + lane - p - 1));
     }
 
-    for (; p < p_end; ++p) {
+    for (; p < p_end; p += pstep) {
         const unsigned nt = __shfl_sync(kAll, win.x, 0);
         const int64_t sbase = (int64_t)(((uint64_t)__shfl_sync(kAll, win.w, 0) << 32) |
                                         (uint64_t)__shfl_sync(kAll, win.z, 0));
-        const int64_t nextrec = rec + 1 + nt;
-        const bool more = p + 1 < p_end;
+        const bool more = p + pstep < p_end;
+        const int64_t nextrec = IL ? (more ? p + pstep + tr_next : 0) : rec + 1 + nt;
+        if (IL) tr_next = (p + 2 * pstep < p_end) ? __ldg(A.tileRowPtr + p + 2 * pstep) : 0;
         uint4 nwin = make_uint4(0u, 0u, 0u, 0u);
         int nprec = 0;
         bool nprec_pending = false;   // a per-column-block map: resolved once nwin is in
@@ -184,15 +171,16 @@ __global__ void __launch_bounds__(kPanelThreads, MB) spmv_panel_kernel(SpmvLaunc
             if (!FORCE64) {
                 // tile index of lane's record in the next panel (its count is not known yet,
                 // so the index is bounded by the tile count instead)
-                const int64_t ti = nextrec + lane - (p + 1) - 1;
+                const int64_t ti = nextrec + lane - (p + pstep) - 1;
                 if (L.map_kind) nprec_pending = true;
                 else if (lane > 0 && ti < A.ntiles) nprec = (int)__ldcs(L.prec + ti);
             }
         }
-        const int64_t row = (int64_t)p * R + lane;
-        const bool rowok = lane < R && row < A.n;
-        double xrow = 0.0;
-        if (DOT && rowok) xrow = __ldg(L.x64 + row);
+        // this panel's slots in every stream
+        const unsigned char *ci = A.colIdx + sbase;
+        const unsigned char *vb64 = reinterpret_cast<const unsigned char *>(A.v64 + sbase);
+        const unsigned char *vb32 = reinterpret_cast<const unsigned char *>(A.v32 + sbase);
+        const unsigned char *vb16 = reinterpret_cast<const unsigned char *>(A.v16 + sbase);
 
         double acc = 0.0;
         float ls = 0.f, lc = 0.f;
@@ -209,84 +197,84 @@ __global__ void __launch_bounds__(kPanelThreads, MB) spmv_panel_kernel(SpmvLaunc
                     prec = L.map_kind ? (int)__ldg(L.prec + (int)d.z) : (int)__ldcs(L.prec + (r - p - 1));
             }
             if (FORCE64 || !valid) prec = 0;
-            const int w = (int)(d.y & 0xFFu);
-            const unsigned mk = d.w;
-            const int h = __popc(mk);
-            const int m = w * h;                         // slots of the tile
-            const int64_t s0 = sbase + (int64_t)d.x;     // its first slot
-            const bool single = valid && w == 1 && h == 1;
-            const bool regular = valid && !single;
             if (!FORCE64) anylow |= __any_sync(kAll, valid && prec != EVOCG_FP64);
-            if (DOT && valid) {   // census: stored entries of the tile, by precision
-                const unsigned e = d.y >> 16;
-                if (prec == EVOCG_FP64) cnt0 += e; else if (prec == EVOCG_FP32) cnt1 += e; else cnt2 += e;
-            }
-            // stage bytes: value cover + x segment of a regular tile, and an upper bound of the
-            // local-column bytes of every tile (its slots)
-            const int dbytes = regular ? 16 * cover16(s0, m, vsize(prec)) + C * xsize(prec) : 0;
-            const int need = valid ? dbytes + m : 0;
-            unsigned left = __ballot_sync(kAll, valid);
-            while (left) {
-                // batch: the lowest tiles still left whose bytes fit the stage (a prefix)
-                const bool in = (left >> lane) & 1u;
-                const int incl = scan_incl(in ? need : 0, lane);
-                unsigned take = __ballot_sync(kAll, in && incl <= kData);
-                const bool big = take == 0u;   // the lowest tile left does not fit alone
-                if (big) take = left & (0u - left);
+            const unsigned vmask = __ballot_sync(kAll, valid);
+            const unsigned smask = __ballot_sync(kAll, valid && (d.y & kSingleBit));
+            unsigned bmask = __ballot_sync(kAll, valid && (d.y & kBatchBit));
+            while (bmask) {
+                const int lo = __ffs(bmask) - 1;
+                bmask &= bmask - 1u;
+                const unsigned upto = bmask ? (1u << (__ffs(bmask) - 1)) - 1u : kAll;
+                const unsigned take = vmask & upto & ~((1u << lo) - 1u);
+                const unsigned treg = take & ~smask, tsgl = take & smask;
                 const bool mine = (take >> lane) & 1u;
-                const unsigned treg = take & __ballot_sync(kAll, regular);
-                const unsigned tsgl = take & __ballot_sync(kAll, single);
-                // local columns of the batch: one cover of its contiguous slot range
-                const int lo_l = __ffs(take) - 1, hi_l = 31 - __clz(take);
-                const int64_t c_a = __shfl_sync(kAll, s0, lo_l) & ~(int64_t)15;
-                const int64_t c_b = (__shfl_sync(kAll, s0 + m, hi_l) + 15) & ~(int64_t)15;
-                const int ncol16 = (int)((c_b - c_a) >> 4);
-                const uint32_t col_st = st0 + kColSt;
-                // each regular tile's value cover and x segment, packed after the columns
-                const int dincl = scan_incl(mine ? dbytes : 0, lane);
-                const uint32_t vst = col_st + 16u * (uint32_t)ncol16 + (uint32_t)(dincl - (mine ? dbytes : 0));
-
-                if (!big) {
-                    // ---- issue the batch's copies
-                    for (int q = lane; q < ncol16; q += 32) cp16(col_st + 16u * q, A.colIdx + c_a + 16 * q);
-                    unsigned tr = treg;
-                    while (tr) {
-                        const int i = __ffs(tr) - 1;
-                        tr &= tr - 1u;
-                        const int pi = __shfl_sync(kAll, prec, i);
-                        const int64_t si = __shfl_sync(kAll, s0, i);
-                        const int mi = __shfl_sync(kAll, m, i);
-                        const uint32_t vi = __shfl_sync(kAll, vst, i);
-                        const int cbi = __shfl_sync(kAll, (int)d.z, i);
-                        const int sz = vsize(pi);
-                        const int64_t a = (si * sz) & ~(int64_t)15;
-                        const int nv16 = cover16(si, mi, sz);
-                        const unsigned char *vsrc =
-                            pi == EVOCG_FP64 ? reinterpret_cast<const unsigned char *>(A.v64)
-                            : pi == EVOCG_FP32 ? reinterpret_cast<const unsigned char *>(A.v32)
-                                               : reinterpret_cast<const unsigned char *>(A.v16);
-                        for (int q = lane; q < nv16; q += 32) cp16(vi + 16u * q, vsrc + a + 16 * q);
-                        const uint32_t xst = vi + 16u * nv16;
-                        const int64_t xj = (int64_t)cbi * C + lane;
-                        if (lane < C && xj < A.n) {
-                            if (pi == EVOCG_FP64) cp8(xst + 8u * lane, L.x64 + xj);
-                            else cp4(xst + 4u * lane, (pi == EVOCG_FP32 ? L.x32 : L.x16f) + xj);
+                const unsigned ylo = __shfl_sync(kAll, d.y, lo);
+                if (ylo & kDirectBit) {   // a tile larger than the stage, from global memory
+                    const int pi = __shfl_sync(kAll, prec, lo);
+                    const unsigned so = __shfl_sync(kAll, d.x, lo);
+                    const int cbi = __shfl_sync(kAll, (int)d.z, lo);
+                    const unsigned mi = __shfl_sync(kAll, d.w, lo);
+                    const int wi = (int)(ylo & 0xFFu), hi = __popc(mi);
+                    const bool has = lane < R && ((mi >> lane) & 1u);
+                    const unsigned s0 = so + (unsigned)__popc(mi & ltm);
+                    for (int k = 0; has && k < wi; ++k) {
+                        const unsigned s = s0 + (unsigned)(k * hi);
+                        const unsigned c = ci[s];
+                        if (c >= (unsigned)C) continue;
+                        const int64_t xj = (int64_t)cbi * C + c;
+                        if (pi == EVOCG_FP64) {
+                            acc = fma(__ldcs(reinterpret_cast<const double *>(vb64) + s), __ldg(L.x64 + xj), acc);
+                            if (DOT) ++cnt0;
+                        } else if (pi == EVOCG_FP32) {
+                            acc_prod(ls, lc, __ldcs(reinterpret_cast<const float *>(vb32) + s), __ldg(L.x32 + xj));
+                            if (DOT) ++cnt1;
+                        } else {
+                            const unsigned b = __ldcs(reinterpret_cast<const unsigned short *>(vb16) + s);
+                            acc_low(ls, lc, __fmul_rn(__uint_as_float(b << 16), __ldg(L.x16f + xj)));
+                            if (DOT) ++cnt2;
                         }
                     }
-                    // single-entry tiles: the value word and the x entry into the lane's slot
-                    if (mine && single) {
-                        const uint32_t sd = st0 + (uint32_t)lane * kSingleBytes;
-                        const int64_t xj = (int64_t)(int)d.z * C + (int64_t)((d.y >> 8) & 0xFFu);
-                        if (prec == EVOCG_FP64) {
-                            cp8(sd, A.v64 + s0);
-                            cp8(sd + 8u, L.x64 + xj);
-                        } else if (prec == EVOCG_FP32) {
-                            cp4(sd, A.v32 + s0);
-                            cp4(sd + 8u, L.x32 + xj);
-                        } else {
-                            cp4(sd, A.v16 + (s0 & ~(int64_t)1));   // the aligned pair holding it
-                            cp4(sd + 8u, L.x16f + xj);
-                        }
+                    continue;
+                }
+                // ---- issue the batch's copies
+                unsigned tr = treg;
+                while (tr) {
+                    const int i = __ffs(tr) - 1;
+                    tr &= tr - 1u;
+                    const unsigned so = __shfl_sync(kAll, d.x, i);
+                    const unsigned y = __shfl_sync(kAll, d.y, i);
+                    const int cbi = __shfl_sync(kAll, (int)d.z, i);
+                    const unsigned mi = __shfl_sync(kAll, d.w, i);
+                    const int pi = __shfl_sync(kAll, prec, i);
+                    const unsigned m8 = ((y & 0xFFu) * (unsigned)__popc(mi) + 7u) & ~7u;
+                    const uint32_t st = st0 + ((y >> 8) & 0xFFFu) * 16u;
+                    const unsigned sz = 8u >> pi;   // 8, 4, 2 bytes
+                    const unsigned char *vs = (pi == EVOCG_FP64 ? vb64 : pi == EVOCG_FP32 ? vb32 : vb16) + so * sz;
+                    const unsigned nv16 = (m8 * sz) >> 4;
+                    for (unsigned q = lane; q < nv16; q += 32) cp16(st + 16u * q, vs + 16u * q);
+                    const uint32_t cst = st + 8u * m8;
+                    for (unsigned q = lane; q < (m8 >> 3); q += 32) cp8(cst + 8u * q, ci + so + 8u * q);
+                    const uint32_t xst = cst + ((m8 + 15u) & ~15u);
+                    const int64_t xj = (int64_t)cbi * C + lane;
+                    if (lane < C && xj < A.n) {
+                        if (pi == EVOCG_FP64) cp8(xst + 8u * lane, L.x64 + xj);
+                        else cp4(xst + 4u * lane, (pi == EVOCG_FP32 ? L.x32 : L.x16f) + xj);
+                    }
+                }
+                // single-entry tiles: their value and x entry into the lane's own 16-byte slot
+                const bool sgl = mine && (d.y & kSingleBit);
+                if (sgl) {
+                    const uint32_t sd = st0 + (uint32_t)lane * 16u;
+                    const int64_t xj = (int64_t)(int)d.z * C + (int64_t)((d.y >> 20) & 0x3Fu);
+                    if (prec == EVOCG_FP64) {
+                        cp8(sd, vb64 + 8u * d.x);
+                        cp8(sd + 8u, L.x64 + xj);
+                    } else if (prec == EVOCG_FP32) {
+                        cp4(sd, vb32 + 4u * d.x);
+                        cp4(sd + 8u, L.x32 + xj);
+                    } else {
+                        cp4(sd, vb16 + 2u * (d.x & ~1u));   // the aligned pair holding it
+                        cp4(sd + 8u, L.x16f + xj);
                     }
                 }
                 if (nprec_pending) {   // the next panel's precisions, while the copies fly
@@ -297,117 +285,101 @@ __global__ void __launch_bounds__(kPanelThreads, MB) spmv_panel_kernel(SpmvLaunc
                 cp_wait_all();
                 __syncwarp();
 
-                // ---- compute the batch
-                if (big) {   // one tile larger than the stage: level by level from global memory
-                    const int pi = __shfl_sync(kAll, prec, lo_l);
-                    const int64_t si = __shfl_sync(kAll, s0, lo_l);
-                    const int wi = __shfl_sync(kAll, w, lo_l);
-                    const unsigned mi = __shfl_sync(kAll, mk, lo_l);
-                    const int cbi = __shfl_sync(kAll, (int)d.z, lo_l);
-                    const int hi = __popc(mi);
-                    const bool has = lane < R && ((mi >> lane) & 1u);
-                    const int j = __popc(mi & ltm);
-                    for (int k = 0; has && k < wi; ++k) {
-                        const int64_t s = si + (int64_t)k * hi + j;
-                        const int c = A.colIdx[s];
-                        if (c >= C) continue;
-                        const int64_t xj = (int64_t)cbi * C + c;
-                        if (pi == EVOCG_FP64) {
-                            acc = fma(__ldcs(A.v64 + s), __ldg(L.x64 + xj), acc);
-                        } else if (pi == EVOCG_FP32) {
-                            acc_prod(ls, lc, __ldcs(A.v32 + s), __ldg(L.x32 + xj));
-                        } else {
-                            const unsigned b = __ldcs(reinterpret_cast<const unsigned short *>(A.v16) + s);
-                            acc_low(ls, lc, __fmul_rn(__uint_as_float(b << 16), __ldg(L.x16f + xj)));
-                        }
-                    }
-                } else {
-                    unsigned tr = treg;
-                    while (tr) {
-                        const int i = __ffs(tr) - 1;
-                        tr &= tr - 1u;
-                        const int pi = __shfl_sync(kAll, prec, i);
-                        const int64_t si = __shfl_sync(kAll, s0, i);
-                        const int wi = __shfl_sync(kAll, w, i);
-                        const unsigned mi = __shfl_sync(kAll, mk, i);
-                        const uint32_t vi = __shfl_sync(kAll, vst, i);
-                        const int hi = __popc(mi);
-                        if (!(lane < R && ((mi >> lane) & 1u))) continue;
-                        const int j = __popc(mi & ltm);
-                        const int sz = vsize(pi);
-                        const uint32_t v0 = vi + (uint32_t)((si * sz) & 15) + (uint32_t)(sz * j);
-                        const uint32_t xst = vi + 16u * cover16(si, hi * wi, sz);
-                        const uint32_t c0 = col_st + (uint32_t)(si - c_a) + (uint32_t)j;
-                        const uint32_t vstep = (uint32_t)(sz * hi);
-                        if (pi == EVOCG_FP64) {
-                            for (int k = 0; k < wi; ++k) {
-                                const unsigned c = lds_u8(c0 + (uint32_t)(k * hi));
-                                if (c < (unsigned)C) acc = fma(lds_f64(v0 + vstep * k), lds_f64(xst + 8u * c), acc);
-                            }
-                        } else if (pi == EVOCG_FP32) {
-                            for (int k = 0; k < wi; ++k) {
-                                const unsigned c = lds_u8(c0 + (uint32_t)(k * hi));
-                                if (c < (unsigned)C) acc_prod(ls, lc, lds_f32(v0 + vstep * k), lds_f32(xst + 4u * c));
-                            }
-                        } else {
-                            for (int k = 0; k < wi; ++k) {
-                                const unsigned c = lds_u8(c0 + (uint32_t)(k * hi));
-                                if (c < (unsigned)C)   // BF16 x BF16 is exact in FP32
-                                    acc_low(ls, lc, __fmul_rn(__uint_as_float(lds_u16(v0 + vstep * k) << 16),
-                                                              lds_f32(xst + 4u * c)));
+                // ---- compute the batch from the stage
+                tr = treg;
+                while (tr) {
+                    const int i = __ffs(tr) - 1;
+                    tr &= tr - 1u;
+                    const unsigned y = __shfl_sync(kAll, d.y, i);
+                    const unsigned mi = __shfl_sync(kAll, d.w, i);
+                    const int pi = __shfl_sync(kAll, prec, i);
+                    if (lane >= R || !((mi >> lane) & 1u)) continue;
+                    const unsigned wi = y & 0xFFu, hi = (unsigned)__popc(mi), j = (unsigned)__popc(mi & ltm);
+                    const unsigned m8 = (wi * hi + 7u) & ~7u;
+                    const uint32_t st = st0 + ((y >> 8) & 0xFFFu) * 16u;
+                    const uint32_t cst = st + 8u * m8 + j;
+                    const uint32_t xst = st + 8u * m8 + ((m8 + 15u) & ~15u);
+                    if (pi == EVOCG_FP64) {
+                        const uint32_t vst = st + 8u * j;
+                        for (unsigned k = 0; k < wi; ++k) {
+                            const unsigned c = lds_u8(cst + k * hi);
+                            if (c < (unsigned)C) {
+                                acc = fma(lds_f64(vst + 8u * k * hi), lds_f64(xst + 8u * c), acc);
+                                if (DOT) ++cnt0;
                             }
                         }
-                    }
-                    // single-entry tiles: the product on the copying lane, added by the row's lane
-                    unsigned sa = 0u, sb = 0u;
-                    if (mine && single) {
-                        const uint32_t sd = st0 + (uint32_t)lane * kSingleBytes;
-                        if (prec == EVOCG_FP64) {
-                            const double pd = lds_f64(sd) * lds_f64(sd + 8u);
-                            sa = (unsigned)__double2loint(pd);
-                            sb = (unsigned)__double2hiint(pd);
-                        } else {
-                            const unsigned wd = lds_u32(sd);
-                            const float a = prec == EVOCG_FP32 ? __uint_as_float(wd)
-                                            : __uint_as_float((s0 & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
-                            const float xv = lds_f32(sd + 8u);
-                            const float pf = __fmul_rn(a, xv);
-                            sa = __float_as_uint(pf);
-                            sb = __float_as_uint(__fmaf_rn(a, xv, -pf));   // exact remainder
+                    } else if (pi == EVOCG_FP32) {
+                        const uint32_t vst = st + 4u * j;
+                        for (unsigned k = 0; k < wi; ++k) {
+                            const unsigned c = lds_u8(cst + k * hi);
+                            if (c < (unsigned)C) {
+                                acc_prod(ls, lc, lds_f32(vst + 4u * k * hi), lds_f32(xst + 4u * c));
+                                if (DOT) ++cnt1;
+                            }
                         }
-                    }
-                    const int srow = __ffs(mk) - 1;
-                    unsigned sm = tsgl;
-                    while (sm) {
-                        const int i = __ffs(sm) - 1;
-                        sm &= sm - 1u;
-                        const unsigned a = __shfl_sync(kAll, sa, i);
-                        const unsigned b = __shfl_sync(kAll, sb, i);
-                        const int rr = __shfl_sync(kAll, srow, i);
-                        const int pi = __shfl_sync(kAll, prec, i);
-                        if (lane == rr) {
-                            if (pi == EVOCG_FP64) {
-                                acc += __hiloint2double((int)b, (int)a);
-                            } else {
-                                acc_low(ls, lc, __uint_as_float(a));
-                                lc = __fadd_rn(lc, __uint_as_float(b));
+                    } else {
+                        const uint32_t vst = st + 2u * j;
+                        for (unsigned k = 0; k < wi; ++k) {
+                            const unsigned c = lds_u8(cst + k * hi);
+                            if (c < (unsigned)C) {   // BF16 x BF16 is exact in FP32
+                                acc_low(ls, lc, __fmul_rn(__uint_as_float(lds_u16(vst + 2u * k * hi) << 16),
+                                                          lds_f32(xst + 4u * c)));
+                                if (DOT) ++cnt2;
                             }
                         }
                     }
                 }
+                // single-entry tiles: the product on the copying lane, added by the row's lane
+                unsigned sa = 0u, sb = 0u;
+                if (sgl) {
+                    const uint32_t sd = st0 + (uint32_t)lane * 16u;
+                    if (prec == EVOCG_FP64) {
+                        const double pd = lds_f64(sd) * lds_f64(sd + 8u);
+                        sa = (unsigned)__double2loint(pd);
+                        sb = (unsigned)__double2hiint(pd);
+                        if (DOT) ++cnt0;
+                    } else {
+                        const unsigned wd = lds_u32(sd);
+                        const float a = prec == EVOCG_FP32 ? __uint_as_float(wd)
+                                        : __uint_as_float((d.x & 1u) ? (wd & 0xFFFF0000u) : (wd << 16));
+                        const float xv = lds_f32(sd + 8u);
+                        const float pf = __fmul_rn(a, xv);
+                        sa = __float_as_uint(pf);
+                        sb = __float_as_uint(__fmaf_rn(a, xv, -pf));   // exact remainder
+                        if (DOT) { if (prec == EVOCG_FP32) ++cnt1; else ++cnt2; }
+                    }
+                }
+                const int srow = __ffs(d.w) - 1;
+                unsigned sm = tsgl;
+                while (sm) {
+                    const int i = __ffs(sm) - 1;
+                    sm &= sm - 1u;
+                    const unsigned a = __shfl_sync(kAll, sa, i);
+                    const unsigned b = __shfl_sync(kAll, sb, i);
+                    const int rr = __shfl_sync(kAll, srow, i);
+                    const int pi = __shfl_sync(kAll, prec, i);
+                    if (lane == rr) {
+                        if (pi == EVOCG_FP64) {
+                            acc += __hiloint2double((int)b, (int)a);
+                        } else {
+                            acc_low(ls, lc, __uint_as_float(a));
+                            lc = __fadd_rn(lc, __uint_as_float(b));
+                        }
+                    }
+                }
                 __syncwarp();   // the stage is free for the next batch
-                left &= ~take;
             }
         }
         if (nprec_pending) {
             const unsigned nnt = __shfl_sync(kAll, nwin.x, 0);
             if (lane > 0 && lane <= (int)nnt) nprec = (int)__ldg(L.prec + (int)nwin.z);
         }
-        if (rowok) {
-            double y = acc;
-            if (!FORCE64 && anylow) y = (acc + f64_from_f32(ls)) + f64_from_f32(lc);
-            L.y[row] = y;
-            if (DOT) dotp = fma(xrow, y, dotp);
+        const int64_t row = p * R + lane;
+        if (lane < R && row < A.n) {
+            double yv = acc;
+            if (!FORCE64 && anylow) yv = (acc + f64_from_f32(ls)) + f64_from_f32(lc);
+            L.y[row] = yv;
+            if (DOT) dotp = fma(__ldg(L.x64 + row), yv, dotp);
         }
         win = nwin;
         wprec = nprec;
@@ -431,58 +403,63 @@ __global__ void __launch_bounds__(kPanelThreads, MB) spmv_panel_kernel(SpmvLaunc
     }
 }
 
-template <int R, int C, int SB, int MB>
+template <int R, int C, int SB, int MB, bool IL>
 cudaError_t launch_v(const SpmvLaunch &L, cudaStream_t s)
 {
     const int grid = L.A.panel_grid;
     const size_t sm = (size_t)SB * (kPanelThreads / 32);
     if (L.force64) {
-        if (L.dot) spmv_panel_kernel<R, C, true, true, SB, MB><<<grid, kPanelThreads, sm, s>>>(L);
-        else spmv_panel_kernel<R, C, true, false, SB, MB><<<grid, kPanelThreads, sm, s>>>(L);
+        if (L.dot) spmv_panel_kernel<R, C, true, true, SB, MB, IL><<<grid, kPanelThreads, sm, s>>>(L);
+        else spmv_panel_kernel<R, C, true, false, SB, MB, IL><<<grid, kPanelThreads, sm, s>>>(L);
     } else {
-        if (L.dot) spmv_panel_kernel<R, C, false, true, SB, MB><<<grid, kPanelThreads, sm, s>>>(L);
-        else spmv_panel_kernel<R, C, false, false, SB, MB><<<grid, kPanelThreads, sm, s>>>(L);
+        if (L.dot) spmv_panel_kernel<R, C, false, true, SB, MB, IL><<<grid, kPanelThreads, sm, s>>>(L);
+        else spmv_panel_kernel<R, C, false, false, SB, MB, IL><<<grid, kPanelThreads, sm, s>>>(L);
     }
     return cudaGetLastError();
 }
 
-template <int R, int C, int SB, int MB>
+template <int R, int C, int SB, int MB, bool IL>
 int grid_v(int sms)
 {
     const int sm = SB * (kPanelThreads / 32);
-    cudaFuncSetAttribute(spmv_panel_kernel<R, C, true, true, SB, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    cudaFuncSetAttribute(spmv_panel_kernel<R, C, true, false, SB, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    cudaFuncSetAttribute(spmv_panel_kernel<R, C, false, true, SB, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-    cudaFuncSetAttribute(spmv_panel_kernel<R, C, false, false, SB, MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(spmv_panel_kernel<R, C, true, true, SB, MB, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(spmv_panel_kernel<R, C, true, false, SB, MB, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(spmv_panel_kernel<R, C, false, true, SB, MB, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+    cudaFuncSetAttribute(spmv_panel_kernel<R, C, false, false, SB, MB, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
     int per = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_panel_kernel<R, C, false, true, SB, MB>,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_panel_kernel<R, C, false, true, SB, MB, IL>,
                                                       kPanelThreads, sm) != cudaSuccess || per < 1)
         per = 1;
     cudaGetLastError();
     return sms * per;
 }
 
-// Variants: (stage bytes per warp, blocks per SM the registers are budgeted for).
+// Variants: (stage bytes per warp, blocks per SM the registers are budgeted for, panels
+// interleaved over the warps).
+#define EVOCG_PANEL_VARIANTS(X)     \
+    X(0, 4096, 8, true)             \
+    X(1, 4096, 8, false)            \
+    X(2, 4096, 6, true)             \
+    X(3, 6144, 6, true)
+
 template <int R, int C>
 cudaError_t launch_RC(const SpmvLaunch &L, cudaStream_t s)
 {
-    switch (L.A.panel_variant) {
-    case 1: return launch_v<R, C, 4096, 6>(L, s);
-    case 2: return launch_v<R, C, 3072, 10>(L, s);
-    case 3: return launch_v<R, C, 6144, 6>(L, s);
-    default: return launch_v<R, C, 4096, 8>(L, s);
-    }
+#define X(id, sb, mb, il) \
+    if (L.A.panel_variant == id) return launch_v<R, C, sb, mb, il>(L, s);
+    EVOCG_PANEL_VARIANTS(X)
+#undef X
+    return cudaErrorInvalidValue;
 }
 
 template <int R, int C>
 int grid_RC(int sms, int variant)
 {
-    switch (variant) {
-    case 1: return grid_v<R, C, 4096, 6>(sms);
-    case 2: return grid_v<R, C, 3072, 10>(sms);
-    case 3: return grid_v<R, C, 6144, 6>(sms);
-    default: return grid_v<R, C, 4096, 8>(sms);
-    }
+#define X(id, sb, mb, il) \
+    if (variant == id) return grid_v<R, C, sb, mb, il>(sms);
+    EVOCG_PANEL_VARIANTS(X)
+#undef X
+    return 0;
 }
 
 }  // namespace
@@ -495,6 +472,15 @@ cudaError_t launch_spmv_panel(const SpmvLaunch &L, cudaStream_t s)
     case 32: return launch_RC<32, 32>(L, s);
     default: return cudaErrorInvalidValue;
     }
+}
+
+int panel_stage_bytes(int variant)
+{
+#define X(id, sb, mb, il) \
+    if (variant == id) return sb;
+    EVOCG_PANEL_VARIANTS(X)
+#undef X
+    return 0;
 }
 
 int panel_grid_for(int T, int sms, int variant)

@@ -71,6 +71,24 @@ int ilog2_abs(double v)
 
 }  // namespace
 
+// Slot placement inside a row block (the SpMV copies whole 16-byte chunks of a tile's slots):
+// a tile with more than one slot starts on a multiple of 8 slots and occupies a multiple of 8
+// slots (its w x h slots, then pads), so its slice of every value stream and of the column
+// bytes starts and ends on 16-byte (BF16) or 8-byte (columns) boundaries; a single-entry tile
+// takes one slot wherever it falls; a row block's slots are a multiple of 16 (its base stays
+// 16-slot aligned). Returns where a tile of m slots starts when the row block's slots so far
+// end at pos, and sets *end to where it ends.
+int64_t place_tile(int64_t pos, int64_t m, int64_t *end)
+{
+    if (m <= 1) {
+        *end = pos + m;
+        return pos;
+    }
+    const int64_t s = (pos + 7) & ~(int64_t)7;
+    *end = s + ((m + 7) & ~(int64_t)7);
+    return s;
+}
+
 int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const double *v, int T,
                      HostTiles *out, std::string *err)
 {
@@ -162,10 +180,10 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
                 int64_t nt = 0, ns = 0;
                 walk(rb, [&](int32_t, uint64_t mask, int w, int, const int64_t *, const int64_t *) {
                     ++nt;
-                    ns += (int64_t)w * __builtin_popcountll(mask);
+                    place_tile(ns, (int64_t)w * __builtin_popcountll(mask), &ns);
                 });
                 ntile_rb[(size_t)rb] = nt;
-                nslot_rb[(size_t)rb] = ns;
+                nslot_rb[(size_t)rb] = (ns + 15) & ~(int64_t)15;
             }
         });
         H.tileRowPtr = new int64_t[(size_t)nrb + 1];
@@ -188,6 +206,11 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
         H.v32 = new float[(size_t)std::max<int64_t>(ns, 1)];
         H.v16 = new uint16_t[(size_t)std::max<int64_t>(ns, 1)];
         H.tileNnzOff[nt] = ns;
+        // slots between tiles (alignment) and after a tile's w x h rectangle: pads
+        std::memset(H.colIdx, T, (size_t)std::max<int64_t>(ns, 1));
+        std::memset(H.v64, 0, sizeof(double) * (size_t)std::max<int64_t>(ns, 1));
+        std::memset(H.v32, 0, sizeof(float) * (size_t)std::max<int64_t>(ns, 1));
+        std::memset(H.v16, 0, sizeof(uint16_t) * (size_t)std::max<int64_t>(ns, 1));
         // --- pass 2: fill the slots of every tile
         parallel_for(nrb, [&](int64_t a, int64_t b) {
             for (int64_t rb = a; rb < b; ++rb) {
@@ -195,6 +218,8 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
                 walk(rb, [&](int32_t cb, uint64_t mask, int w, int nr, const int64_t *k0,
                              const int64_t *k1) {
                     const int h = __builtin_popcountll(mask);
+                    int64_t tile_end = 0;
+                    pos = place_tile(pos, (int64_t)w * h, &tile_end);
                     H.tileColIdx[t] = cb;
                     H.tileNnzOff[t] = pos;
                     H.tileRowIdx[t] = (int32_t)rb;
@@ -225,7 +250,7 @@ int build_host_tiles(int64_t n, const int64_t *rp, const int32_t *ci, const doub
                         }
                         ++j;
                     }
-                    pos += (int64_t)w * h;
+                    pos = tile_end;
                     ++t;
                 });
             }

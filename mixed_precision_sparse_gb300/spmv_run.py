@@ -8,8 +8,9 @@ For each workload: build the tile structure, set the seeded 40/40/20 per-tile ma
 all-FP64 map), and launch the SpMV kernel back to back on device-resident x and y (every
 workload's matrix streams are larger than L2 except the 64 x 64 Laplacian's), timed with
 CUDA events on the launching stream. Prints one JSON line per (workload, map) with the
-microseconds per launch and the algorithmic bytes of the launch (the active value stream of
-each tile, the index bytes, x read once and y written once).
+microseconds per launch and the algorithmic bytes of the launch over EvoCG's Tile-CSC layout
+(the active value stream of each tile, the row indices, column pointers and descriptors, x
+read once and y written once).
 
 `--launches K` skips the timing and issues exactly K SpMV launches after one x-copy launch,
 for use under a profiler.
@@ -30,13 +31,14 @@ from mixed_precision_sparse_gb300 import evocg  # noqa: E402
 from mixed_precision_sparse_gb300 import workloads as W  # noqa: E402
 
 
-def spmv_bytes(n, ntiles, nrb, nnz_by_prec):
-    """Algorithmic bytes of one SpMV launch: the active value stream of every stored entry
-    (pads not counted), one local-column byte per entry, per tile its column block (4),
-    first slot (8), row mask (8), width (1) and precision code (1), the row-block
-    pointers, x read once and y written once."""
+def spmv_bytes(n, ntiles, nrb, nnz_by_prec, T):
+    """Algorithmic bytes of one SpMV launch over EvoCG's Tile-CSC layout: the active value
+    stream of every stored entry (sentinels not counted), one row-index byte per entry, per
+    tile its column pointers (2(T+1) bytes) and a 12-byte descriptor, the tile row pointers,
+    x read once and y written once."""
     vals = 8 * int(nnz_by_prec[0]) + 4 * int(nnz_by_prec[1]) + 2 * int(nnz_by_prec[2])
-    return vals + int(sum(nnz_by_prec)) + 22 * int(ntiles) + 8 * (int(nrb) + 1) + 16 * int(n)
+    return (vals + int(sum(nnz_by_prec)) + (2 * (int(T) + 1) + 12) * int(ntiles) +
+            8 * (int(nrb) + 1) + 16 * int(n))
 
 
 def tile_entries(ex, T):
@@ -99,7 +101,7 @@ def main(argv=None):
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1000.0 / a.reps
             per = np.bincount(mp, weights=tnnz, minlength=3).astype(np.int64)
-            B = spmv_bytes(G.n, G.ntiles, G.nrb, per)
+            B = spmv_bytes(G.n, G.ntiles, G.nrb, per, G.T)
             print(json.dumps({"workload": w.name, "map": label,
                               "kernel": a.kernel, "n": w.n, "nnz": w.nnz,
                               "ntiles": int(G.ntiles), "us": round(us, 2), "bytes": B,

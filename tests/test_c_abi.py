@@ -46,7 +46,20 @@ def test_layout_from_c_matches_the_oracle(c_output):
     nrows = np.bincount(rt // n, minlength=tile.max() + 1)
     assert got["widest"] == int(width.max())
     assert int(c_output["rows_in_masks"][0]) == rt.size
-    assert got["nslots"] == int((width * nrows).sum())
+    # slots: a tile of m > 1 slots starts on a multiple of 8 and takes m rounded up to 8; a
+    # single-entry tile takes one slot; each row block's slots are rounded up to 16
+    m = width * nrows
+    nrb = (n + T - 1) // T
+    slots = 0
+    for rb in range(nrb):
+        pos = 0
+        for tt in range(rb * nrb, (rb + 1) * nrb):
+            if tt < m.size and m[tt] > 1:
+                pos = (pos + 7) // 8 * 8 + (m[tt] + 7) // 8 * 8
+            elif tt < m.size:
+                pos += m[tt]
+        slots += (pos + 15) // 16 * 16
+    assert got["nslots"] == slots
 
 
 def test_plan_and_kstar_from_c(c_output):

@@ -67,13 +67,22 @@ def test_host_tile_csc_fig4b():
 
 def slot_layout_holds_the_csr(h, n, rp, ci, v, T):
     """The kernels' slot-major interior (row mask, width, w x h slots, pads at local column T)
-    rebuilt into CSR with numpy equals the input; every pad is +0 in all three streams."""
+    rebuilt into CSR with numpy equals the input; every pad is +0 in all three streams. A tile
+    with more than one slot starts on a multiple of 8 slots and is followed by pads up to a
+    multiple of 8; every row block's slots start on a multiple of 16."""
     rows, cols, vals = [], [], []
     trow = np.repeat(np.arange(len(h["tileRowPtr"]) - 1), np.diff(h["tileRowPtr"]))
+    first = h["tileNnzOff"][h["tileRowPtr"][:-1][np.diff(h["tileRowPtr"]) > 0]]
+    assert np.all(first % 16 == 0)
+    real = np.zeros(h["nslots"], bool)
     for t in range(h["ntiles"]):
         m, w, off = int(h["rowMask"][t]), int(h["tileWidth"][t]), int(h["tileNnzOff"][t])
         rr = [r for r in range(T) if (m >> r) & 1]
-        assert h["tileNnzOff"][t + 1] - off == w * len(rr)
+        if w * len(rr) > 1:
+            assert off % 8 == 0 and h["tileNnzOff"][t + 1] - off >= (w * len(rr) + 7) // 8 * 8
+        else:
+            assert h["tileNnzOff"][t + 1] - off >= 1
+        real[off:off + w * len(rr)] = True
         for k in range(w):
             for j, r in enumerate(rr):
                 s = off + k * len(rr) + j
@@ -83,6 +92,8 @@ def slot_layout_holds_the_csr(h, n, rp, ci, v, T):
                 rows.append(trow[t] * T + r)
                 cols.append(int(h["tileColIdx"][t]) * T + int(h["colIdx"][s]))
                 vals.append(h["v64"][s])
+    gaps = ~real            # slots outside every tile's rectangle: pads
+    assert np.all(h["colIdx"][gaps] == T) and np.all(h["v64"][gaps] == 0) and np.all(h["v16"][gaps] == 0)
     rows, cols, vals = np.array(rows), np.array(cols), np.array(vals)
     o = np.lexsort((cols, rows))
     assert np.array_equal(cols[o], ci) and np.array_equal(vals[o].view(np.uint64), np.asarray(v).view(np.uint64))
