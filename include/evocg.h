@@ -197,20 +197,20 @@ int evocg_tiles_export_csc(evocg_tiles_t A, int pad, int64_t *nnz_p, int64_t *ti
                            int8_t *colExp);
 
 /*
- * The staged SpMV's static work plan for a matrix, computed on the HOST only (no GPU), for
- * inspection. The paper has no counterpart: the plan belongs to this library's SpMV kernel
- * (batches of tiles staged in shared memory). The same builder and planner evocg_tile_build
- * runs, for `warps` consumer
- * warps (the library plans for its grid times the consumer warps of a block).
+ * The panel SpMV's batch plan for a matrix, computed on the HOST only (no GPU), for inspection.
+ * The paper has no counterpart: the plan belongs to this library's SpMV kernel. The same
+ * builder and planner evocg_tile_build runs cut every 32-row panel's tiles into batches that
+ * fit a shared-memory stage of stage_bytes (each tile sized for FP64), for `warps` warps
+ * walking contiguous panel ranges.
  *   *nbatches receives the number of batches; *valid 1 when the plan passes the checks the
- *   library applies before using it (warp ranges tiling the row blocks, batches covering
- *   each warp's tiles in order, every batch inside a stage), 0 when the library would run
- *   the direct kernel instead. Either pointer may be NULL.
- * Errors: as evocg_tile_build; EINVAL for warps < 1 or a tile size without a staged kernel.
+ *   library applies before using it (every record matching the tile structure, tile slices
+ *   16-byte aligned inside the streams, every batch inside its stage), 0 when the library would
+ *   run the direct kernel instead (the reason is in evocg_last_error). Either may be NULL.
+ * Errors: as evocg_tile_build; EINVAL for warps < 1 or stage_bytes < 1.
  */
-int evocg_staged_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
-                           const double *vals, int tile_size, int64_t warps, int64_t *nbatches,
-                           int *valid);
+int evocg_panel_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                          const double *vals, int tile_size, int64_t warps, int stage_bytes,
+                          int64_t *nbatches, int *valid);
 
 /*
  * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
@@ -243,22 +243,18 @@ enum {
                                      handle; x must hold the same values as in that call */
     EVOCG_SPMV_DIRECT = 2,        /* run the direct kernel: a warp per row block, every operand
                                      loaded by the lanes from global memory, one tile after
-                                     the other */
-    EVOCG_SPMV_STAGED = 4,        /* run the staged kernel (the default where it can run): a
-                                     producer warp copies each tile's value slice and x segment
-                                     into shared memory by bulk asynchronous copies for two
-                                     consumer warps (needs 16-byte aligned x; the direct kernel
-                                     runs otherwise). Both kernels sum every row in ascending
-                                     column with the same arithmetic; for tiles of 32 and 64
-                                     they give the same bits; for tiles of 16 the direct kernel
-                                     splits a row block's tiles over two half-warps (same sums
-                                     to rounding). At most one of DIRECT, STAGED, PANEL may be
-                                     set */
-    EVOCG_SPMV_PANEL = 8          /* run the panel kernel (tiles of 16 or 32): a warp streams the
-                                     tile descriptors of consecutive row blocks and keeps several
-                                     tiles' loads in flight; single-entry tiles take one lane
-                                     each. Low-precision products are summed in FP32 pairs and
-                                     folded into the FP64 row sum once per row */
+                                     the other (the kernel for tiles of 64). At most one of
+                                     DIRECT, PANEL may be set */
+    EVOCG_SPMV_PANEL = 8,         /* run the panel kernel (the default for tiles of 16 and 32):
+                                     a warp streams batches of tiles of consecutive row blocks
+                                     through two shared-memory stages, every tile's own lane
+                                     issuing its bulk copies; single-entry tiles take one lane
+                                     each */
+    EVOCG_SPMV_TEST_LOST_WAIT = 16 /* test hook of the panel kernel: one warp withholds its first
+                                     stage arrival and waits 2 ms instead of 2 s, so that the
+                                     path of a lost stage wait runs; the call must then return
+                                     EVOCG_ETIMEOUT (host pointers) and the handle's error word
+                                     is cleared by that report */
 };
 
 /*

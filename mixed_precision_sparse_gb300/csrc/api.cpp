@@ -5,6 +5,8 @@
 // conditional while node, so no host round trip happens per iteration).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -275,7 +277,7 @@ bool graphs_enabled()
 
 // --------------------------------------------------------------------------------------
 
-extern "C" int evocg_version(void) { return 1; }
+extern "C" int evocg_version(void) { return 2; }
 
 extern "C" const char *evocg_last_error(void) { return g_err.c_str(); }
 
@@ -319,34 +321,6 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
     up(&A->v16, H.v16, H.nslots);
     up(&A->colExp, H.colExp, H.n);
     up(&A->dinv, H.dinv, H.n);
-    // The staged kernel pays a fixed issue cost per batch of tiles and stages each tile's
-    // whole x segment; for sparse tiles (banded matrices: a handful of entries per 64 x 64
-    // tile) the direct kernel is faster, so the staged plan is built only when tiles hold
-    // on average at least kStagedMinEntries entries.
-    constexpr int64_t kStagedMinEntries = 12;
-    StagedLimits lim;
-    if (e == cudaSuccess && H.nrb > 0 && H.nslots >= kStagedMinEntries * H.ntiles && staged_limits(H.T, &lim)) {
-        const int grid = staged_grid_for(H.T, sms);
-        if (grid > 0) {
-            std::vector<int32_t> wr, wbt;
-            std::vector<int64_t> bt;
-            std::vector<uint16_t> slot;
-            staged_plan(H, (int64_t)grid * lim.warps_per_block, lim, &wr, &wbt, &bt, &slot);
-            bool small = staged_plan_ok(H, (int64_t)grid * lim.warps_per_block, lim, wr, wbt, bt, slot);
-            // the kernel uses 32-bit entry offsets inside a warp
-            for (size_t w = 0; w + 1 < wr.size() && small; ++w)
-                small = H.tileNnzOff[H.tileRowPtr[wr[w + 1]]] - H.tileNnzOff[H.tileRowPtr[wr[w]]] <
-                        (1ll << 28) - 64;
-            if (small) {
-            up(&A->warpRb, wr.data(), (int64_t)wr.size());
-            up(&A->warpBatch, wbt.data(), (int64_t)wbt.size());
-            up(&A->batchTile, bt.data(), (int64_t)bt.size());
-            up(&A->tileSlot, slot.data(), (int64_t)slot.size());
-            A->nbatches = (int64_t)bt.size() - 1;
-            A->staged_grid = grid;
-            }
-        }
-    }
     // panel SpMV plan (tiles of 16 or 32)
     if (e == cudaSuccess && H.nrb > 0) {
         int variant = 0;
@@ -354,18 +328,30 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
         if (variant < 0 || variant >= kPanelVariants) variant = 0;
         const int pg = panel_grid_for(H.T, sms, variant);
         if (pg > 0) {
-            std::vector<uint4> pd;
-            std::vector<int64_t> wrec;
-            std::vector<int32_t> wpan;
+            PanelPlan pl;
             std::string why;
             const int64_t warps = (int64_t)pg * (kPanelThreads / 32);
             const int sb = panel_stage_bytes(variant);
-            if (panel_plan(H, warps, sb, &pd, &wrec, &wpan, &why) &&
-                panel_plan_ok(H, warps, sb, pd, wrec, wpan, &why)) {
+            if (panel_plan(H, warps, sb, &pl, &why) && panel_plan_ok(H, warps, sb, pl, &why) &&
+                pl.panelRec.back() < INT32_MAX) {
                 A->panel_variant = variant;
-                up(&A->pdesc, pd.data(), (int64_t)pd.size());
-                up(&A->warpRec, wrec.data(), (int64_t)wrec.size());
-                up(&A->warpPanel, wpan.data(), (int64_t)wpan.size());
+                A->nrec = pl.panelRec.back();
+                try {   // every tile's record, for the record-ordered precision map
+                    A->tileRec.assign((size_t)std::max<int64_t>(H.ntiles, 1), 0);
+                    int64_t t = 0;
+                    for (int64_t r = 0; r < A->nrec;) {
+                        const int64_t nt = pl.desc[(size_t)r].x & 0xFFu;
+                        for (int64_t i = 1; i <= nt; ++i) A->tileRec[(size_t)t++] = (int32_t)(r + i);
+                        r += 1 + nt;
+                    }
+                } catch (const std::bad_alloc &) {
+                    e = cudaErrorMemoryAllocation;
+                }
+                up(&A->pdesc, pl.desc.data(), (int64_t)pl.desc.size());
+                up(&A->warpRec, pl.warpRec.data(), (int64_t)pl.warpRec.size());
+                up(&A->panelRec, pl.panelRec.data(), (int64_t)pl.panelRec.size());
+                if (e == cudaSuccess) e = dalloc(&A->recPrec, A->nrec + 32);
+                if (e == cudaSuccess) e = cudaMemset(A->recPrec, 0, (size_t)(A->nrec + 32));
                 A->panel_grid = pg;
             }
         }
@@ -386,14 +372,12 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
         return code;
     }
     A->spmv_grid = spmv_grid_for(A->T, sms);
-    // Default kernel: the staged one where its plan exists and x is aligned, else the
-    // direct one; EVOCG_SPMV_KERNEL=direct selects the direct kernel for every SpMV of the
-    // matrices built afterwards.
+    // Default kernel: the panel kernel where its plan exists, else the direct one;
+    // EVOCG_SPMV_KERNEL=direct selects the direct kernel for every SpMV of the matrices built
+    // afterwards.
     A->spmv_kind = SPMV_KIND_AUTO;
-    if (const char *k = std::getenv("EVOCG_SPMV_KERNEL")) {
+    if (const char *k = std::getenv("EVOCG_SPMV_KERNEL"))
         if (!std::strcmp(k, "direct")) A->spmv_kind = SPMV_KIND_DIRECT;
-        if (!std::strcmp(k, "panel")) A->spmv_kind = SPMV_KIND_PANEL;
-    }
     A->vec_grid = sms * 4 > kMaxBlocks ? kMaxBlocks : sms * 4;
     *out = A;
     return EVOCG_OK;
@@ -405,8 +389,8 @@ extern "C" int evocg_tiles_free(evocg_tiles_t A)
     cudaDeviceSynchronize();
     release_ws(A->ws);
     dfree(A->tileRowPtr); dfree(A->tileColIdx); dfree(A->tileNnzOff); dfree(A->tileRowIdx);
-    dfree(A->rowMask); dfree(A->tileWidth); dfree(A->warpRb); dfree(A->warpBatch); dfree(A->batchTile);
-    dfree(A->tileSlot); dfree(A->errw); dfree(A->pdesc); dfree(A->warpRec); dfree(A->warpPanel);
+    dfree(A->rowMask); dfree(A->tileWidth);
+    dfree(A->errw); dfree(A->pdesc); dfree(A->warpRec); dfree(A->panelRec); dfree(A->recPrec);
     dfree(A->colIdx); dfree(A->v64); dfree(A->v32); dfree(A->v16); dfree(A->colExp);
     dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16f);
     dfree(A->xstage); dfree(A->ystage);
@@ -479,6 +463,12 @@ extern "C" int evocg_set_tile_precision(evocg_tiles_t A, const uint8_t *map, int
                                               " at " + std::to_string(i) + " (codes are 0, 1, 2)");
         uint8_t *dst = (map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
         CK(cudaMemcpyAsync(dst, h.data(), (size_t)len, cudaMemcpyHostToDevice, s), "upload map");
+        std::vector<uint8_t> rp;
+        if (map_kind == EVOCG_MAP_PER_TILE && A->recPrec) {   // the same map in record order
+            rp.assign((size_t)(A->nrec + 32), 0);
+            for (int64_t t = 0; t < len; ++t) rp[(size_t)A->tileRec[(size_t)t]] = h[(size_t)t];
+            CK(cudaMemcpyAsync(A->recPrec, rp.data(), rp.size(), cudaMemcpyHostToDevice, s), "upload map");
+        }
         CK(cudaStreamSynchronize(s), "synchronise");
     }
     A->map_kind = map_kind;
@@ -510,8 +500,8 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
 {
     g_err.clear();
     if (!A || (A->n > 0 && (!x || !y))) return fail(EVOCG_EINVAL, "NULL argument");
-    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED | EVOCG_SPMV_PANEL);
-    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_STAGED | EVOCG_SPMV_PANEL))
+    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL);
+    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL | EVOCG_SPMV_TEST_LOST_WAIT))
         return fail(EVOCG_EINVAL, "unknown flags");
     if (kflags & (kflags - 1)) return fail(EVOCG_EINVAL, "at most one kernel flag");
     if (A->n == 0) return EVOCG_OK;
@@ -545,7 +535,8 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     S.map_kind = A->map_kind;
     S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
     S.direct = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
-    S.kind = (flags & EVOCG_SPMV_STAGED) ? SPMV_KIND_STAGED : (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : 0;
+    S.kind = (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : 0;
+    S.test_lost_wait = (flags & EVOCG_SPMV_TEST_LOST_WAIT) ? 1 : 0;
     CK(launch_spmv(S, s), "launch spmv");
     if (!ydev) {
         int lost = 0;
@@ -555,7 +546,7 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
         if (lost) {
             cudaMemsetAsync(A->errw, 0, sizeof(int), s);
             cudaStreamSynchronize(s);
-            return fail(EVOCG_ETIMEOUT, "an SpMV stage wait ran out (bulk copies did not complete)");
+            return fail(EVOCG_ETIMEOUT, "an SpMV stage wait ran out (its bulk copies did not complete)");
         }
     }
     return EVOCG_OK;

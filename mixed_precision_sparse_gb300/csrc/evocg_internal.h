@@ -18,8 +18,7 @@ constexpr int kUpdMinBlocks = 3;      // resident blocks per SM of the CG update
 constexpr int kSpmvThreads = 256;     // threads per block of the SpMV
 constexpr int kSpmvMinBlocks = 4;     // resident blocks per SM the SpMV registers are budgeted for
 constexpr int kMlpHiddenMax = 64;
-constexpr int kStages = 5;            // tile slots per warp in the SpMV's shared-memory ring
-constexpr int kSlack = 16;            // bytes past the end of every staged array
+constexpr int kSlack = 16;            // bytes past the end of every device array (16-byte copies)
 constexpr int kPanelThreads = 128;    // threads per block of the panel SpMV
 constexpr int kPanelVariants = 4;     // (tiles issued together, blocks per SM) variants built
 
@@ -62,50 +61,24 @@ struct TilesView {
     const float *v32;
     const uint16_t *v16;
     const int8_t *colExp;
-    // staged SpMV plan (NULL warpRb = direct kernel only): row-block range and batch range
-    // of every warp (warps + 1 entries each), first tile of every batch (batches + 1), the
-    // shared-memory slot of every tile inside its batch's stage (kDirectSlot: a tile too
-    // large for a stage), the staged grid, and the error word a lost stage wait sets
-    const int32_t *warpRb;
-    const int32_t *warpBatch;
-    const int64_t *batchTile;
-    const uint16_t *tileSlot;
-    int staged_grid;
-    int *err;
+    int *err;          // error word: a panel-kernel stage wait that ran out sets it
     int spmv_kind;     // kernel launch_spmv runs by default (SPMV_KIND_*)
-    // panel SpMV: descriptor stream, first record and first panel of every warp (warps + 1
-    // entries each), and the grid the plan was made for (0: no plan)
+    // panel SpMV: batch stream (panel_plan.cpp), the first batch record of every warp's
+    // contiguous range (warps + 1) and of every panel (nrb + 1), and the grid the plan was made
+    // for (0: no plan)
     const uint4 *pdesc;
     const int64_t *warpRec;
-    const int32_t *warpPanel;
+    const int64_t *panelRec;
+    const uint8_t *recPrec;   // a per-tile precision map in record order (0 at headers)
+    int64_t nrec;             // records of the stream before its 32 closing records
     int panel_grid;
     int panel_variant;
 };
 
-// SpMV kernels: the direct kernel (warp per row block, global loads) and the staged kernel
-// (operands in shared memory by bulk asynchronous copies). AUTO: staged when it can run.
-enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_STAGED = 2, SPMV_KIND_PANEL = 3 };
-
-constexpr uint16_t kDirectSlot = 0xFFFF;
-
-// Capacities of one stage of the staged SpMV for tile size T (spmv_staged.cu).
-struct StagedLimits {
-    int warps_per_block;
-    int nb;          // tiles per batch
-    int col_bytes;   // local-column bytes
-    int data_bytes;  // value slices + x segments
-};
-bool staged_limits(int T, StagedLimits *out);
-
-// Worst-case stage bytes of a tile with m slots: the 16-byte cover of its value slice in
-// any precision (at most 8m + 8 bytes before rounding) followed by its x segment in FP64.
-#ifdef __CUDACC__
-__host__ __device__
-#endif
-inline int staged_slot_bytes(int64_t m, int T)
-{
-    return (int)(((8 * m + 8 + 15) / 16) * 16) + 8 * T;
-}
+// SpMV kernels: the panel kernel (spmv_panel.cu; tiles of 16 and 32) and the direct kernel
+// (spmv.cu: warp per row block, global loads; tiles of 64, or no panel plan). AUTO: the panel
+// kernel when its plan exists.
+enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_PANEL = 3 };
 
 struct SolveWS {
     int64_t cap_n = 0, cap_ncb = 0;
@@ -148,15 +121,12 @@ struct evocg_tiles {
     float *v32 = nullptr;
     uint16_t *v16 = nullptr;
     int8_t *colExp = nullptr;
-    int32_t *warpRb = nullptr;     // staged SpMV plan (see TilesView)
-    int32_t *warpBatch = nullptr;
-    int64_t *batchTile = nullptr;
-    uint16_t *tileSlot = nullptr;
-    int64_t nbatches = 0;
-    int staged_grid = 0;
     uint4 *pdesc = nullptr;        // panel SpMV plan (see TilesView)
     int64_t *warpRec = nullptr;
-    int32_t *warpPanel = nullptr;
+    int64_t *panelRec = nullptr;
+    uint8_t *recPrec = nullptr;
+    int64_t nrec = 0;
+    std::vector<int32_t> tileRec;  // host: the record of every tile (for recPrec)
     int panel_grid = 0;
     int panel_variant = 0;
     int *errw = nullptr;           // device error word (a lost stage wait)
@@ -178,8 +148,7 @@ struct evocg_tiles {
     {
         return evocg::TilesView{n, nrb, ntiles, nslots, T, tileRowPtr, tileColIdx, tileNnzOff,
                                 tileRowIdx, rowMask, tileWidth, colIdx, v64, v32, v16, colExp,
-                                warpRb, warpBatch, batchTile, tileSlot, staged_grid, errw,
-                                spmv_kind, pdesc, warpRec, warpPanel, panel_grid, panel_variant};
+                                errw, spmv_kind, pdesc, warpRec, panelRec, recPrec, nrec, panel_grid, panel_variant};
     }
 };
 
@@ -233,33 +202,26 @@ struct SpmvLaunch {
     int grid;              // grid of the direct kernel
     int direct;            // 1: the direct kernel whatever the default
     int kind;              // SPMV_KIND_*: a kernel other than the matrix's default (0: default)
+    int test_lost_wait;    // test hook of the panel kernel: one warp withholds its first stage
+                           // arrival and waits 2 ms, so that the lost-wait path runs
 };
-// Kernel choice: L.direct, else L.kind, else the matrix's default; the staged kernel only
-// when the view has its plan and every x operand is 16-byte aligned (else the direct one).
+// Kernel choice: L.direct, else L.kind, else the matrix's default; the panel kernel only when
+// the view has its plan (else the direct one).
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
 cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s);
 int spmv_dot_partials(const SpmvLaunch &L);   // warps that write a p.q partial
-cudaError_t launch_spmv_staged(const SpmvLaunch &L, cudaStream_t s);
 cudaError_t launch_spmv_panel(const SpmvLaunch &L, cudaStream_t s);
 int panel_grid_for(int T, int sms, int variant);   // 0 if no panel kernel exists for T
 int panel_stage_bytes(int variant);                // shared-memory stage of one warp
-bool panel_plan(const HostTiles &H, int64_t warps, int stage_bytes, std::vector<uint4> *desc,
-                std::vector<int64_t> *warpRec, std::vector<int32_t> *warpPanel, std::string *why);
-bool panel_plan_ok(const HostTiles &H, int64_t warps, int stage_bytes, const std::vector<uint4> &desc,
-                   const std::vector<int64_t> &warpRec, const std::vector<int32_t> &warpPanel,
-                   std::string *why);
+struct PanelPlan {
+    std::vector<uint4> desc;        // the batch stream
+    std::vector<int64_t> warpRec;   // warps + 1
+    std::vector<int64_t> panelRec;  // nrb + 1
+    uint32_t batches = 0;
+};
+bool panel_plan(const HostTiles &H, int64_t warps, int stage_bytes, PanelPlan *out, std::string *why);
+bool panel_plan_ok(const HostTiles &H, int64_t warps, int stage_bytes, const PanelPlan &pl, std::string *why);
 
-int staged_grid_for(int T, int sms);   // 0 if it cannot run
-int staged_warps_per_block(int T);      // consumer warps (the ones with rows) per block
-
-// Host: the staged SpMV plan for `warps` warps (staged_plan.cpp), and its check against
-// what the kernel assumes of it.
-void staged_plan(const HostTiles &H, int64_t warps, const StagedLimits &lim,
-                 std::vector<int32_t> *warpRb, std::vector<int32_t> *warpBatch,
-                 std::vector<int64_t> *batchTile, std::vector<uint16_t> *tileSlot);
-bool staged_plan_ok(const HostTiles &H, int64_t warps, const StagedLimits &lim,
-                    const std::vector<int32_t> &wr, const std::vector<int32_t> &wbt,
-                    const std::vector<int64_t> &bt, const std::vector<uint16_t> &slot);
 cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, float *x16f,
                            int grid, cudaStream_t s);
 cudaError_t launch_round(const double *x, int64_t n, float *o32, uint16_t *o16, cudaStream_t s);

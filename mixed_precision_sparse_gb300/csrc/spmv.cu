@@ -1,6 +1,8 @@
-// spmv.cu -- the tile-wise mixed-precision SpMV (EvoCG, "Self-Evolving Precision Control
-// for Faster Conjugate Gradient", §3.3 EvoSpMV, Eq. 2 / Eq. 5) for sm_103a, its launchers,
-// the rounded x copies it reads, and the device rounding entry point.
+// spmv.cu -- the direct tile-wise mixed-precision SpMV (EvoCG, "Self-Evolving Precision
+// Control for Faster Conjugate Gradient", §3.3 EvoSpMV, Eq. 2 / Eq. 5) for sm_103a, the kernel
+// choice, the rounded x copies the SpMV reads, and the device rounding entry point. The
+// panel kernel (spmv_panel.cu) runs wherever its plan exists (tiles of 16 and 32); this
+// kernel runs the rest (tiles of 64) and on request.
 //
 // Work mapping. A warp owns a row block (T rows) at a time and walks its tiles in
 // ascending column block, so every row is summed in column order. Lane l owns local row
@@ -196,19 +198,13 @@ static int chosen_kind(const SpmvLaunch &L)
 {
     if (L.direct) return SPMV_KIND_DIRECT;
     const int k = L.kind ? L.kind : L.A.spmv_kind;
-    if (k == SPMV_KIND_PANEL && L.A.pdesc && L.A.panel_grid > 0) return SPMV_KIND_PANEL;
-    if (k == SPMV_KIND_STAGED || k == SPMV_KIND_AUTO) {
-        const auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-        if (L.A.warpRb && L.A.staged_grid > 0 && al(L.x64) && (L.force64 || (al(L.x32) && al(L.x16f))))
-            return SPMV_KIND_STAGED;
-    }
+    if ((k == SPMV_KIND_PANEL || k == SPMV_KIND_AUTO) && L.A.pdesc && L.A.panel_grid > 0) return SPMV_KIND_PANEL;
     return SPMV_KIND_DIRECT;
 }
 
 int spmv_dot_partials(const SpmvLaunch &L)
 {
     switch (chosen_kind(L)) {
-    case SPMV_KIND_STAGED: return L.A.staged_grid * staged_warps_per_block(L.A.T);
     case SPMV_KIND_PANEL: return L.A.panel_grid * (kPanelThreads / 32);
     default: return L.grid * (kSpmvThreads / 32);
     }
@@ -216,15 +212,9 @@ int spmv_dot_partials(const SpmvLaunch &L)
 
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
 {
-    SpmvLaunch S = L;
     switch (chosen_kind(L)) {
-    case SPMV_KIND_STAGED:
-        S.grid = L.A.staged_grid;
-        return launch_spmv_staged(S, s);
-    case SPMV_KIND_PANEL:
-        return launch_spmv_panel(S, s);
-    default:
-        return launch_spmv_direct(L, s);
+    case SPMV_KIND_PANEL: return launch_spmv_panel(L, s);
+    default: return launch_spmv_direct(L, s);
     }
 }
 

@@ -71,21 +71,21 @@ int ilog2_abs(double v)
 
 }  // namespace
 
-// Slot placement inside a row block (the SpMV copies whole 16-byte chunks of a tile's slots):
-// a tile with more than one slot starts on a multiple of 8 slots and occupies a multiple of 8
-// slots (its w x h slots, then pads), so its slice of every value stream and of the column
-// bytes starts and ends on 16-byte (BF16) or 8-byte (columns) boundaries; a single-entry tile
-// takes one slot wherever it falls; a row block's slots are a multiple of 16 (its base stays
-// 16-slot aligned). Returns where a tile of m slots starts when the row block's slots so far
-// end at pos, and sets *end to where it ends.
+// Slot placement inside a row block (the SpMV moves a tile's slots with bulk copies, which
+// need 16-byte aligned addresses and sizes): a tile with more than one slot starts on a
+// multiple of 16 slots and occupies a multiple of 16 slots (its w x h slots, then pads), so
+// its slice of every value stream and of the column bytes starts and ends on a 16-byte
+// boundary; a single-entry tile takes one slot wherever it falls; a row block's slots are a
+// multiple of 16 (its base stays 16-slot aligned). Returns where a tile of m slots starts
+// when the row block's slots so far end at pos, and sets *end to where it ends.
 int64_t place_tile(int64_t pos, int64_t m, int64_t *end)
 {
     if (m <= 1) {
         *end = pos + m;
         return pos;
     }
-    const int64_t s = (pos + 7) & ~(int64_t)7;
-    *end = s + ((m + 7) & ~(int64_t)7);
+    const int64_t s = (pos + 15) & ~(int64_t)15;
+    *end = s + ((m + 15) & ~(int64_t)15);
     return s;
 }
 

@@ -110,8 +110,8 @@ def lib():
                                        C.POINTER(C.c_int)],
                 "evocg_tile_layout_host": [i64, P, P, P, i32, C.POINTER(C.c_int64),
                                            C.POINTER(C.c_int64)] + [P] * 10,
-                "evocg_staged_plan_host": [i64, P, P, P, i32, i64, C.POINTER(C.c_int64),
-                                           C.POINTER(C.c_int)],
+                "evocg_panel_plan_host": [i64, P, P, P, i32, i64, i32, C.POINTER(C.c_int64),
+                                          C.POINTER(C.c_int)],
                 "evocg_tile_csc_host": [i64, P, P, P, i32, i32, C.POINTER(C.c_int64),
                                         C.POINTER(C.c_int64)] + [P] * 9,
                 "evocg_tiles_export_csc": [P, i32, C.POINTER(C.c_int64)] + [P] * 9,
@@ -285,12 +285,13 @@ def tile_layout_host(n, row_ptr, col_idx, vals, tile_size: int) -> dict:
     return out
 
 
-def staged_plan_host(n, row_ptr, col_idx, vals, tile_size: int, warps: int):
-    """(batches, valid) of the staged SpMV's plan for `warps` consumer warps, on the host."""
+def panel_plan_host(n, row_ptr, col_idx, vals, tile_size: int, warps: int, stage_bytes: int = 4096):
+    """(batches, valid) of the panel SpMV's plan for `warps` warps and stages of stage_bytes,
+    on the host."""
     rp, ci, v = _np(row_ptr, np.int64), _np(col_idx, np.int32), _np(vals, np.float64)
     nb, ok = C.c_int64(), C.c_int()
-    _check(lib().evocg_staged_plan_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), int(tile_size),
-                                        int(warps), C.byref(nb), C.byref(ok)))
+    _check(lib().evocg_panel_plan_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), int(tile_size),
+                                       int(warps), int(stage_bytes), C.byref(nb), C.byref(ok)))
     return nb.value, bool(ok.value)
 
 
@@ -308,8 +309,8 @@ def get_tile_precision(A: Tiles, stream=None):
 
 SPMV_REUSE_XCOPIES = 1
 SPMV_DIRECT = 2
-SPMV_STAGED = 4
 SPMV_PANEL = 8
+SPMV_TEST_LOST_WAIT = 16
 
 
 def spmv(A: Tiles, x, y, stream=None):

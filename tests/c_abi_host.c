@@ -1,5 +1,5 @@
 /* A plain C caller of the library's host-only entry points (no GPU needed): the tile layout
- * of a small 2D Laplacian, the staged SpMV's plan check, the reuse-interval choice of a
+ * of a small 2D Laplacian, the panel SpMV's plan check, the reuse-interval choice of a
  * decision log, and an error path with its message. Prints one line per result; exits
  * non-zero on the first unexpected status. Built and run by tests/test_c_abi.py. */
 #include <stdio.h>
@@ -59,7 +59,7 @@ int main(void)
 
     int64_t nb = 0;
     int ok = 0;
-    if (check(evocg_staged_plan_host(n, rp, ci, v, 16, 8, &nb, &ok), EVOCG_OK, "plan"))
+    if (check(evocg_panel_plan_host(n, rp, ci, v, 16, 8, 4096, &nb, &ok), EVOCG_OK, "plan"))
         return 1;
     printf("plan batches %lld valid %d\n", (long long)nb, ok);
 

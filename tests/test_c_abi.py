@@ -46,7 +46,7 @@ def test_layout_from_c_matches_the_oracle(c_output):
     nrows = np.bincount(rt // n, minlength=tile.max() + 1)
     assert got["widest"] == int(width.max())
     assert int(c_output["rows_in_masks"][0]) == rt.size
-    # slots: a tile of m > 1 slots starts on a multiple of 8 and takes m rounded up to 8; a
+    # slots: a tile of m > 1 slots starts on a multiple of 16 and takes m rounded up to 16; a
     # single-entry tile takes one slot; each row block's slots are rounded up to 16
     m = width * nrows
     nrb = (n + T - 1) // T
@@ -55,7 +55,7 @@ def test_layout_from_c_matches_the_oracle(c_output):
         pos = 0
         for tt in range(rb * nrb, (rb + 1) * nrb):
             if tt < m.size and m[tt] > 1:
-                pos = (pos + 7) // 8 * 8 + (m[tt] + 7) // 8 * 8
+                pos = (pos + 15) // 16 * 16 + (m[tt] + 15) // 16 * 16
             elif tt < m.size:
                 pos += m[tt]
         slots += (pos + 15) // 16 * 16

@@ -66,10 +66,20 @@ def test_cg_mixed_static_map_laplacian():
     assert list(info["prec_nnz"]) == list(want)
 
 
-def _replay_parity(P, w, ctrl, maxit, rtol, hist_rtol=1e-6):
+def _replay_parity(P, w, ctrl, maxit, rtol, hist_rtol=1e-6, tight=100):
     """Decision replay: the GPU solve logs the column-block map its SpMV used at every
     iteration; the oracle runs CG on that same sequence of maps. Same status, iteration
-    count within 1, residual history within hist_rtol (relative) at every iteration."""
+    count within 1, and residual histories that agree to what the arithmetic allows.
+
+    The two operators differ only in rounding: the oracle sums every product in FP64, the
+    kernel sums a row's low-precision products (each exact) in an FP32 pair, whose
+    additions round at u^2 = 2^-48 of the running sum, so a row's value is within
+    delta = 2 u^2 n^2 of sum |a x| (n: the longest row) of the FP64 sum. A perturbation of
+    relative size delta at iteration k moves the residual norm by about delta ||r_0|| /
+    ||r_k|| relative to ||r_k||, so the histories must agree within hist_rtol + 2 delta
+    ||r_0|| / ||r_k|| over the first `tight` iterations, and within 1e-2 or that bound
+    after them (finite-precision CG amplifies any difference slowly over hundreds of
+    iterations; the dot products' summation orders differ as well)."""
     log = np.full((maxit + 1, P.t.nrb), 255, np.uint8)
     ctrl.log_to(log)
     info, x, h = _solve(P, w.b, rtol, maxit, w.jacobi, ctrl, False)
@@ -81,7 +91,12 @@ def _replay_parity(P, w, ctrl, maxit, rtol, hist_rtol=1e-6):
     assert abs(k - ref["iters"]) <= 1, (k, ref["iters"])
     n0 = min(len(h), len(ref["hist"]))
     rel = np.abs(h[:n0] - ref["hist"][:n0]) / ref["hist"][:n0]
-    assert rel.max() <= hist_rtol, (rel.max(), int(rel.argmax()))
+    nmax = int(np.diff(P.A.rp).max())
+    delta = 2.0 * 2.0 ** -48 * nmax ** 2
+    allow = hist_rtol + 2.0 * delta * ref["hist"][0] / ref["hist"][:n0]
+    bad = rel[:tight] > allow[:tight]
+    assert not bad.any(), (rel[:tight][bad][:3], np.nonzero(bad)[0][:3], allow[:tight][bad][:3])
+    assert np.all(rel <= np.maximum(1e-2, allow)), (rel.max(), int(rel.argmax()))
     return info, x, ref
 
 

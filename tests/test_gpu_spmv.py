@@ -176,50 +176,41 @@ def test_spmv_parity_full_size(cfg):
     ("dense_t64", W.dense_to_csr(np.random.default_rng(1).standard_normal((200, 200)) + 300 * np.eye(200)), 64),
 ], ids=[c[0] for c in CASES] + ["dense_t32", "dense_t64"])
 def test_spmv_kernels_agree(name, m, T):
-    """The staged kernel (operands copied to shared memory by bulk asynchronous copies) and
-    the direct kernel sum the same products in the same order for T >= 32: identical bits.
-    For T = 16 the direct kernel gives alternate tiles of a row block to the two half-warps
-    and merges them at the end, so the two agree to rounding only. Dense tiles exercise the
-    path for tiles larger than a stage; n not a multiple of T the partial last x segment."""
+    """The panel kernel (the default for tiles of 16 and 32) and the direct kernel sum the same
+    exactly rounded-operand products in different orders: they agree to rounding, and each
+    matches the oracle. Dense tiles exercise the panel kernel's path for a tile larger than a
+    stage; n not a multiple of T the partial last x segment."""
     P = Pair(m, T)
     rng = np.random.default_rng(5)
     x = torch.from_numpy(rng.uniform(-1, 1, P.n) * 10.0 ** rng.uniform(-3, 3, P.n)).cuda()
     for mp in (np.zeros(P.t.ntiles, np.uint8), P.tile_map(1), P.tile_map(2, (0, 0, 1)), P.tile_map(3, (0, 1, 0))):
         evocg.set_tile_precision(P.G, mp)
         ys = {}
-        for k, flag in (("staged", evocg.SPMV_STAGED), ("direct", evocg.SPMV_DIRECT), ("default", 0)):
+        for k, flag in (("direct", evocg.SPMV_DIRECT), ("default", 0)):
             ys[k] = torch.full((P.n,), np.nan, dtype=torch.float64, device="cuda")
             evocg.spmv_ex(P.G, x, ys[k], flag)
         torch.cuda.synchronize()
         want = oracle.mixed_spmv(P.A, P.t, mp, x.cpu().numpy())
         den = P.abs_sum(mp, x.cpu().numpy())
-        assert torch.equal(ys["default"].view(torch.int64), ys["staged"].view(torch.int64))
-        if T >= 32:
-            assert torch.equal(ys["staged"].view(torch.int64), ys["direct"].view(torch.int64))
-        else:
-            assert row_rel_err(ys["staged"].cpu().numpy(), ys["direct"].cpu().numpy(), den).max() <= 1e-12
+        assert row_rel_err(ys["default"].cpu().numpy(), ys["direct"].cpu().numpy(), den).max() <= 1e-12
         for k in ys:
             err = row_rel_err(ys[k].cpu().numpy(), want, den)
             assert err.max() <= (TOL64 if not mp.any() else TOLMIX), k
 
 
-def test_spmv_misaligned_x_uses_direct_kernel():
-    """An x that is not 16-byte aligned cannot be a bulk-copy source: asked for the staged
-    kernel, the library runs the direct kernel and the result is unchanged; the default
-    kernel reads x element by element and takes it as is."""
+def test_spmv_misaligned_x():
+    """An x that is not 16-byte aligned cannot be a bulk-copy source: the panel kernel copies
+    its FP64 segments entry by entry instead, with the same result bit for bit."""
     P = Pair(W.diffusion3d_7pt(16, 2), 32)
-    mp = P.tile_map(4)
-    evocg.set_tile_precision(P.G, mp)
-    buf = torch.from_numpy(np.random.default_rng(9).standard_normal(P.n + 1)).cuda()
-    xa = buf[1:]                       # 8 bytes past a 256-byte boundary
-    xb = buf[1:].clone()               # aligned copy of the same values
-    assert xa.data_ptr() % 16 == 8 and xb.data_ptr() % 16 == 0
-    ya = torch.empty(P.n, dtype=torch.float64, device="cuda")
-    yb = torch.empty_like(ya)
-    yc = torch.empty_like(ya)
-    evocg.spmv_ex(P.G, xa, ya, evocg.SPMV_STAGED)
-    evocg.spmv_ex(P.G, xb, yb, evocg.SPMV_STAGED)
-    evocg.spmv(P.G, xa, yc)
-    torch.cuda.synchronize()
-    assert torch.equal(ya.view(torch.int64), yb.view(torch.int64))
-    assert torch.equal(ya.view(torch.int64), yc.view(torch.int64))
+    for mp in (P.tile_map(4), np.zeros(P.t.ntiles, np.uint8)):
+        evocg.set_tile_precision(P.G, mp)
+        buf = torch.from_numpy(np.random.default_rng(9).standard_normal(P.n + 1)).cuda()
+        xa = buf[1:]                       # 8 bytes past a 256-byte boundary
+        xb = buf[1:].clone()               # aligned copy of the same values
+        assert xa.data_ptr() % 16 == 8 and xb.data_ptr() % 16 == 0
+        ya = torch.empty(P.n, dtype=torch.float64, device="cuda")
+        yb = torch.empty_like(ya)
+        evocg.spmv(P.G, xa, ya)
+        evocg.spmv(P.G, xb, yb)
+        torch.cuda.synchronize()
+        assert torch.equal(ya.view(torch.int64), yb.view(torch.int64))

@@ -87,3 +87,20 @@ def test_panel_spmv_parity_full_size(cfg):
         want = oracle.mixed_spmv(P.A, P.t, mp, xh)
         err = row_rel_err(y, want, P.abs_sum(mp, xh))
         assert err.max() <= tol, (err.max(), int(err.argmax()))
+
+
+def test_lost_stage_wait_is_reported_and_the_context_stays_usable():
+    """The panel kernel's stage waits are bounded in time. Under the test hook one warp
+    withholds its first arrival, so its wait runs out (after 2 ms): the call returns
+    EVOCG_ETIMEOUT instead of hanging, and the next call on the same handle is correct."""
+    P = Pair(W.diffusion3d_7pt(16, 9), 32)
+    mp = P.tile_map(3)
+    evocg.set_tile_precision(P.G, mp)
+    xh = np.random.default_rng(4).standard_normal(P.n)
+    y = np.empty(P.n)
+    with pytest.raises(evocg.EvocgError) as e:
+        evocg.spmv_ex(P.G, xh, y, evocg.SPMV_PANEL | evocg.SPMV_TEST_LOST_WAIT)
+    assert e.value.code == evocg.ETIMEOUT
+    evocg.spmv_ex(P.G, xh, y, evocg.SPMV_PANEL)
+    want = oracle.mixed_spmv(P.A, P.t, mp, xh)
+    assert row_rel_err(y, want, P.abs_sum(mp, xh)).max() <= TOLMIX

@@ -68,8 +68,8 @@ def test_host_tile_csc_fig4b():
 def slot_layout_holds_the_csr(h, n, rp, ci, v, T):
     """The kernels' slot-major interior (row mask, width, w x h slots, pads at local column T)
     rebuilt into CSR with numpy equals the input; every pad is +0 in all three streams. A tile
-    with more than one slot starts on a multiple of 8 slots and is followed by pads up to a
-    multiple of 8; every row block's slots start on a multiple of 16."""
+    with more than one slot starts on a multiple of 16 slots and is followed by pads up to a
+    multiple of 16; every row block's slots start on a multiple of 16."""
     rows, cols, vals = [], [], []
     trow = np.repeat(np.arange(len(h["tileRowPtr"]) - 1), np.diff(h["tileRowPtr"]))
     first = h["tileNnzOff"][h["tileRowPtr"][:-1][np.diff(h["tileRowPtr"]) > 0]]
@@ -79,7 +79,7 @@ def slot_layout_holds_the_csr(h, n, rp, ci, v, T):
         m, w, off = int(h["rowMask"][t]), int(h["tileWidth"][t]), int(h["tileNnzOff"][t])
         rr = [r for r in range(T) if (m >> r) & 1]
         if w * len(rr) > 1:
-            assert off % 8 == 0 and h["tileNnzOff"][t + 1] - off >= (w * len(rr) + 7) // 8 * 8
+            assert off % 16 == 0 and h["tileNnzOff"][t + 1] - off >= (w * len(rr) + 15) // 16 * 16
         else:
             assert h["tileNnzOff"][t + 1] - off >= 1
         real[off:off + w * len(rr)] = True
@@ -120,30 +120,36 @@ def test_host_builder_rejects_bad_input():
         evocg.tile_layout_host(n, rp, ci2, v, 16)                # columns ascending per row
 
 
-@pytest.mark.parametrize("name,m,T", list(_cases()), ids=[c[0] for c in _cases()])
-@pytest.mark.parametrize("warps", [1, 7, 2432])
-def test_staged_plan_passes_its_checks(name, m, T, warps):
-    """The staged SpMV's plan, built as the library builds it, passes the checks the library
-    applies before using it, for one warp, a few warps, and the 128^3 solve's 2432 consumer
-    warps (more warps than row blocks leaves warps without work)."""
+@pytest.mark.parametrize("name,m,T", [c for c in _cases() if c[2] <= 32], ids=[c[0] for c in _cases() if c[2] <= 32])
+@pytest.mark.parametrize("warps,stage", [(1, 4096), (7, 3072), (3648, 4096), (4864, 2560)])
+def test_panel_plan_passes_its_checks(name, m, T, warps, stage):
+    """The panel SpMV's batch plan, built as the library builds it, passes the checks the
+    library applies before using it, for one warp, a few warps and the grids of the kernel
+    variants (more warps than panels leaves warps without work), with stages from 2.5 to 4 KB
+    (a dense tile larger than a stage becomes a direct batch)."""
     n, rp, ci, v = m
-    nb, ok = evocg.staged_plan_host(n, rp, ci, v, T, warps)
-    assert ok and nb >= (1 if n > 0 else 0)
+    nb, ok = evocg.panel_plan_host(n, rp, ci, v, T, warps, stage)
+    assert ok, evocg.last_error()
+    assert nb >= (n + T - 1) // T   # at least one batch per panel
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3])
-def test_staged_plan_of_the_stencil_workloads(cfg):
+def test_panel_plan_of_the_stencil_workloads(cfg):
     w = W.workload(cfg)
-    for warps in (1216 * 2, 152 * 4 * 4):   # the T = 32 and T = 16 kernels' consumer warps
-        nb, ok = evocg.staged_plan_host(w.n, w.rp, w.ci, w.v, w.T, warps)
-        assert ok and nb > 0
-    if cfg == 2:   # the 128^3 solve's plan: 65,294 batches of at most 16 tiles
-        nb, _ = evocg.staged_plan_host(w.n, w.rp, w.ci, w.v, w.T, 2432)
-        assert 423936 / 16 <= nb <= 423936
+    nb, ok = evocg.panel_plan_host(w.n, w.rp, w.ci, w.v, w.T, 3648, 4096)
+    assert ok, evocg.last_error()
+    if cfg == 2:   # every 128^3 panel's tiles fit one 4 KB stage sized for FP64
+        assert nb == w.n // 32
+
+
+def test_panel_plan_rejects_tiles_of_64():
+    n, rp, ci, v = W.laplace2d_5pt(70)
+    nb, ok = evocg.panel_plan_host(n, rp, ci, v, 64, 8, 4096)
+    assert not ok and nb == 0
 
 
 def test_empty_matrix():
     z64, z32, zf = np.zeros(1, np.int64), np.zeros(0, np.int32), np.zeros(0)
     h = evocg.tile_layout_host(0, z64, z32, zf, 16)
     assert (h["ntiles"], h["nslots"]) == (0, 0) and list(h["tileRowPtr"]) == [0]
-    assert evocg.staged_plan_host(0, z64, z32, zf, 32, 4) == (0, True)
+    assert evocg.panel_plan_host(0, z64, z32, zf, 32, 4) == (0, True)
