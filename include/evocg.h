@@ -213,6 +213,23 @@ int evocg_panel_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *col_
                           int64_t *nbatches, int *valid);
 
 /*
+ * The row-block SpMV's plan for a matrix (tiles of 32), computed on the HOST only (no GPU),
+ * for inspection. The paper has no counterpart: the plan belongs to this library's SpMV
+ * kernel. Every tile of two or more slots gets a 16-byte descriptor; the single-entry tiles
+ * of each row block are gathered into a row-owned ELL block (rows with such tiles x the
+ * largest count of them in one row, shorter rows padded).
+ *   *ndesc receives the descriptor count, *nsingle_slots the ELL slots (pads included),
+ *   *valid 1 when the plan passes the checks the library applies before using it (every
+ *   descriptor and single matching the tile structure, tile slices 16-slot aligned), 0 when
+ *   the library would run another kernel (tiles other than 32, a size limit; the reason is
+ *   in evocg_last_error). Each pointer may be NULL.
+ * Errors: as evocg_tile_build.
+ */
+int evocg_rowblock_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                             const double *vals, int tile_size, int64_t *ndesc,
+                             int64_t *nsingle_slots, int *valid);
+
+/*
  * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
  *   map: host or device, len = ntiles (PER_TILE) or nrb (PER_COLBLOCK).
  * The SpMV and static-map solves read the map set last. Errors: EINVAL on a wrong length
@@ -244,17 +261,22 @@ enum {
     EVOCG_SPMV_DIRECT = 2,        /* run the direct kernel: a warp per row block, every operand
                                      loaded by the lanes from global memory, one tile after
                                      the other (the kernel for tiles of 64). At most one of
-                                     DIRECT, PANEL may be set */
-    EVOCG_SPMV_PANEL = 8,         /* run the panel kernel (the default for tiles of 16 and 32):
+                                     DIRECT, PANEL, ROWBLOCK may be set */
+    EVOCG_SPMV_PANEL = 8,         /* run the panel kernel (the default for tiles of 16):
                                      a warp streams batches of tiles of consecutive row blocks
                                      through two shared-memory stages, every tile's own lane
                                      issuing its bulk copies; single-entry tiles take one lane
                                      each */
-    EVOCG_SPMV_TEST_LOST_WAIT = 16 /* test hook of the panel kernel: one warp withholds its first
+    EVOCG_SPMV_TEST_LOST_WAIT = 16, /* test hook of the panel kernel: one warp withholds its first
                                      stage arrival and waits 2 ms instead of 2 s, so that the
                                      path of a lost stage wait runs; the call must then return
                                      EVOCG_ETIMEOUT (host pointers) and the handle's error word
                                      is cleared by that report */
+    EVOCG_SPMV_ROWBLOCK = 32       /* run the row-block kernel (the default for tiles of 32): a
+                                     warp per row block, lane l owning row l; regular tiles from
+                                     16-byte descriptors, the single-entry tiles of the row block
+                                     from a row-owned ELL block; the next row block's tile
+                                     slices prefetched into L2 */
 };
 
 /*

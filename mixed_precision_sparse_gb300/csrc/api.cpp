@@ -356,6 +356,21 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
             }
         }
     }
+    // row-block SpMV plan (tiles of 32)
+    if (e == cudaSuccess && H.nrb > 0 && H.T == 32) {
+        RowBlockPlan P;
+        std::string why;
+        if (rowblock_plan(H, &P, &why) && rowblock_plan_ok(H, P, &why)) {
+            up(&A->rbMeta, P.meta.data(), (int64_t)P.meta.size());
+            up(&A->rgDesc, P.desc.data(), (int64_t)P.desc.size());
+            up(&A->sgCol, P.sgCol.data(), (int64_t)P.sgCol.size());
+            up(&A->sgTile, P.sgTile.data(), (int64_t)P.sgTile.size());
+            up(&A->sgV64, P.sgV64.data(), (int64_t)P.sgV64.size());
+            up(&A->sgV32, P.sgV32.data(), (int64_t)P.sgV32.size());
+            up(&A->sgV16, P.sgV16.data(), (int64_t)P.sgV16.size());
+            if (e == cudaSuccess) A->rb_grid = rowblock_grid_for(sms);
+        }
+    }
     if (e == cudaSuccess) e = dalloc(&A->errw, 1);
     if (e == cudaSuccess) e = cudaMemset(A->errw, 0, sizeof(int));
     H.release();
@@ -372,12 +387,15 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
         return code;
     }
     A->spmv_grid = spmv_grid_for(A->T, sms);
-    // Default kernel: the panel kernel where its plan exists, else the direct one;
-    // EVOCG_SPMV_KERNEL=direct selects the direct kernel for every SpMV of the matrices built
-    // afterwards.
+    // Default kernel: the row-block kernel where its plan exists, else the panel kernel where
+    // its plan exists, else the direct one; EVOCG_SPMV_KERNEL=direct|panel|rowblock selects
+    // another for every SpMV of the matrices built afterwards (where its plan exists).
     A->spmv_kind = SPMV_KIND_AUTO;
-    if (const char *k = std::getenv("EVOCG_SPMV_KERNEL"))
+    if (const char *k = std::getenv("EVOCG_SPMV_KERNEL")) {
         if (!std::strcmp(k, "direct")) A->spmv_kind = SPMV_KIND_DIRECT;
+        else if (!std::strcmp(k, "panel")) A->spmv_kind = SPMV_KIND_PANEL;
+        else if (!std::strcmp(k, "rowblock")) A->spmv_kind = SPMV_KIND_ROWBLOCK;
+    }
     A->vec_grid = sms * 4 > kMaxBlocks ? kMaxBlocks : sms * 4;
     *out = A;
     return EVOCG_OK;
@@ -391,6 +409,8 @@ extern "C" int evocg_tiles_free(evocg_tiles_t A)
     dfree(A->tileRowPtr); dfree(A->tileColIdx); dfree(A->tileNnzOff); dfree(A->tileRowIdx);
     dfree(A->rowMask); dfree(A->tileWidth);
     dfree(A->errw); dfree(A->pdesc); dfree(A->warpRec); dfree(A->panelRec); dfree(A->recPrec);
+    dfree(A->rbMeta); dfree(A->rgDesc); dfree(A->sgCol); dfree(A->sgTile); dfree(A->sgV64);
+    dfree(A->sgV32); dfree(A->sgV16);
     dfree(A->colIdx); dfree(A->v64); dfree(A->v32); dfree(A->v16); dfree(A->colExp);
     dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16f);
     dfree(A->xstage); dfree(A->ystage);
@@ -500,8 +520,9 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
 {
     g_err.clear();
     if (!A || (A->n > 0 && (!x || !y))) return fail(EVOCG_EINVAL, "NULL argument");
-    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL);
-    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL | EVOCG_SPMV_TEST_LOST_WAIT))
+    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL | EVOCG_SPMV_ROWBLOCK);
+    if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL | EVOCG_SPMV_TEST_LOST_WAIT |
+                  EVOCG_SPMV_ROWBLOCK))
         return fail(EVOCG_EINVAL, "unknown flags");
     if (kflags & (kflags - 1)) return fail(EVOCG_EINVAL, "at most one kernel flag");
     if (A->n == 0) return EVOCG_OK;
@@ -535,7 +556,7 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     S.map_kind = A->map_kind;
     S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
     S.direct = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
-    S.kind = (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : 0;
+    S.kind = (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : (flags & EVOCG_SPMV_ROWBLOCK) ? SPMV_KIND_ROWBLOCK : 0;
     S.test_lost_wait = (flags & EVOCG_SPMV_TEST_LOST_WAIT) ? 1 : 0;
     CK(launch_spmv(S, s), "launch spmv");
     if (!ydev) {

@@ -21,6 +21,7 @@ constexpr int kMlpHiddenMax = 64;
 constexpr int kSlack = 16;            // bytes past the end of every device array (16-byte copies)
 constexpr int kPanelThreads = 128;    // threads per block of the panel SpMV
 constexpr int kPanelVariants = 4;     // (tiles issued together, blocks per SM) variants built
+constexpr int kRbThreads = 256;       // threads per block of the row-block SpMV
 
 // Device-resident solver state; one per handle. Written by the last block of each
 // reducing kernel, read by every block of the next kernel.
@@ -73,12 +74,23 @@ struct TilesView {
     int64_t nrec;             // records of the stream before its 32 closing records
     int panel_grid;
     int panel_variant;
+    // row-block SpMV (tiles of 32): meta words (nrb + 1), regular-tile descriptors and the
+    // single-entry tiles' ELL blocks (rowblock_plan.cpp); rb_grid 0: no plan
+    const uint4 *rbMeta;
+    const uint4 *rgDesc;
+    const int32_t *sgCol;
+    const int32_t *sgTile;
+    const double *sgV64;
+    const float *sgV32;
+    const uint16_t *sgV16;
+    int rb_grid;
 };
 
-// SpMV kernels: the panel kernel (spmv_panel.cu; tiles of 16 and 32) and the direct kernel
-// (spmv.cu: warp per row block, global loads; tiles of 64, or no panel plan). AUTO: the panel
-// kernel when its plan exists.
-enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_PANEL = 3 };
+// SpMV kernels: the row-block kernel (spmv_rowblock.cu; tiles of 32), the panel kernel
+// (spmv_panel.cu; tiles of 16 and 32) and the direct kernel (spmv.cu: warp per row block,
+// plain loads; any tile size). AUTO: the row-block kernel where its plan exists, else the
+// panel kernel where its plan exists, else the direct one.
+enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_PANEL = 3, SPMV_KIND_ROWBLOCK = 4 };
 
 struct SolveWS {
     int64_t cap_n = 0, cap_ncb = 0;
@@ -129,6 +141,14 @@ struct evocg_tiles {
     std::vector<int32_t> tileRec;  // host: the record of every tile (for recPrec)
     int panel_grid = 0;
     int panel_variant = 0;
+    uint4 *rbMeta = nullptr;       // row-block SpMV plan (see TilesView)
+    uint4 *rgDesc = nullptr;
+    int32_t *sgCol = nullptr;
+    int32_t *sgTile = nullptr;
+    double *sgV64 = nullptr;
+    float *sgV32 = nullptr;
+    uint16_t *sgV16 = nullptr;
+    int rb_grid = 0;
     int *errw = nullptr;           // device error word (a lost stage wait)
     int spmv_kind = 0;             // default SpMV kernel (SPMV_KIND_*)
     uint8_t *tilePrec = nullptr;   // per-tile map
@@ -148,7 +168,8 @@ struct evocg_tiles {
     {
         return evocg::TilesView{n, nrb, ntiles, nslots, T, tileRowPtr, tileColIdx, tileNnzOff,
                                 tileRowIdx, rowMask, tileWidth, colIdx, v64, v32, v16, colExp,
-                                errw, spmv_kind, pdesc, warpRec, panelRec, recPrec, nrec, panel_grid, panel_variant};
+                                errw, spmv_kind, pdesc, warpRec, panelRec, recPrec, nrec, panel_grid, panel_variant,
+                                rbMeta, rgDesc, sgCol, sgTile, sgV64, sgV32, sgV16, rb_grid};
     }
 };
 
@@ -221,6 +242,19 @@ struct PanelPlan {
 };
 bool panel_plan(const HostTiles &H, int64_t warps, int stage_bytes, PanelPlan *out, std::string *why);
 bool panel_plan_ok(const HostTiles &H, int64_t warps, int stage_bytes, const PanelPlan &pl, std::string *why);
+cudaError_t launch_spmv_rowblock(const SpmvLaunch &L, cudaStream_t s);
+int rowblock_grid_for(int sms);
+struct RowBlockPlan {
+    std::vector<uint4> meta;      // nrb + 1: {first descriptor, first single slot, rows mask, width}
+    std::vector<uint4> desc;      // regular tiles: {first slot, column block | width << 26, rows, tile}
+    std::vector<int32_t> sgCol;   // single-entry tiles, row-owned ELL per row block (-1: pad)
+    std::vector<int32_t> sgTile;
+    std::vector<double> sgV64;
+    std::vector<float> sgV32;
+    std::vector<uint16_t> sgV16;
+};
+bool rowblock_plan(const HostTiles &H, RowBlockPlan *out, std::string *why);
+bool rowblock_plan_ok(const HostTiles &H, const RowBlockPlan &P, std::string *why);
 
 cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, float *x16f,
                            int grid, cudaStream_t s);

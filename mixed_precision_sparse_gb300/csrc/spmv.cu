@@ -1,8 +1,9 @@
 // spmv.cu -- the direct tile-wise mixed-precision SpMV (EvoCG, "Self-Evolving Precision
 // Control for Faster Conjugate Gradient", §3.3 EvoSpMV, Eq. 2 / Eq. 5) for sm_103a, the kernel
 // choice, the rounded x copies the SpMV reads, and the device rounding entry point. The
-// panel kernel (spmv_panel.cu) runs wherever its plan exists (tiles of 16 and 32); this
-// kernel runs the rest (tiles of 64) and on request.
+// row-block kernel (spmv_rowblock.cu, tiles of 32) and the panel kernel (spmv_panel.cu,
+// tiles of 16) run wherever their plans exist; this kernel runs the rest (tiles of 64) and
+// on request.
 //
 // Work mapping. A warp owns a row block (T rows) at a time and walks its tiles in
 // ascending column block, so every row is summed in column order. Lane l owns local row
@@ -198,13 +199,16 @@ static int chosen_kind(const SpmvLaunch &L)
 {
     if (L.direct) return SPMV_KIND_DIRECT;
     const int k = L.kind ? L.kind : L.A.spmv_kind;
-    if ((k == SPMV_KIND_PANEL || k == SPMV_KIND_AUTO) && L.A.pdesc && L.A.panel_grid > 0) return SPMV_KIND_PANEL;
+    const bool rb = L.A.rbMeta && L.A.rb_grid > 0, panel = L.A.pdesc && L.A.panel_grid > 0;
+    if (k == SPMV_KIND_ROWBLOCK && rb) return SPMV_KIND_ROWBLOCK;
+    if ((k == SPMV_KIND_PANEL || k == SPMV_KIND_AUTO) && panel) return SPMV_KIND_PANEL;
     return SPMV_KIND_DIRECT;
 }
 
 int spmv_dot_partials(const SpmvLaunch &L)
 {
     switch (chosen_kind(L)) {
+    case SPMV_KIND_ROWBLOCK: return L.A.rb_grid * (kRbThreads / 32);
     case SPMV_KIND_PANEL: return L.A.panel_grid * (kPanelThreads / 32);
     default: return L.grid * (kSpmvThreads / 32);
     }
@@ -213,6 +217,7 @@ int spmv_dot_partials(const SpmvLaunch &L)
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
 {
     switch (chosen_kind(L)) {
+    case SPMV_KIND_ROWBLOCK: return launch_spmv_rowblock(L, s);
     case SPMV_KIND_PANEL: return launch_spmv_panel(L, s);
     default: return launch_spmv_direct(L, s);
     }

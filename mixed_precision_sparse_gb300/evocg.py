@@ -112,6 +112,8 @@ def lib():
                                            C.POINTER(C.c_int64)] + [P] * 10,
                 "evocg_panel_plan_host": [i64, P, P, P, i32, i64, i32, C.POINTER(C.c_int64),
                                           C.POINTER(C.c_int)],
+                "evocg_rowblock_plan_host": [i64, P, P, P, i32, C.POINTER(C.c_int64),
+                                             C.POINTER(C.c_int64), C.POINTER(C.c_int)],
                 "evocg_tile_csc_host": [i64, P, P, P, i32, i32, C.POINTER(C.c_int64),
                                         C.POINTER(C.c_int64)] + [P] * 9,
                 "evocg_tiles_export_csc": [P, i32, C.POINTER(C.c_int64)] + [P] * 9,
@@ -295,6 +297,15 @@ def panel_plan_host(n, row_ptr, col_idx, vals, tile_size: int, warps: int, stage
     return nb.value, bool(ok.value)
 
 
+def rowblock_plan_host(n, row_ptr, col_idx, vals, tile_size: int):
+    """(descriptors, single-entry ELL slots, valid) of the row-block SpMV's plan, on the host."""
+    rp, ci, v = _np(row_ptr, np.int64), _np(col_idx, np.int32), _np(vals, np.float64)
+    nd, ns, ok = C.c_int64(), C.c_int64(), C.c_int()
+    _check(lib().evocg_rowblock_plan_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), int(tile_size),
+                                          C.byref(nd), C.byref(ns), C.byref(ok)))
+    return nd.value, ns.value, bool(ok.value)
+
+
 def set_tile_precision(A: Tiles, prec_map, map_kind: int = MAP_PER_TILE, stream=None):
     m = prec_map if hasattr(prec_map, "data_ptr") else _np(prec_map, np.uint8)
     n = m.numel() if hasattr(m, "numel") else m.size
@@ -311,6 +322,7 @@ SPMV_REUSE_XCOPIES = 1
 SPMV_DIRECT = 2
 SPMV_PANEL = 8
 SPMV_TEST_LOST_WAIT = 16
+SPMV_ROWBLOCK = 32
 
 
 def spmv(A: Tiles, x, y, stream=None):

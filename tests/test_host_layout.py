@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 
 import oracle
+from helpers import many_tiles_t32, rowblock_counts
 from mixed_precision_sparse_gb300 import build, evocg
 from mixed_precision_sparse_gb300 import workloads as W
 
@@ -148,8 +149,36 @@ def test_panel_plan_rejects_tiles_of_64():
     assert not ok and nb == 0
 
 
+@pytest.mark.parametrize("name,m", [(c[0], c[1]) for c in _cases() if c[2] == 32] +
+                         [("many_tiles", many_tiles_t32()), ("lap2d_t32", W.laplace2d_5pt(100))],
+                         ids=[c[0] for c in _cases() if c[2] == 32] + ["many_tiles", "lap2d_t32"])
+def test_rowblock_plan_passes_its_checks(name, m):
+    """The row-block SpMV's plan, built as the library builds it, passes the checks the library
+    applies before using it, and its descriptor and single-entry ELL counts equal those counted
+    from the CSR with numpy."""
+    n, rp, ci, v = m
+    nd, ns, ok = evocg.rowblock_plan_host(n, rp, ci, v, 32)
+    assert ok, evocg.last_error()
+    assert (nd, ns) == rowblock_counts(n, rp, ci)
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_rowblock_plan_of_the_stencil_workloads(cfg):
+    w = W.workload(cfg)
+    nd, ns, ok = evocg.rowblock_plan_host(w.n, w.rp, w.ci, w.v, w.T)
+    assert ok, evocg.last_error()
+    assert (nd, ns) == rowblock_counts(w.n, w.rp, w.ci)
+
+
+def test_rowblock_plan_is_for_tiles_of_32():
+    n, rp, ci, v = W.laplace2d_5pt(70)
+    for T in (16, 64):
+        assert evocg.rowblock_plan_host(n, rp, ci, v, T) == (0, 0, False)
+
+
 def test_empty_matrix():
     z64, z32, zf = np.zeros(1, np.int64), np.zeros(0, np.int32), np.zeros(0)
     h = evocg.tile_layout_host(0, z64, z32, zf, 16)
     assert (h["ntiles"], h["nslots"]) == (0, 0) and list(h["tileRowPtr"]) == [0]
     assert evocg.panel_plan_host(0, z64, z32, zf, 32, 4) == (0, True)
+    assert evocg.rowblock_plan_host(0, z64, z32, zf, 32) == (0, 0, True)
