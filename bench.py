@@ -128,7 +128,7 @@ def _src_hash():
     builder whose layout they read, and the internal header."""
     csrc = os.path.join(ROOT, "mixed_precision_sparse_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("spmv_panel.cu", "panel_plan.cpp", "tile_build.cpp", "spmv.cu", "fpconv.cuh",
+    for name in ("spmv_rowblock.cu", "rowblock_plan.cpp", "tile_build.cpp", "spmv.cu", "fpconv.cuh",
                  "evocg_internal.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
@@ -421,7 +421,7 @@ def run_ours(args):
     mixed = spmv["mixed_40_40_20"]
     roofline = {"bound": "hbm", "achieved": mixed["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": mixed["frac_of_peak"], "traffic": traffic,
-                "kernel": "spmv_panel_kernel (panel-streaming, cp.async-staged; mixed 40/40/20 map)",
+                "kernel": "spmv_rowblock_kernel (row-block units staged by per-lane cp.async; mixed 40/40/20 map)",
                 "peak_kind": peak_kind, "frac_of_8tbs": mixed["frac_of_8tbs"],
                 "bytes_per_launch": mixed["bytes"], "us_per_launch": mixed["us"],
                 "bytes_rule": "Tile-CSC algorithmic bytes: active value stream + 1 row-index "

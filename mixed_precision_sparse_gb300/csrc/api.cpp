@@ -531,6 +531,8 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     const bool xdev = is_device_ptr(x), ydev = is_device_ptr(y);
     if (reuse && (!xdev || !ydev))
         return fail(EVOCG_EINVAL, "EVOCG_SPMV_REUSE_XCOPIES needs device x and y");
+    const int kdirect = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
+    const int kkind = (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : (flags & EVOCG_SPMV_ROWBLOCK) ? SPMV_KIND_ROWBLOCK : 0;
     if (reuse && !A->xcopies_valid)
         return fail(EVOCG_EINVAL, "EVOCG_SPMV_REUSE_XCOPIES: no earlier SpMV made the copies");
     const size_t bytes = sizeof(double) * (size_t)A->n;
@@ -555,8 +557,8 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     S.prec = (A->map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
     S.map_kind = A->map_kind;
     S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
-    S.direct = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
-    S.kind = (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : (flags & EVOCG_SPMV_ROWBLOCK) ? SPMV_KIND_ROWBLOCK : 0;
+    S.direct = kdirect;
+    S.kind = kkind;
     S.test_lost_wait = (flags & EVOCG_SPMV_TEST_LOST_WAIT) ? 1 : 0;
     CK(launch_spmv(S, s), "launch spmv");
     if (!ydev) {

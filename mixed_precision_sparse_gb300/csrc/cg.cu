@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
             st->tickets[TK_INIT] = 0;
             st->rho = L.jacobi ? RZ : RR;
             st->rr = RR;
+            st->xstep = 0;
             if (!restart) {
                 st->nr0 = sqrt(RR);
                 st->k = 0;
@@ -175,14 +176,18 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
 }
 
 // sigma = p.q from the SpMV's per-warp partials (summed in warp order, identically in every
-// block), alpha = rho / sigma; then x += alpha p; r -= alpha q; z = D^-1 r; r.z and ||r||^2.
-// The last block appends the history entry, tests convergence and forms beta. A sigma that
-// is not finite and positive stops the solve with EVOCG_EBREAKDOWN.
+// block), alpha = rho / sigma; then r -= alpha q; z = D^-1 r; r.z and ||r||^2 (x += alpha p is
+// left to the p-update, which reads p anyway). The last block appends the history entry, tests
+// convergence and forms beta. A sigma that is not finite and positive stops the solve with
+// EVOCG_EBREAKDOWN.
 __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(CgLaunch L, int npq)
 {
     DevState *st = L.st;
     if (st->done) {
-        if (L.use_cond && blockIdx.x == 0 && threadIdx.x == 0) cudaGraphSetConditional(L.cond, 0u);
+        if (blockIdx.x == 0 && threadIdx.x == 0) {
+            st->xstep = 0;
+            if (L.use_cond) cudaGraphSetConditional(L.cond, 0u);
+        }
         return;
     }
     __shared__ double s_alpha;
@@ -195,6 +200,7 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
             s_alpha = ok ? st->rho / sigma : 0.0;
             if (blockIdx.x == 0) {
                 st->sigma = sigma;
+                st->xstep = ok ? 1 : 0;
                 if (ok) {
                     st->alpha = s_alpha;
                 } else {
@@ -215,13 +221,9 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
     // of dot-product partials, so that neither the loads nor the FP64 pipe wait on one
     // chain of fused multiply-adds.
     double rz0 = 0.0, rr0 = 0.0, rz1 = 0.0, rr1 = 0.0;
-    auto pair_update = [&](int64_t j, double2 p, double2 q, double2 x, double2 r, double2 d,
-                           double &rz, double &rr) {
-        x.x = fma(alpha, p.x, x.x);
-        x.y = fma(alpha, p.y, x.y);
+    auto pair_update = [&](int64_t j, double2 q, double2 r, double2 d, double &rz, double &rr) {
         r.x = fma(-alpha, q.x, r.x);
         r.y = fma(-alpha, q.y, r.y);
-        *reinterpret_cast<double2 *>(L.x + j) = x;
         *reinterpret_cast<double2 *>(L.r + j) = r;
         rr = fma(r.x, r.x, rr);
         rr = fma(r.y, r.y, rr);
@@ -238,25 +240,21 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
     int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (; pair + stride < nfull; pair += 2 * stride) {
         const int64_t ja = 2 * pair, jb = 2 * (pair + stride);
-        const double2 pa = ld2(L.p, ja), pb = ld2(L.p, jb);
         const double2 qa = ld2(L.q, ja), qb = ld2(L.q, jb);
-        const double2 xa = ld2(L.x, ja), xb = ld2(L.x, jb);
         const double2 ra = ld2(L.r, ja), rb = ld2(L.r, jb);
         double2 da = make_double2(0.0, 0.0), db = da;
         if (L.jacobi) { da = ld2(L.dinv, ja); db = ld2(L.dinv, jb); }
-        pair_update(ja, pa, qa, xa, ra, da, rz0, rr0);
-        pair_update(jb, pb, qb, xb, rb, db, rz1, rr1);
+        pair_update(ja, qa, ra, da, rz0, rr0);
+        pair_update(jb, qb, rb, db, rz1, rr1);
     }
     if (pair < nfull) {
         const int64_t j = 2 * pair;
         const double2 d = L.jacobi ? ld2(L.dinv, j) : make_double2(0.0, 0.0);
-        pair_update(j, ld2(L.p, j), ld2(L.q, j), ld2(L.x, j), ld2(L.r, j), d, rz0, rr0);
+        pair_update(j, ld2(L.q, j), ld2(L.r, j), d, rz0, rr0);
     }
     if ((n & 1) && blockIdx.x == 0 && threadIdx.x == 0) {   // odd last entry
         const int64_t j = n - 1;
-        const double x = fma(alpha, L.p[j], L.x[j]);
         const double r = fma(-alpha, L.q[j], L.r[j]);
-        L.x[j] = x;
         L.r[j] = r;
         rr1 = fma(r, r, rr1);
         if (L.jacobi) {
@@ -299,17 +297,20 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
     }
 }
 
-// p = z + beta p, its rounded copies, and the threshold rule when it is due.
+// x += alpha p with the p of this iteration (when the update formed a valid alpha), then
+// p = z + beta p, its rounded copies and the threshold rule when it is due; after the last
+// iteration only the x step.
 template <int T>
 __global__ void __launch_bounds__(kVecThreads) cg_pupdate_kernel(CgLaunch L)
 {
     DevState *st = L.st;
-    if (st->done) return;
-    const double beta = st->beta;
+    const bool xs = st->xstep != 0, pdue = !st->done;
+    if (!xs && !pdue) return;
+    const double alpha = st->alpha, beta = st->beta;
     const int64_t n = L.n, npairs = (n + 1) / 2;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int lane = threadIdx.x & 31;
-    const bool thr = (L.ctrl == EVOCG_CTRL_THRESHOLD) && (st->k % st->kstar == 0);
+    const bool thr = pdue && (L.ctrl == EVOCG_CTRL_THRESHOLD) && (st->k % st->kstar == 0);
     const uint64_t lo_bits = (uint64_t)__double_as_longlong(st->eps_lo);
     const uint64_t hi_bits = (uint64_t)__double_as_longlong(st->eps_hi);
     const int64_t ncb = (n + T - 1) / T;
@@ -321,19 +322,31 @@ __global__ void __launch_bounds__(kVecThreads) cg_pupdate_kernel(CgLaunch L)
         if (pair < npairs) {
             const int64_t j = 2 * pair;
             if (j + 1 < n) {
-                const double2 z = *reinterpret_cast<const double2 *>(zsrc + j);
                 double2 p = *reinterpret_cast<const double2 *>(L.p + j);
-                p.x = fma(beta, p.x, z.x);
-                p.y = fma(beta, p.y, z.y);
-                *reinterpret_cast<double2 *>(L.p + j) = p;
-                write_copies2(L, j, p.x, p.y);
-                const uint64_t a0 = abs_bits(p.x), a1 = abs_bits(p.y);
-                m = a0 > a1 ? a0 : a1;
+                if (xs) {
+                    double2 x = *reinterpret_cast<const double2 *>(L.x + j);
+                    x.x = fma(alpha, p.x, x.x);
+                    x.y = fma(alpha, p.y, x.y);
+                    *reinterpret_cast<double2 *>(L.x + j) = x;
+                }
+                if (pdue) {
+                    const double2 z = *reinterpret_cast<const double2 *>(zsrc + j);
+                    p.x = fma(beta, p.x, z.x);
+                    p.y = fma(beta, p.y, z.y);
+                    *reinterpret_cast<double2 *>(L.p + j) = p;
+                    write_copies2(L, j, p.x, p.y);
+                    const uint64_t a0 = abs_bits(p.x), a1 = abs_bits(p.y);
+                    m = a0 > a1 ? a0 : a1;
+                }
             } else {
-                const double p = fma(beta, L.p[j], zsrc[j]);
-                L.p[j] = p;
-                write_copies(L, j, p);
-                m = abs_bits(p);
+                double p = L.p[j];
+                if (xs) L.x[j] = fma(alpha, p, L.x[j]);
+                if (pdue) {
+                    p = fma(beta, p, zsrc[j]);
+                    L.p[j] = p;
+                    write_copies(L, j, p);
+                    m = abs_bits(p);
+                }
             }
         }
         if (thr) threshold_segments<T>(m, pair, ncb, lo_bits, hi_bits, L.cbPrec);

@@ -39,6 +39,7 @@ struct DevState {
     int done;          // 1: the loop stops
     int status;        // EVOCG_OK / ENOTCONV / EBREAKDOWN while running or done
     int converged;
+    int xstep;         // 1: the last update formed a valid alpha, so x += alpha p is due
     unsigned int tickets[8];
     unsigned long long census[3];
     unsigned long long ctrl_calls;
@@ -229,6 +230,8 @@ struct SpmvLaunch {
 // Kernel choice: L.direct, else L.kind, else the matrix's default; the panel kernel only when
 // the view has its plan (else the direct one).
 cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s);
+// The kernel an SpMV with these flags runs on this matrix (SPMV_KIND_*).
+int spmv_kind_for(const TilesView &A, int direct, int kind);
 cudaError_t launch_spmv_direct(const SpmvLaunch &L, cudaStream_t s);
 int spmv_dot_partials(const SpmvLaunch &L);   // warps that write a p.q partial
 cudaError_t launch_spmv_panel(const SpmvLaunch &L, cudaStream_t s);

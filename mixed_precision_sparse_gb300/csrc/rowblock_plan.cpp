@@ -6,8 +6,8 @@
 //   regular tiles (two or more slots): one 16-byte descriptor each, in the row block's tile
 //     order, {first slot, column block | width << 26, row mask, tile index}; the slots
 //     themselves stay where the builder put them (16-slot aligned, a multiple of 16 long),
-//     so that a tile's slices of the value streams and of the column bytes can be
-//     prefetched whole;
+//     so that a tile's slices of the value streams and of the column bytes are copied
+//     whole in 16-byte pieces;
 //   single-entry tiles: on stencil matrices most tiles of a row block hold one entry (the
 //     neighbour across a column-block edge: six of the nine tiles of a 9-point row block,
 //     eighteen of the twenty-seven of a 27-point one), and a warp pass per such tile
@@ -69,9 +69,9 @@ void singles_geo(const HostTiles &H, int64_t rb, unsigned *hs, unsigned *ws, int
 bool rowblock_plan(const HostTiles &H, RowBlockPlan *out, std::string *why)
 {
     if (H.T != 32) { *why = "row-block plan: tiles of 32 only"; return false; }
-    if (H.nslots >= ((int64_t)1 << 32) || H.ntiles >= ((int64_t)1 << 31) ||
+    if (H.nslots >= ((int64_t)1 << 30) || H.ntiles >= ((int64_t)1 << 31) ||
         H.nrb >= ((int64_t)1 << kCbBits)) {
-        *why = "row-block plan: 2^32 slots, 2^31 tiles or 2^26 row blocks or more";
+        *why = "row-block plan: 2^30 slots, 2^31 tiles or 2^26 row blocks or more";
         return false;
     }
     const int64_t nrb = H.nrb;

@@ -195,15 +195,17 @@ static cudaError_t launch_T(const SpmvLaunch &L, cudaStream_t s)
     return cudaGetLastError();
 }
 
-static int chosen_kind(const SpmvLaunch &L)
+int spmv_kind_for(const TilesView &A, int direct, int kind)
 {
-    if (L.direct) return SPMV_KIND_DIRECT;
-    const int k = L.kind ? L.kind : L.A.spmv_kind;
-    const bool rb = L.A.rbMeta && L.A.rb_grid > 0, panel = L.A.pdesc && L.A.panel_grid > 0;
-    if (k == SPMV_KIND_ROWBLOCK && rb) return SPMV_KIND_ROWBLOCK;
+    if (direct) return SPMV_KIND_DIRECT;
+    const int k = kind ? kind : A.spmv_kind;
+    const bool rb = A.rbMeta && A.rb_grid > 0, panel = A.pdesc && A.panel_grid > 0;
+    if ((k == SPMV_KIND_ROWBLOCK || k == SPMV_KIND_AUTO) && rb) return SPMV_KIND_ROWBLOCK;
     if ((k == SPMV_KIND_PANEL || k == SPMV_KIND_AUTO) && panel) return SPMV_KIND_PANEL;
     return SPMV_KIND_DIRECT;
 }
+
+static int chosen_kind(const SpmvLaunch &L) { return spmv_kind_for(L.A, L.direct, L.kind); }
 
 int spmv_dot_partials(const SpmvLaunch &L)
 {

@@ -7,13 +7,15 @@
 // reduction). The row block's work comes from its plan (rowblock_plan.cpp): the regular
 // tiles' descriptors and the row-owned ELL block of its single-entry tiles.
 //
-// Latency. Every load a panel needs is issued ahead of it: a warp keeps three row blocks in
-// flight -- the meta words of the one after next, the descriptors of the next one (lane i
-// holding tile i) and, once their precisions are known, a bulk L2 prefetch of each of the
-// next row block's tile slices in the value stream that tile will be read in, plus its
-// column bytes (cp.async.bulk.prefetch.L2: no registers, no completion to wait for). The
-// current row block's loads then hit L2, and they are issued together per tile (up to four
-// levels at once), never one dependent load per entry.
+// Latency. A row block's descriptors and precisions are loaded lane-parallel one row block
+// ahead (lane i holding tile i), and a tile's loads are issued together (up to four levels at
+// once) before its first product. Single-entry tiles are the exception the plan isolates:
+// each needs its own column before its precision, value and x entry can be fetched, a chain
+// of dependent loads per entry. So a warp stages the next row block's single-entry operands in
+// shared memory with per-lane asynchronous copies (cp.async: both values, the x entry in all
+// three formats and the 4-byte word holding its precision code), from columns loaded two row
+// blocks ahead; the owner lanes then read them from shared memory. Completion is the copies'
+// own group count (cp.async.wait_group): no device-side wait.
 //
 // x. A tile's 32 x entries (its column block) are one coalesced load, one per lane, in the
 // tile's format (FP64 x, or the scaled FP32 / BF16 copies); a slot takes its entry with a
@@ -34,7 +36,8 @@ namespace {
 constexpr unsigned kAll = 0xffffffffu;
 constexpr unsigned kCbMask = (1u << 26) - 1u;
 constexpr int kRbMinBlocks = 4;   // resident blocks of kRbThreads per SM the registers are sized for
-constexpr int kSgUnroll = 2;      // single-entry tiles of a row loaded together
+constexpr int kSgUnroll = 2;      // single-entry tiles of a row loaded together (unstaged path)
+constexpr unsigned kSgMax = 32;   // ELL slots of a row block staged in shared memory (more: unstaged)
 
 __device__ __forceinline__ unsigned lanemask_lt()
 {
@@ -43,12 +46,42 @@ __device__ __forceinline__ unsigned lanemask_lt()
     return m;
 }
 
-// Prefetch [p, p + bytes) into L2; p and bytes are multiples of 16 and the range lies inside
-// one allocation.
-__device__ __forceinline__ void prefetch_l2(const void *p, unsigned bytes)
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Asynchronous global -> shared copies of 4 and 8 bytes; completion by group count.
+__device__ __forceinline__ void cp4(uint32_t dst, const void *src)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp8(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ unsigned lds_u32(uint32_t a)
+{
+    unsigned v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ double lds_f64(uint32_t a)
+{
+    double v;
+    asm volatile("ld.shared.f64 %0, [%1];" : "=d"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t a, unsigned v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+// Staged single-entry operands of one row block (ELL slot e < kSgMax), as arrays: FP64 value
+// and x at 8e and 256 + 8e, FP32 value and x at 512 + 4e and 640 + 4e, the 4-byte words
+// holding the BF16 value and the precision code at 768 + 4e and 1024 + 4e, the BF16 x at
+// 896 + 4e, and the slot's code word at 1152 + 4e (bit 0: an entry; bit 1: the BF16 half;
+// bits 2-3: the precision's byte in its word).
+constexpr unsigned kSgBuf = 1280;
 
 template <int PR> struct Fmt;
 template <> struct Fmt<EVOCG_FP64> {
@@ -151,8 +184,9 @@ __device__ __forceinline__ void run_tiles(const SpmvLaunch &L, const uint4 &d, i
     }
 }
 
-// The row block's single-entry tiles: a lane whose row has some walks its ELL row, kSgUnroll
-// entries at a time (columns and tile indices first, then precisions, then values and x).
+// The row block's single-entry tiles read from global memory (a row block with more ELL slots
+// than a buffer holds): a lane whose row has some walks its ELL row, kSgUnroll entries at a
+// time (columns and tile indices first, then precisions, then values and x).
 template <bool FORCE64>
 __device__ __forceinline__ void run_singles(const SpmvLaunch &L, unsigned sg0, unsigned hs, unsigned ws,
                                             int lane, unsigned ltm, double &acc, F32Pair &lp,
@@ -208,9 +242,38 @@ __device__ __forceinline__ void run_singles(const SpmvLaunch &L, unsigned sg0, u
     }
 }
 
+// The staged single-entry tiles of a row block: owner lanes walk their ELL row in the buffer.
+template <bool FORCE64>
+__device__ __forceinline__ void staged_singles(uint32_t sb, unsigned hs, unsigned ws, int lane, unsigned ltm,
+                                               double &acc, F32Pair &lp, unsigned (&cnt)[3])
+{
+    if (!((hs >> lane) & 1u)) return;
+    const unsigned hc = __popc(hs), j = __popc(hs & ltm);
+    for (unsigned k = 0; k < ws; ++k) {
+        const unsigned e = k * hc + j;
+        const unsigned code = lds_u32(sb + 1152u + 4u * e);
+        if (!(code & 1u)) continue;   // a pad
+        const int prec = FORCE64 ? EVOCG_FP64
+                                 : (int)((lds_u32(sb + 1024u + 4u * e) >> (8u * ((code >> 2) & 3u))) & 0xFFu);
+        if (prec == EVOCG_FP64) {
+            acc = fma(lds_f64(sb + 8u * e), lds_f64(sb + 256u + 8u * e), acc);
+            ++cnt[0];
+        } else if (prec == EVOCG_FP32) {
+            lp.add_prod(__uint_as_float(lds_u32(sb + 512u + 4u * e)), __uint_as_float(lds_u32(sb + 640u + 4u * e)));
+            ++cnt[1];
+        } else {
+            const unsigned w = lds_u32(sb + 768u + 4u * e);
+            const float a = f32_from_bf16((uint16_t)((code & 2u) ? (w >> 16) : (w & 0xFFFFu)));
+            lp.add(__fmul_rn(a, __uint_as_float(lds_u32(sb + 896u + 4u * e))));
+            ++cnt[2];
+        }
+    }
+}
+
 template <bool FORCE64, bool DOT>
 __global__ void __launch_bounds__(kRbThreads, kRbMinBlocks) spmv_rowblock_kernel(SpmvLaunch L)
 {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     if ((DOT || L.gate) && L.st->done) return;  // a stopped solve: nothing to compute or count
     const TilesView &A = L.A;
     const int lane = threadIdx.x & 31;
@@ -221,6 +284,7 @@ __global__ void __launch_bounds__(kRbThreads, kRbMinBlocks) spmv_rowblock_kernel
     const int64_t nrb = A.nrb;
     double dotp = 0.0;
     unsigned cnt[3] = {0u, 0u, 0u};
+    const uint32_t sgbuf = smem_u32(smem_raw) + (uint32_t)(threadIdx.x >> 5) * 2u * kSgBuf;
 
     // meta words of a row block, one per lane: lanes 0-3 hold meta[rb] (first descriptor,
     // first single slot, single rows, singles per row), lane 4 meta[rb + 1]'s first descriptor
@@ -237,14 +301,42 @@ __global__ void __launch_bounds__(kRbThreads, kRbMinBlocks) spmv_rowblock_kernel
         if (rb < nrb && (unsigned)lane < nt) d = __ldcs(A.rgDesc + r0 + lane);
         return d;
     };
-    auto prefetch = [&](int64_t rb, unsigned m, const uint4 &d, int pr) {
-        const unsigned nt = ntiles(m);
-        if (rb >= nrb || (unsigned)lane >= nt) return;
-        const unsigned m16 = ((d.y >> 26) * (unsigned)__popc(d.z) + 15u) & ~15u;
-        if (pr == EVOCG_FP64) prefetch_l2(A.v64 + d.x, m16 * 8u);
-        else if (pr == EVOCG_FP32) prefetch_l2(A.v32 + d.x, m16 * 4u);
-        else prefetch_l2(A.v16 + d.x, m16 * 2u);
-        prefetch_l2(A.colIdx + d.x, m16);
+    auto nslots = [&](unsigned m) { return __popc(__shfl_sync(kAll, m, 2)) * __shfl_sync(kAll, m, 3); };
+    // a row block's single-entry columns and tiles, lane e holding ELL slot e (when it has at
+    // most kSgMax slots: those are staged)
+    auto sgload = [&](int64_t rb, unsigned m, int &col, int &tile) {
+        const unsigned sg0 = __shfl_sync(kAll, m, 1), ns = nslots(m);
+        col = -1;
+        tile = 0;
+        if (rb < nrb && ns <= kSgMax && (unsigned)lane < ns) {
+            col = __ldg(A.sgCol + sg0 + lane);
+            if (!FORCE64 && !L.map_kind) tile = __ldg(A.sgTile + sg0 + lane);
+        }
+    };
+    // issue the copies of a row block's single-entry operands into buffer sb (one group)
+    auto stage = [&](int64_t rb, unsigned m, int col, int tile, uint32_t sb) {
+        const unsigned sg0 = __shfl_sync(kAll, m, 1), ns = nslots(m);
+        if (rb < nrb && ns <= kSgMax && (unsigned)lane < ns) {
+            const unsigned e = (unsigned)lane, g = sg0 + e;
+            unsigned code = 0u;
+            if (col >= 0) {
+                cp8(sb + 8u * e, A.sgV64 + g);
+                cp8(sb + 256u + 8u * e, L.x64 + col);
+                unsigned key = 0u;
+                if (!FORCE64) {   // an all-FP64 product reads no low-precision operand (x32 and
+                                  // x16f may not exist for it)
+                    cp4(sb + 512u + 4u * e, A.sgV32 + g);
+                    cp4(sb + 640u + 4u * e, L.x32 + col);
+                    cp4(sb + 768u + 4u * e, A.sgV16 + (g & ~1u));
+                    cp4(sb + 896u + 4u * e, L.x16f + col);
+                    key = L.map_kind ? ((unsigned)col >> 5) : (unsigned)tile;
+                    cp4(sb + 1024u + 4u * e, L.prec + (key & ~3u));
+                }
+                code = 1u | ((g & 1u) << 1) | ((key & 3u) << 2);
+            }
+            sts_u32(sb + 1152u + 4u * e, code);
+        }
+        cp_commit();
     };
 
     int64_t rb = wid;
@@ -254,14 +346,27 @@ __global__ void __launch_bounds__(kRbThreads, kRbMinBlocks) spmv_rowblock_kernel
     unsigned m1 = meta(rb + nw);
     unsigned m2 = meta(rb + 2 * nw);
     uint4 d1 = descs(rb + nw, m1);
+    int sc, st;   // single-entry columns and tiles of the row block after the next one
+    sgload(rb, m0, sc, st);
+    stage(rb, m0, sc, st, sgbuf);
+    sgload(rb + nw, m1, sc, st);
+    unsigned buf = 0u;
     while (rb < nrb) {
         const int p1 = desc_prec<FORCE64>(L, d1, rb + nw < nrb && (unsigned)lane < ntiles(m1));
+        stage(rb + nw, m1, sc, st, sgbuf + (buf ^ 1u) * kSgBuf);   // the next row block's singles
+        sgload(rb + 2 * nw, m2, sc, st);
         double acc = 0.0;
         F32Pair lp;
         const unsigned nt = ntiles(m0);
-        run_singles<FORCE64>(L, __shfl_sync(kAll, m0, 1), __shfl_sync(kAll, m0, 2),
-                             __shfl_sync(kAll, m0, 3), lane, ltm, acc, lp, cnt);
-        prefetch(rb + nw, m1, d1, p1);
+        const unsigned hs = __shfl_sync(kAll, m0, 2), ws = __shfl_sync(kAll, m0, 3);
+        if (__popc(hs) * ws <= kSgMax) {
+            cp_wait1();   // this row block's copies (the older group) have landed
+            __syncwarp();
+            staged_singles<FORCE64>(sgbuf + buf * kSgBuf, hs, ws, lane, ltm, acc, lp, cnt);
+        } else {
+            run_singles<FORCE64>(L, __shfl_sync(kAll, m0, 1), hs, ws, lane, ltm, acc, lp, cnt);
+        }
+        __syncwarp();   // the buffer is refilled two row blocks later
         run_tiles<FORCE64>(L, d0, p0, nt < 32u ? (int)nt : 32, lane, ltm, acc, lp, cnt);
         for (unsigned c0 = 32; c0 < nt; c0 += 32) {   // a row block of more than 32 regular tiles
             const unsigned r0 = __shfl_sync(kAll, m0, 0);
@@ -279,6 +384,7 @@ __global__ void __launch_bounds__(kRbThreads, kRbMinBlocks) spmv_rowblock_kernel
             if (DOT) dotp = fma(__ldg(L.x64 + row), y, dotp);
         }
         rb += nw;
+        buf ^= 1u;
         m0 = m1;
         d0 = d1;
         p0 = p1;
@@ -304,13 +410,15 @@ __global__ void __launch_bounds__(kRbThreads, kRbMinBlocks) spmv_rowblock_kernel
     }
 }
 
+constexpr size_t kRbSmem = (size_t)(kRbThreads / 32) * 2u * kSgBuf;
+
 }  // namespace
 
 int rowblock_grid_for(int sms)
 {
     int per = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_rowblock_kernel<false, true>, kRbThreads, 0) !=
-            cudaSuccess || per < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, spmv_rowblock_kernel<false, true>, kRbThreads,
+                                                      kRbSmem) != cudaSuccess || per < 1)
         per = 1;
     cudaGetLastError();
     const int g = sms * per;
@@ -322,11 +430,11 @@ cudaError_t launch_spmv_rowblock(const SpmvLaunch &L, cudaStream_t s)
     const int g = L.A.rb_grid;
     if (g <= 0 || !L.A.rbMeta) return cudaErrorInvalidValue;
     if (L.force64) {
-        if (L.dot) spmv_rowblock_kernel<true, true><<<g, kRbThreads, 0, s>>>(L);
-        else spmv_rowblock_kernel<true, false><<<g, kRbThreads, 0, s>>>(L);
+        if (L.dot) spmv_rowblock_kernel<true, true><<<g, kRbThreads, kRbSmem, s>>>(L);
+        else spmv_rowblock_kernel<true, false><<<g, kRbThreads, kRbSmem, s>>>(L);
     } else {
-        if (L.dot) spmv_rowblock_kernel<false, true><<<g, kRbThreads, 0, s>>>(L);
-        else spmv_rowblock_kernel<false, false><<<g, kRbThreads, 0, s>>>(L);
+        if (L.dot) spmv_rowblock_kernel<false, true><<<g, kRbThreads, kRbSmem, s>>>(L);
+        else spmv_rowblock_kernel<false, false><<<g, kRbThreads, kRbSmem, s>>>(L);
     }
     return cudaGetLastError();
 }

@@ -80,9 +80,9 @@ def main(argv=None):
             else:
                 mp = np.zeros(G.ntiles, np.uint8)
             evocg.set_tile_precision(G, mp)
-            evocg.spmv(G, x, y)
             kflag = {"default": 0, "direct": evocg.SPMV_DIRECT, "panel": evocg.SPMV_PANEL,
                      "rowblock": evocg.SPMV_ROWBLOCK}[a.kernel]
+            evocg.spmv_ex(G, x, y, kflag)   # makes the x copies the kernel reads, if any
             flags = evocg.SPMV_REUSE_XCOPIES | kflag
             if a.launches:
                 for _ in range(a.launches):

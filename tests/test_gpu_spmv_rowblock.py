@@ -90,3 +90,22 @@ def test_rowblock_spmv_parity_full_size(cfg):
         want = oracle.mixed_spmv(P.A, P.t, mp, xh)
         err = row_rel_err(y, want, P.abs_sum(mp, xh))
         assert err.max() <= tol, (err.max(), int(err.argmax()))
+
+
+def test_rowblock_fp64_variants_in_a_solve():
+    """A solve with the FP64 finish runs the kernel's all-FP64 variants (the restart product
+    q = A x and the FP64 true residual) besides the mixed one, here on a matrix whose row
+    blocks have single-entry tiles: the solve reaches rtol in the oracle's FP64 residual."""
+    n, rp, ci, v = W.aniso2d_q1_9pt(70)
+    P = Pair((n, rp, ci, v), 32)
+    evocg.set_tile_precision(P.G, P.tile_map(2, (0.2, 0.3, 0.5)))
+    b = np.random.default_rng(3).uniform(-1, 1, n)
+    x = np.empty(n)
+    info = evocg.cg_solve(P.G, b, x, 1e-8, 20000, True, None, True)
+    assert info["status"] == evocg.OK, info
+    assert oracle.true_residual(P.A, b, x) <= 1e-8
+    for it in range(2):   # and the all-FP64 product alone, against the oracle
+        xh = np.random.default_rng(it).standard_normal(n)
+        y = _run(P, torch.from_numpy(xh).cuda(), np.zeros(P.t.ntiles, np.uint8))
+        want = oracle.mixed_spmv(P.A, P.t, None, xh)
+        assert row_rel_err(y, want, P.abs_sum(np.zeros(P.t.ntiles, np.uint8), xh)).max() <= TOL64
