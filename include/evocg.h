@@ -303,7 +303,9 @@ int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int flags, void *
  * module anew); make that first call before any stream capture. Every call shares the
  * one array and overwrites all of it that it reads, so no state carries over between calls,
  * but calls that may overlap on the GPU (concurrent streams, or several handles at once)
- * race on it: order them. Asynchronous on `stream`.
+ * race on it: order them. It runs only SpMV kernels without device-side waits (the
+ * row-block kernel for tiles of 32, the direct kernel for the other sizes), so no stage
+ * wait can run out unreported. Asynchronous on `stream`.
  */
 int evocg_spmv_noalloc(evocg_tiles_t A, const double *x, double *y, void *stream);
 

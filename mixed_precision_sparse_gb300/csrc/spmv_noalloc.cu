@@ -123,6 +123,8 @@ extern "C" int evocg_spmv_noalloc(evocg_tiles_t A, const double *x, double *y, v
     S.st = nullptr;
     S.census = 0;
     S.grid = A->spmv_grid;
+    // only kernels without device waits: a lost wait could not be reported by this call
+    S.direct = evocg::spmv_kind_for(A->view(), 0, 0) == evocg::SPMV_KIND_PANEL ? 1 : 0;
     e = evocg::launch_spmv(S, s);
     if (e != cudaSuccess) return evocg::cuda_fail(e, "launch spmv (allocation-free)");
     return EVOCG_OK;

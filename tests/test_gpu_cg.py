@@ -248,12 +248,15 @@ def _golden_iterations():
         return json.load(f)
 
 
-@pytest.mark.parametrize("cfg", [2, 3])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
 def test_cg_full_solve_matches_oracle_count(cfg):
-    """Full-size workloads solved to rtol exactly as the benchmark configures them (solver,
-    map or controller, FP64 finish): the iteration count is within 3% of the oracle's full
-    solve (stored by tests/golden/make_oracle_iterations.py, which calls only the oracle)
-    and the FP64 true residual, recomputed by the oracle from the GPU's x, is <= rtol."""
+    """Full-size workloads solved exactly as the benchmark configures them (solver, map or
+    controller, FP64 finish, maxit) against the oracle's full solve, stored by
+    tests/golden/make_oracle_iterations.py (which calls only the oracle): the same status;
+    iteration counts (in total and at the first recursive convergence) within 3%; for static
+    maps the first 200 entries of the residual history within 1e-6 (the same operator: only
+    summation orders differ); a converged solve's FP64 true residual, recomputed by the oracle
+    from the GPU's x, <= rtol, and one stopped at maxit within 1% of the oracle's."""
     gold = _golden_iterations().get(str(cfg))
     if gold is None:
         pytest.skip(f"no oracle full-solve count stored for workload {cfg}")
@@ -266,7 +269,16 @@ def test_cg_full_solve_matches_oracle_count(cfg):
     else:
         ctrl = None
         evocg.set_tile_precision(P.G, P.tile_map(w.map_seed))
-    info, x, _ = _solve(P, w.b, w.rtol, w.maxit, w.jacobi, ctrl, True)
-    assert info["status"] == gold["status"] == evocg.OK, (info, gold)
+    info, x, h = _solve(P, w.b, w.rtol, w.maxit, w.jacobi, ctrl, True)
+    assert info["status"] == gold["status"], (info, gold)
     assert abs(info["iters"] - gold["iters"]) <= max(2, 0.03 * gold["iters"]), (info, gold)
-    assert oracle.true_residual(P.A, w.b, x) <= w.rtol
+    assert abs(info["iters_recursive"] - gold["iters_rec"]) <= max(2, 0.03 * gold["iters_rec"]), (info, gold)
+    if ctrl is None:
+        head = np.asarray(gold["hist_head"])
+        k = min(len(head), len(h))
+        assert np.max(np.abs(h[:k] - head[:k]) / head[:k]) <= 1e-6
+    tr = oracle.true_residual(P.A, w.b, x)
+    if gold["status"] == evocg.OK:
+        assert tr <= w.rtol
+    else:
+        assert abs(tr - gold["true_res"]) <= 1e-2 * gold["true_res"], (tr, gold["true_res"])
