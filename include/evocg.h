@@ -88,6 +88,10 @@ typedef struct {
                               of EvoCG §3.4 interval reuse: log with kstar = 1, then choose the
                               interval with evocg_kstar_select. Ignored for EVOCG_CTRL_STATIC */
     int64_t map_log_rows;
+    int eps_relative;      /* THRESHOLD: 0 (the default) applies eps as an absolute bound, as
+                              EvoCG §4.7 states the rule; 1 scales both cut points by
+                              ||r_0||_inf = ||b||_inf (x0 = 0), an option beside the paper's
+                              rule. Ignored by evocg_ctrl_decide */
 } evocg_ctrl;
 
 typedef struct {
@@ -230,6 +234,21 @@ int evocg_rowblock_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *c
                              int64_t *nsingle_slots, int *valid);
 
 /*
+ * The row-ELL SpMV's plan for a matrix, computed on the HOST only (no GPU), for inspection.
+ * The paper has no counterpart. It exists for tiles of 64 holding at most 1.5 entries per
+ * nonempty tile row (random banded matrices): each row block's entries laid out by row, an
+ * ELL block of width = its longest row, every slot with its absolute column, its tile and
+ * the tile slot's three values.
+ *   *nslots receives the ELL slots (pads included), *valid 1 when the plan exists and passes
+ *   the checks the library applies before using it (every row's entries, in column order,
+ *   with their tiles and values), 0 otherwise (the reason is in evocg_last_error). Each
+ *   pointer may be NULL.
+ * Errors: as evocg_tile_build.
+ */
+int evocg_rowell_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *col_idx,
+                           const double *vals, int tile_size, int64_t *nslots, int *valid);
+
+/*
  * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
  *   map: host or device, len = ntiles (PER_TILE) or nrb (PER_COLBLOCK).
  * The SpMV and static-map solves read the map set last. Errors: EINVAL on a wrong length
@@ -261,7 +280,7 @@ enum {
     EVOCG_SPMV_DIRECT = 2,        /* run the direct kernel: a warp per row block, every operand
                                      loaded by the lanes from global memory, one tile after
                                      the other (the kernel for tiles of 64). At most one of
-                                     DIRECT, PANEL, ROWBLOCK may be set */
+                                     DIRECT, PANEL, ROWBLOCK, ROWELL may be set */
     EVOCG_SPMV_PANEL = 8,         /* run the panel kernel (the default for tiles of 16):
                                      a warp streams batches of tiles of consecutive row blocks
                                      through two shared-memory stages, every tile's own lane
@@ -272,6 +291,9 @@ enum {
                                      path of a lost stage wait runs; the call must then return
                                      EVOCG_ETIMEOUT (host pointers) and the handle's error word
                                      is cleared by that report */
+    EVOCG_SPMV_ROWELL = 64,        /* run the row-ELL kernel (the default for tiles of 64 that
+                                     hold at most 1.5 entries per nonempty tile row): each row
+                                     block's entries laid out by row, lanes owning rows */
     EVOCG_SPMV_ROWBLOCK = 32       /* run the row-block kernel (the default for tiles of 32): a
                                      warp per row block, lane l owning row l; regular tiles from
                                      16-byte descriptors, the single-entry tiles of the row block

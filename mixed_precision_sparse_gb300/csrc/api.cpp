@@ -188,6 +188,8 @@ int build_graph(CgLaunch L, int restart, cudaGraph_t *graph_out, cudaGraphExec_t
         S.census = 0; S.grid = L.spmv_grid;
         e = launch_spmv(S, cs);
     }
+    if (e == cudaSuccess && !restart && L.ctrl == EVOCG_CTRL_THRESHOLD && L.eps_relative)
+        e = launch_threshold_scale(L, cs);
     if (e == cudaSuccess) e = launch_cg_init(L, restart, cs);
     // cudaGraphNodeParams has no default constructor in C++ (a union member has one);
     // zeroed storage is its documented initial state.
@@ -257,6 +259,8 @@ int run_plain(evocg_tiles *A, CgLaunch L, int restart, cudaStream_t s)
         S.census = 0; S.grid = L.spmv_grid;
         CK(launch_spmv(S, s), "spmv (restart)");
     }
+    if (!restart && L.ctrl == EVOCG_CTRL_THRESHOLD && L.eps_relative)
+        CK(launch_threshold_scale(L, s), "threshold scale");
     CK(launch_cg_init(L, restart, s), "cg init");
     for (;;) {
         CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");
@@ -371,6 +375,23 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
             if (e == cudaSuccess) A->rb_grid = rowblock_grid_for(sms);
         }
     }
+    // row-ELL SpMV plan (tiles of 64 holding about one entry per row)
+    if (e == cudaSuccess && H.nrb > 0 && rowell_wanted(H)) {
+        RowEllPlan P;
+        std::string why;
+        if (rowell_plan(H, &P, &why) && rowell_plan_ok(H, P, &why)) {
+            A->el_slots = P.base.back();
+            up(&A->elBase, P.base.data(), (int64_t)P.base.size());
+            up(&A->elCol, P.col.data(), (int64_t)P.col.size());
+            up(&A->elTile, P.tile.data(), (int64_t)P.tile.size());
+            up(&A->elV64, P.v64.data(), (int64_t)P.v64.size());
+            up(&A->elV32, P.v32.data(), (int64_t)P.v32.size());
+            up(&A->elV16, P.v16.data(), (int64_t)P.v16.size());
+            if (e == cudaSuccess) e = dalloc(&A->elPrec, A->el_slots);
+            if (e == cudaSuccess) e = cudaMemset(A->elPrec, 0, (size_t)(A->el_slots > 0 ? A->el_slots : 1));
+            if (e == cudaSuccess) A->el_grid = rowell_grid_for(sms);
+        }
+    }
     if (e == cudaSuccess) e = dalloc(&A->errw, 1);
     if (e == cudaSuccess) e = cudaMemset(A->errw, 0, sizeof(int));
     H.release();
@@ -395,6 +416,7 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
         if (!std::strcmp(k, "direct")) A->spmv_kind = SPMV_KIND_DIRECT;
         else if (!std::strcmp(k, "panel")) A->spmv_kind = SPMV_KIND_PANEL;
         else if (!std::strcmp(k, "rowblock")) A->spmv_kind = SPMV_KIND_ROWBLOCK;
+        else if (!std::strcmp(k, "rowell")) A->spmv_kind = SPMV_KIND_ROWELL;
     }
     A->vec_grid = sms * 4 > kMaxBlocks ? kMaxBlocks : sms * 4;
     *out = A;
@@ -411,6 +433,8 @@ extern "C" int evocg_tiles_free(evocg_tiles_t A)
     dfree(A->errw); dfree(A->pdesc); dfree(A->warpRec); dfree(A->panelRec); dfree(A->recPrec);
     dfree(A->rbMeta); dfree(A->rgDesc); dfree(A->sgCol); dfree(A->sgTile); dfree(A->sgV64);
     dfree(A->sgV32); dfree(A->sgV16);
+    dfree(A->elBase); dfree(A->elCol); dfree(A->elTile); dfree(A->elPrec); dfree(A->elV64);
+    dfree(A->elV32); dfree(A->elV16);
     dfree(A->colIdx); dfree(A->v64); dfree(A->v32); dfree(A->v16); dfree(A->colExp);
     dfree(A->tilePrec); dfree(A->cbPrec); dfree(A->dinv); dfree(A->x32); dfree(A->x16f);
     dfree(A->xstage); dfree(A->ystage);
@@ -489,6 +513,8 @@ extern "C" int evocg_set_tile_precision(evocg_tiles_t A, const uint8_t *map, int
             for (int64_t t = 0; t < len; ++t) rp[(size_t)A->tileRec[(size_t)t]] = h[(size_t)t];
             CK(cudaMemcpyAsync(A->recPrec, rp.data(), rp.size(), cudaMemcpyHostToDevice, s), "upload map");
         }
+        if (map_kind == EVOCG_MAP_PER_TILE && A->elTile)   // the per-slot copy of the row-ELL plan
+            CK(launch_elprec(A->el_slots, A->elTile, A->tilePrec, A->elPrec, s), "per-slot map");
         CK(cudaStreamSynchronize(s), "synchronise");
     }
     A->map_kind = map_kind;
@@ -520,9 +546,9 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
 {
     g_err.clear();
     if (!A || (A->n > 0 && (!x || !y))) return fail(EVOCG_EINVAL, "NULL argument");
-    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL | EVOCG_SPMV_ROWBLOCK);
+    const int kflags = flags & (EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL | EVOCG_SPMV_ROWBLOCK | EVOCG_SPMV_ROWELL);
     if (flags & ~(EVOCG_SPMV_REUSE_XCOPIES | EVOCG_SPMV_DIRECT | EVOCG_SPMV_PANEL | EVOCG_SPMV_TEST_LOST_WAIT |
-                  EVOCG_SPMV_ROWBLOCK))
+                  EVOCG_SPMV_ROWBLOCK | EVOCG_SPMV_ROWELL))
         return fail(EVOCG_EINVAL, "unknown flags");
     if (kflags & (kflags - 1)) return fail(EVOCG_EINVAL, "at most one kernel flag");
     if (A->n == 0) return EVOCG_OK;
@@ -532,7 +558,8 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     if (reuse && (!xdev || !ydev))
         return fail(EVOCG_EINVAL, "EVOCG_SPMV_REUSE_XCOPIES needs device x and y");
     const int kdirect = (flags & EVOCG_SPMV_DIRECT) ? 1 : 0;
-    const int kkind = (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : (flags & EVOCG_SPMV_ROWBLOCK) ? SPMV_KIND_ROWBLOCK : 0;
+    const int kkind = (flags & EVOCG_SPMV_PANEL) ? SPMV_KIND_PANEL : (flags & EVOCG_SPMV_ROWBLOCK) ? SPMV_KIND_ROWBLOCK
+                      : (flags & EVOCG_SPMV_ROWELL) ? SPMV_KIND_ROWELL : 0;
     if (reuse && !A->xcopies_valid)
         return fail(EVOCG_EINVAL, "EVOCG_SPMV_REUSE_XCOPIES: no earlier SpMV made the copies");
     const size_t bytes = sizeof(double) * (size_t)A->n;
@@ -688,6 +715,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     CgLaunch L{};
     L.A = A->view();
     L.n = n; L.T = A->T; L.jacobi = jacobi ? 1 : 0; L.ctrl = kind; L.dinv = A->dinv;
+    L.eps_relative = (kind == EVOCG_CTRL_THRESHOLD && ctrl->eps_relative) ? 1 : 0;
     L.b = w.b; L.x = w.x; L.r = w.r; L.p = w.p; L.q = w.q; L.z = w.z;
     L.x32 = A->x32; L.x16f = A->x16f; L.hist = w.hist; L.partials = w.partials; L.pq = w.pq;
     L.cbPrec = w.cbPrec;

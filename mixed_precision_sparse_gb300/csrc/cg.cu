@@ -100,6 +100,47 @@ __device__ __forceinline__ void write_copies2(const CgLaunch &L, int64_t j, doub
                     __fmul_rn(f32_from_bf16(bf16_from_f64_rn(v1)), s1));
 }
 
+// The relative threshold option: both cut points times ||b||_inf (= ||r_0||_inf with x0 = 0),
+// before the first decision. Block maxima of |b| through the bit patterns (non-negative
+// doubles order like their patterns), the last block scales.
+__global__ void __launch_bounds__(kVecThreads) threshold_scale_kernel(CgLaunch L)
+{
+    DevState *st = L.st;
+    uint64_t m = 0;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < L.n; j += (int64_t)gridDim.x * blockDim.x) {
+        const uint64_t a = abs_bits(L.b[j]);
+        m = a > m ? a : m;
+    }
+    for (int o = 16; o; o >>= 1) {
+        const uint64_t t = __shfl_xor_sync(0xffffffffu, m, o);
+        m = t > m ? t : m;
+    }
+    __shared__ uint64_t wm[kVecThreads / 32];
+    if ((threadIdx.x & 31) == 0) wm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int i = 1; i < kVecThreads / 32; ++i) m = wm[i] > m ? wm[i] : m;
+        L.partials[blockIdx.x] = __longlong_as_double((long long)m);
+    }
+    if (last_block_cg(st, TK_SCALE) && threadIdx.x == 0) {
+        uint64_t g = 0;
+        for (int i = 0; i < (int)gridDim.x; ++i) {
+            const uint64_t v = (uint64_t)__double_as_longlong(__ldcg(L.partials + i));
+            g = v > g ? v : g;
+        }
+        const double binf = __longlong_as_double((long long)g);
+        st->tickets[TK_SCALE] = 0;
+        st->eps_hi *= binf;
+        st->eps_lo = 0.1 * st->eps_hi;   // 0.1 eps' with eps' = eps ||b||_inf, as the host forms 0.1 eps
+    }
+}
+
+cudaError_t launch_threshold_scale(const CgLaunch &L, cudaStream_t s)
+{
+    threshold_scale_kernel<<<L.vec_grid, kVecThreads, 0, s>>>(L);
+    return cudaGetLastError();
+}
+
 // Start (restart = 0) or FP64-finish restart (restart = 1, after q = A x in FP64):
 //   r = b (x = 0) or r = b - q; z = D^-1 r; p = z; rho = r.z; ||r||^2.
 template <int T>

@@ -22,6 +22,7 @@ constexpr int kSlack = 16;            // bytes past the end of every device arra
 constexpr int kPanelThreads = 128;    // threads per block of the panel SpMV
 constexpr int kPanelVariants = 4;     // (tiles issued together, blocks per SM) variants built
 constexpr int kRbThreads = 256;       // threads per block of the row-block SpMV
+constexpr int kElThreads = 256;       // threads per block of the row-ELL SpMV
 
 // Device-resident solver state; one per handle. Written by the last block of each
 // reducing kernel, read by every block of the next kernel.
@@ -46,7 +47,7 @@ struct DevState {
 };
 
 // ticket slots
-enum { TK_SPMV = 0, TK_UPDATE = 1, TK_INIT = 2, TK_TRUE = 3 };
+enum { TK_SPMV = 0, TK_UPDATE = 1, TK_INIT = 2, TK_TRUE = 3, TK_SCALE = 4 };
 
 // Everything the SpMV reads from the tile structure.
 struct TilesView {
@@ -85,13 +86,23 @@ struct TilesView {
     const float *sgV32;
     const uint16_t *sgV16;
     int rb_grid;
+    // row-ELL SpMV (tiles of 64 with about one entry per row): block bases (nrb + 1) and the
+    // slots' columns, per-slot precision codes and values (rowell_plan.cpp); el_grid 0: no plan
+    const int64_t *elBase;
+    const int32_t *elCol;
+    const uint8_t *elPrec;
+    const double *elV64;
+    const float *elV32;
+    const uint16_t *elV16;
+    int el_grid;
 };
 
-// SpMV kernels: the row-block kernel (spmv_rowblock.cu; tiles of 32), the panel kernel
+// SpMV kernels: the row-block kernel (spmv_rowblock.cu; tiles of 32), the row-ELL kernel
+// (spmv_rowell.cu; tiles of 64 holding about one entry per row), the panel kernel
 // (spmv_panel.cu; tiles of 16 and 32) and the direct kernel (spmv.cu: warp per row block,
-// plain loads; any tile size). AUTO: the row-block kernel where its plan exists, else the
-// panel kernel where its plan exists, else the direct one.
-enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_PANEL = 3, SPMV_KIND_ROWBLOCK = 4 };
+// plain loads; any tile size). AUTO: the row-block or row-ELL kernel where its plan exists,
+// else the panel kernel where its plan exists, else the direct one.
+enum { SPMV_KIND_AUTO = 0, SPMV_KIND_DIRECT = 1, SPMV_KIND_PANEL = 3, SPMV_KIND_ROWBLOCK = 4, SPMV_KIND_ROWELL = 5 };
 
 struct SolveWS {
     int64_t cap_n = 0, cap_ncb = 0;
@@ -150,6 +161,15 @@ struct evocg_tiles {
     float *sgV32 = nullptr;
     uint16_t *sgV16 = nullptr;
     int rb_grid = 0;
+    int64_t *elBase = nullptr;     // row-ELL SpMV plan (see TilesView)
+    int32_t *elCol = nullptr;
+    int32_t *elTile = nullptr;     // the tile of every slot (for the per-slot precision copy)
+    uint8_t *elPrec = nullptr;
+    double *elV64 = nullptr;
+    float *elV32 = nullptr;
+    uint16_t *elV16 = nullptr;
+    int64_t el_slots = 0;
+    int el_grid = 0;
     int *errw = nullptr;           // device error word (a lost stage wait)
     int spmv_kind = 0;             // default SpMV kernel (SPMV_KIND_*)
     uint8_t *tilePrec = nullptr;   // per-tile map
@@ -170,7 +190,8 @@ struct evocg_tiles {
         return evocg::TilesView{n, nrb, ntiles, nslots, T, tileRowPtr, tileColIdx, tileNnzOff,
                                 tileRowIdx, rowMask, tileWidth, colIdx, v64, v32, v16, colExp,
                                 errw, spmv_kind, pdesc, warpRec, panelRec, recPrec, nrec, panel_grid, panel_variant,
-                                rbMeta, rgDesc, sgCol, sgTile, sgV64, sgV32, sgV16, rb_grid};
+                                rbMeta, rgDesc, sgCol, sgTile, sgV64, sgV32, sgV16, rb_grid,
+                                elBase, elCol, elPrec, elV64, elV32, elV16, el_grid};
     }
 };
 
@@ -213,8 +234,9 @@ struct SpmvLaunch {
     const uint8_t *prec;   // tilePrec (map_kind 0) or cbPrec (map_kind 1); ignored if force64
     int map_kind;
     int force64;
-    // p.q for CG (dot != 0): every warp writes the sum over its rows of x_i y_i to pq[warp]
-    // (spmv_dot_partials() of them); the update kernel sums them in warp order
+    // p.q for CG (dot != 0): the sum over rows of x_i y_i, as spmv_dot_partials() partials in
+    // pq (one per warp, or one per block for the row-block kernel); the update kernel sums
+    // them in order
     int dot;
     double *pq;
     double *partials;
@@ -258,6 +280,20 @@ struct RowBlockPlan {
 };
 bool rowblock_plan(const HostTiles &H, RowBlockPlan *out, std::string *why);
 bool rowblock_plan_ok(const HostTiles &H, const RowBlockPlan &P, std::string *why);
+cudaError_t launch_spmv_rowell(const SpmvLaunch &L, cudaStream_t s);
+int rowell_grid_for(int sms);
+cudaError_t launch_elprec(int64_t ns, const int32_t *tile, const uint8_t *tilePrec, uint8_t *out, cudaStream_t s);
+struct RowEllPlan {
+    std::vector<int64_t> base;    // nrb + 1: first slot of every row block's ELL block
+    std::vector<int32_t> col;     // absolute column (-1: pad), slot (k, r) at base + k*T + r
+    std::vector<int32_t> tile;
+    std::vector<double> v64;
+    std::vector<float> v32;
+    std::vector<uint16_t> v16;
+};
+bool rowell_wanted(const HostTiles &H);   // tiles of 64 with at most 1.5 entries per nonempty tile row
+bool rowell_plan(const HostTiles &H, RowEllPlan *out, std::string *why);
+bool rowell_plan_ok(const HostTiles &H, const RowEllPlan &P, std::string *why);
 
 cudaError_t launch_xcopies(const TilesView &A, const double *x, float *x32, float *x16f,
                            int grid, cudaStream_t s);
@@ -270,6 +306,7 @@ struct CgLaunch {
     int T;
     int jacobi;
     int ctrl;              // EVOCG_CTRL_*
+    int eps_relative;      // threshold cut points scaled by ||b||_inf before the first decision
     const double *dinv;
     double *b, *x, *r, *p, *q, *z;
     float *x32;
@@ -292,6 +329,7 @@ struct CgLaunch {
     int use_cond;          // 1 inside the solve graph: the kernels drive its while node
 };
 cudaError_t launch_cg_init(const CgLaunch &L, int restart, cudaStream_t s);
+cudaError_t launch_threshold_scale(const CgLaunch &L, cudaStream_t s);
 cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s);
 cudaError_t launch_true_residual(const CgLaunch &L, cudaStream_t s);
 cudaError_t launch_ctrl_threshold(const TilesView &A, const double *p, double eps_lo,

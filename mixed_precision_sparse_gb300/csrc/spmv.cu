@@ -1,9 +1,10 @@
 // spmv.cu -- the direct tile-wise mixed-precision SpMV (EvoCG, "Self-Evolving Precision
 // Control for Faster Conjugate Gradient", §3.3 EvoSpMV, Eq. 2 / Eq. 5) for sm_103a, the kernel
 // choice, the rounded x copies the SpMV reads, and the device rounding entry point. The
-// row-block kernel (spmv_rowblock.cu, tiles of 32) and the panel kernel (spmv_panel.cu,
-// tiles of 16) run wherever their plans exist; this kernel runs the rest (tiles of 64) and
-// on request.
+// row-block kernel (spmv_rowblock.cu, tiles of 32), the row-ELL kernel (spmv_rowell.cu, sparse
+// tiles of 64) and the panel kernel (spmv_panel.cu, tiles of 16) run wherever their plans
+// exist; this kernel runs the rest (tiles of 64 that hold several entries per row) and on
+// request.
 //
 // Work mapping. A warp owns a row block (T rows) at a time and walks its tiles in
 // ascending column block, so every row is summed in column order. Lane l owns local row
@@ -199,8 +200,10 @@ int spmv_kind_for(const TilesView &A, int direct, int kind)
 {
     if (direct) return SPMV_KIND_DIRECT;
     const int k = kind ? kind : A.spmv_kind;
-    const bool rb = A.rbMeta && A.rb_grid > 0, panel = A.pdesc && A.panel_grid > 0;
+    const bool rb = A.rbMeta && A.rb_grid > 0, el = A.elBase && A.el_grid > 0;
+    const bool panel = A.pdesc && A.panel_grid > 0;
     if ((k == SPMV_KIND_ROWBLOCK || k == SPMV_KIND_AUTO) && rb) return SPMV_KIND_ROWBLOCK;
+    if ((k == SPMV_KIND_ROWELL || k == SPMV_KIND_AUTO) && el) return SPMV_KIND_ROWELL;
     if ((k == SPMV_KIND_PANEL || k == SPMV_KIND_AUTO) && panel) return SPMV_KIND_PANEL;
     return SPMV_KIND_DIRECT;
 }
@@ -210,7 +213,8 @@ static int chosen_kind(const SpmvLaunch &L) { return spmv_kind_for(L.A, L.direct
 int spmv_dot_partials(const SpmvLaunch &L)
 {
     switch (chosen_kind(L)) {
-    case SPMV_KIND_ROWBLOCK: return L.A.rb_grid * (kRbThreads / 32);
+    case SPMV_KIND_ROWBLOCK: return L.A.rb_grid;   // one per block
+    case SPMV_KIND_ROWELL: return L.A.el_grid;     // one per block
     case SPMV_KIND_PANEL: return L.A.panel_grid * (kPanelThreads / 32);
     default: return L.grid * (kSpmvThreads / 32);
     }
@@ -220,6 +224,7 @@ cudaError_t launch_spmv(const SpmvLaunch &L, cudaStream_t s)
 {
     switch (chosen_kind(L)) {
     case SPMV_KIND_ROWBLOCK: return launch_spmv_rowblock(L, s);
+    case SPMV_KIND_ROWELL: return launch_spmv_rowell(L, s);
     case SPMV_KIND_PANEL: return launch_spmv_panel(L, s);
     default: return launch_spmv_direct(L, s);
     }

@@ -404,9 +404,16 @@ __global__ void __launch_bounds__(kRbThreads, kRbMinBlocks) spmv_rowblock_kernel
             if (cnt[2]) atomicAdd(&L.st->census[2], (unsigned long long)cnt[2]);
         }
     }
-    if (DOT) {   // this warp's p.q partial (lanes summed in a fixed tree)
+    if (DOT) {   // this block's p.q partial: lanes in a fixed tree, then the warps in order
+        __shared__ double s_pq[kRbThreads / 32];
         for (int o = 16; o; o >>= 1) dotp += __shfl_xor_sync(kAll, dotp, o);
-        if (lane == 0) L.pq[wid] = dotp;
+        if (lane == 0) s_pq[threadIdx.x >> 5] = dotp;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            double v = 0.0;
+            for (int i = 0; i < kRbThreads / 32; ++i) v += s_pq[i];
+            L.pq[blockIdx.x] = v;
+        }
     }
 }
 

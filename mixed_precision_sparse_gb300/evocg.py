@@ -42,7 +42,8 @@ class TilesDesc(C.Structure):
 class Ctrl(C.Structure):
     _fields_ = [("kind", C.c_int), ("kstar", C.c_int), ("eps", C.c_double),
                 ("hidden1", C.c_int), ("hidden2", C.c_int), ("weights", C.c_void_p),
-                ("delta", C.c_double), ("map_log", C.c_void_p), ("map_log_rows", C.c_int64)]
+                ("delta", C.c_double), ("map_log", C.c_void_p), ("map_log_rows", C.c_int64),
+                ("eps_relative", C.c_int)]
 
     def log_to(self, log) -> "Ctrl":
         """Record the per-iteration column-block maps into `log` (rows x nrb uint8, a numpy
@@ -53,8 +54,10 @@ class Ctrl(C.Structure):
         return self
 
     @staticmethod
-    def threshold(eps: float, kstar: int = 1) -> "Ctrl":
-        return Ctrl(kind=CTRL_THRESHOLD, kstar=kstar, eps=eps)
+    def threshold(eps: float, kstar: int = 1, relative: bool = False) -> "Ctrl":
+        """EvoCG §4.7's rule with eps absolute, or (relative=True, an option beside the paper's
+        rule) with both cut points scaled by ||b||_inf."""
+        return Ctrl(kind=CTRL_THRESHOLD, kstar=kstar, eps=eps, eps_relative=int(bool(relative)))
 
     @staticmethod
     def mlp(weights, kstar: int = 1, delta: float = 1e-30) -> "Ctrl":
@@ -114,6 +117,7 @@ def lib():
                                           C.POINTER(C.c_int)],
                 "evocg_rowblock_plan_host": [i64, P, P, P, i32, C.POINTER(C.c_int64),
                                              C.POINTER(C.c_int64), C.POINTER(C.c_int)],
+                "evocg_rowell_plan_host": [i64, P, P, P, i32, C.POINTER(C.c_int64), C.POINTER(C.c_int)],
                 "evocg_tile_csc_host": [i64, P, P, P, i32, i32, C.POINTER(C.c_int64),
                                         C.POINTER(C.c_int64)] + [P] * 9,
                 "evocg_tiles_export_csc": [P, i32, C.POINTER(C.c_int64)] + [P] * 9,
@@ -306,6 +310,15 @@ def rowblock_plan_host(n, row_ptr, col_idx, vals, tile_size: int):
     return nd.value, ns.value, bool(ok.value)
 
 
+def rowell_plan_host(n, row_ptr, col_idx, vals, tile_size: int):
+    """(ELL slots, valid) of the row-ELL SpMV's plan, on the host."""
+    rp, ci, v = _np(row_ptr, np.int64), _np(col_idx, np.int32), _np(vals, np.float64)
+    ns, ok = C.c_int64(), C.c_int()
+    _check(lib().evocg_rowell_plan_host(int(n), _ptr(rp), _ptr(ci), _ptr(v), int(tile_size),
+                                        C.byref(ns), C.byref(ok)))
+    return ns.value, bool(ok.value)
+
+
 def set_tile_precision(A: Tiles, prec_map, map_kind: int = MAP_PER_TILE, stream=None):
     m = prec_map if hasattr(prec_map, "data_ptr") else _np(prec_map, np.uint8)
     n = m.numel() if hasattr(m, "numel") else m.size
@@ -323,6 +336,7 @@ SPMV_DIRECT = 2
 SPMV_PANEL = 8
 SPMV_TEST_LOST_WAIT = 16
 SPMV_ROWBLOCK = 32
+SPMV_ROWELL = 64
 
 
 def spmv(A: Tiles, x, y, stream=None):

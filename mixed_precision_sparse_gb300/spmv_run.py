@@ -2,7 +2,7 @@
 
     python -m mixed_precision_sparse_gb300.spmv_run [--workloads 2,3,5] [--reps 50]
                                                     [--maps mixed,fp64] [--launches K]
-                                                    [--kernel default|direct|panel|rowblock]
+                                                    [--kernel default|direct|panel|rowblock|rowell]
 
 For each workload: build the tile structure, set the seeded 40/40/20 per-tile map (or the
 all-FP64 map), and launch the SpMV kernel back to back on device-resident x and y (every
@@ -57,7 +57,7 @@ def main(argv=None):
     ap.add_argument("--maps", default="mixed,fp64")
     ap.add_argument("--reps", type=int, default=50)
     ap.add_argument("--launches", type=int, default=0)
-    ap.add_argument("--kernel", default="default", choices=["default", "direct", "panel", "rowblock"],
+    ap.add_argument("--kernel", default="default", choices=["default", "direct", "panel", "rowblock", "rowell"],
                     help="SpMV kernel to time (default: the library's choice)")
     a = ap.parse_args(argv)
     dev = torch.device("cuda", 0)
@@ -81,7 +81,7 @@ def main(argv=None):
                 mp = np.zeros(G.ntiles, np.uint8)
             evocg.set_tile_precision(G, mp)
             kflag = {"default": 0, "direct": evocg.SPMV_DIRECT, "panel": evocg.SPMV_PANEL,
-                     "rowblock": evocg.SPMV_ROWBLOCK}[a.kernel]
+                     "rowblock": evocg.SPMV_ROWBLOCK, "rowell": evocg.SPMV_ROWELL}[a.kernel]
             evocg.spmv_ex(G, x, y, kflag)   # makes the x copies the kernel reads, if any
             flags = evocg.SPMV_REUSE_XCOPIES | kflag
             if a.launches:

@@ -176,6 +176,33 @@ def test_rowblock_plan_is_for_tiles_of_32():
         assert evocg.rowblock_plan_host(n, rp, ci, v, T) == (0, 0, False)
 
 
+def _rowell_slots(n, rp, ci, T=64):
+    """ELL slots of the row-ELL plan counted from the CSR with numpy: per row block, T times
+    its longest row."""
+    per = np.diff(rp)
+    nrb = (n + T - 1) // T
+    return int(sum(T * per[b * T:(b + 1) * T].max(initial=0) for b in range(nrb)))
+
+
+@pytest.mark.parametrize("name,m", [("banded_20k", W.banded_spd(20000, 6, band=700)),
+                                    ("banded_ragged", W.banded_spd(5003, 3, band=3000)),
+                                    ("banded_wide", W.banded_spd(30000, 4, band=4096))])
+def test_rowell_plan_passes_its_checks(name, m):
+    """The row-ELL plan of a matrix of sparse 64 x 64 tiles passes the checks the library
+    applies before using it, with the ELL size counted from the CSR."""
+    n, rp, ci, v = m
+    ns, ok = evocg.rowell_plan_host(n, rp, ci, v, 64)
+    assert ok, evocg.last_error()
+    assert ns == _rowell_slots(n, rp, ci)
+
+
+def test_rowell_plan_only_for_sparse_tiles_of_64():
+    dense = W.dense_to_csr(np.random.default_rng(1).standard_normal((130, 130)) + 300 * np.eye(130))
+    assert evocg.rowell_plan_host(*dense, 64) == (0, False)                 # dense tiles
+    n, rp, ci, v = W.banded_spd(20000, 6, band=700)
+    assert evocg.rowell_plan_host(n, rp, ci, v, 32)[1] is False            # tiles of 32
+
+
 def test_empty_matrix():
     z64, z32, zf = np.zeros(1, np.int64), np.zeros(0, np.int32), np.zeros(0)
     h = evocg.tile_layout_host(0, z64, z32, zf, 16)

@@ -32,9 +32,10 @@ def _tiles_with_map(m, T, seed):
     ("banded_30k", W.banded_spd(30000, 4, band=900), 64),
 ])
 def test_noalloc_matches_regular_spmv_twice(name, m, T):
-    """Two calls in a row (they share the fixed scratch): the same kernels as evocg_spmv, so
-    the same bits; and every row against the oracle at the mixed-map tolerance (1e-6 of the
-    row's absolute sum)."""
+    """Two calls in a row (they share the fixed scratch): the same kernel as evocg_spmv_ex
+    forcing the kernel the allocation-free entry point runs (the direct kernel for tiles of 16,
+    the default otherwise), so the same bits; and every row against the oracle at the
+    mixed-map tolerance (1e-6 of the row's absolute sum)."""
     n, rp, ci, v = m
     G = _tiles_with_map(m, T, 11)
     A = oracle.CSR(n, rp, ci, v)
@@ -47,7 +48,7 @@ def test_noalloc_matches_regular_spmv_twice(name, m, T):
         x = torch.from_numpy(xh).cuda()
         y_ref = torch.empty_like(x)
         y_new = torch.full_like(x, float("nan"))
-        evocg.spmv(G, x, y_ref)
+        evocg.spmv_ex(G, x, y_ref, evocg.SPMV_DIRECT if T == 16 else 0)
         evocg.spmv_noalloc(G, x, y_new)
         torch.cuda.synchronize()
         assert torch.equal(y_new.view(torch.int64), y_ref.view(torch.int64)), call
