@@ -2,6 +2,7 @@
 
 Objects go to mixed_precision_sparse_gb300/_build/, the library next to this file.
 Translation units compile in parallel; a unit is rebuilt when it or a header changed.
+build_probe() builds librates.so, the arithmetic-rate probe (probe/rates.cu; rates.py).
 """
 from __future__ import annotations
 
@@ -18,6 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INC = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libevocg.so")
+PROBE_SRC = os.path.join(HERE, "probe", "rates.cu")
+PROBE_LIB = os.path.join(HERE, "librates.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -94,6 +97,22 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
             raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
         os.replace(tmp, LIB)
     return LIB
+
+
+def build_probe(force: bool = False) -> str:
+    """The arithmetic-rate probe library (not part of the solver)."""
+    deps = [PROBE_SRC, os.path.join(CSRC, "fpconv.cuh")]
+    if not force and os.path.exists(PROBE_LIB) and \
+            all(os.path.getmtime(d) <= os.path.getmtime(PROBE_LIB) for d in deps):
+        return PROBE_LIB
+    tmp = PROBE_LIB + f".tmp{os.getpid()}"
+    cmd = [_nvcc(), *ARCH, "-std=c++17", "-O3", "-lineinfo", "-I", CSRC, "-Xcompiler", "-fPIC", "-shared",
+           "-cudart", "shared", "-o", tmp, PROBE_SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode:
+        raise RuntimeError("probe build failed:\n" + r.stdout + r.stderr)
+    os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
 
 
 if __name__ == "__main__":

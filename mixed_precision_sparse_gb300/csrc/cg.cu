@@ -2,10 +2,10 @@
 // for Faster Conjugate Gradient": the solver lines of Algorithm 1, §2.1 Fig. 1, §3.4
 // fused step, §4.6 Jacobi-PCG) for sm_103a.
 //
-// One iteration is three kernels in a CUDA graph: the SpMV (with one p.q partial per warp),
-// cg_update (alpha from those partials; x, r, z and the two dot products;
+// One iteration is three kernels in a CUDA graph: the SpMV (with one p.q partial per block),
+// cg_update (alpha from those partials; r, z and the two dot products;
 // its last block forms beta, the history entry and the stop flag, and drives the graph's
-// while node), and cg_pupdate (p, the rounded copies of p that the next SpMV reads, and
+// while node), and cg_pupdate (x += alpha p, then p, the rounded copies of p that the next SpMV reads, and
 // the threshold controller's decisions). Reductions are per-thread FP64 partials in a
 // fixed order, a fixed shuffle tree per block, and a last-block sum over the blocks in
 // index order: bit-reproducible from run to run. FP64 instructions are only the method's
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
     }
 }
 
-// sigma = p.q from the SpMV's per-warp partials (summed in warp order, identically in every
+// sigma = p.q from the SpMV's partials (one per warp or per block; summed in order, identically in every
 // block), alpha = rho / sigma; then r -= alpha q; z = D^-1 r; r.z and ||r||^2 (x += alpha p is
 // left to the p-update, which reads p anyway). The last block appends the history entry, tests
 // convergence and forms beta. A sigma that is not finite and positive stops the solve with
@@ -224,6 +224,30 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
 __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(CgLaunch L, int npq)
 {
     DevState *st = L.st;
+    const int64_t n = L.n, nfull = n / 2;   // whole pairs; an odd last entry separately
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const bool jac = L.jacobi != 0;
+    // Every thread takes two pairs per pass (pair and pair + stride) and holds the next
+    // pass's q, r, dinv in registers while it does this pass's arithmetic, so that the loads
+    // stay in flight under the FP64 instructions (4 per entry with Jacobi, which on this part
+    // take about as long as streaming the entries). The first pass's loads go out before
+    // sigma is known: they do not depend on it.
+    double2 q[2], r[2], d[2];
+    auto ld2 = [](const double *a, int64_t j) { return *reinterpret_cast<const double2 *>(a + j); };
+    auto load = [&](int64_t pr) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t ph = pr + h * stride;
+            q[h] = r[h] = d[h] = make_double2(0.0, 0.0);
+            if (ph < nfull) {
+                q[h] = ld2(L.q, 2 * ph);
+                r[h] = ld2(L.r, 2 * ph);
+                if (jac) d[h] = ld2(L.dinv, 2 * ph);
+            }
+        }
+    };
+    int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    load(pair);
     if (st->done) {
         if (blockIdx.x == 0 && threadIdx.x == 0) {
             st->xstep = 0;
@@ -256,55 +280,45 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
     }
     const double alpha = s_alpha;
     if (isnan(alpha)) return;   // every block saw the same sigma
-    const int64_t n = L.n, nfull = n / 2;   // whole pairs; an odd last entry separately
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    // Two pairs per thread and pass, every load issued before any arithmetic, and two sets
-    // of dot-product partials, so that neither the loads nor the FP64 pipe wait on one
-    // chain of fused multiply-adds.
-    double rz0 = 0.0, rr0 = 0.0, rz1 = 0.0, rr1 = 0.0;
-    auto pair_update = [&](int64_t j, double2 q, double2 r, double2 d, double &rz, double &rr) {
-        r.x = fma(-alpha, q.x, r.x);
-        r.y = fma(-alpha, q.y, r.y);
-        *reinterpret_cast<double2 *>(L.r + j) = r;
-        rr = fma(r.x, r.x, rr);
-        rr = fma(r.y, r.y, rr);
-        if (L.jacobi) {
-            double2 z;
-            z.x = d.x * r.x;
-            z.y = d.y * r.y;
-            *reinterpret_cast<double2 *>(L.z + j) = z;
-            rz = fma(r.x, z.x, rz);
-            rz = fma(r.y, z.y, rz);
+    // two sets of dot-product partials, so that the FP64 pipe does not wait on one chain
+    double rzs[2] = {0.0, 0.0}, rrs[2] = {0.0, 0.0};
+    for (; pair < nfull; pair += 2 * stride) {
+        double2 cq[2], cr[2], cd[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) { cq[h] = q[h]; cr[h] = r[h]; cd[h] = d[h]; }
+        load(pair + 2 * stride);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t ph = pair + h * stride;
+            if (ph >= nfull) break;
+            double2 rv = cr[h];
+            rv.x = fma(-alpha, cq[h].x, rv.x);
+            rv.y = fma(-alpha, cq[h].y, rv.y);
+            *reinterpret_cast<double2 *>(L.r + 2 * ph) = rv;
+            rrs[h] = fma(rv.x, rv.x, rrs[h]);
+            rrs[h] = fma(rv.y, rv.y, rrs[h]);
+            if (jac) {
+                double2 z;
+                z.x = cd[h].x * rv.x;
+                z.y = cd[h].y * rv.y;
+                *reinterpret_cast<double2 *>(L.z + 2 * ph) = z;
+                rzs[h] = fma(rv.x, z.x, rzs[h]);
+                rzs[h] = fma(rv.y, z.y, rzs[h]);
+            }
         }
-    };
-    auto ld2 = [](const double *a, int64_t j) { return *reinterpret_cast<const double2 *>(a + j); };
-    int64_t pair = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    for (; pair + stride < nfull; pair += 2 * stride) {
-        const int64_t ja = 2 * pair, jb = 2 * (pair + stride);
-        const double2 qa = ld2(L.q, ja), qb = ld2(L.q, jb);
-        const double2 ra = ld2(L.r, ja), rb = ld2(L.r, jb);
-        double2 da = make_double2(0.0, 0.0), db = da;
-        if (L.jacobi) { da = ld2(L.dinv, ja); db = ld2(L.dinv, jb); }
-        pair_update(ja, qa, ra, da, rz0, rr0);
-        pair_update(jb, qb, rb, db, rz1, rr1);
-    }
-    if (pair < nfull) {
-        const int64_t j = 2 * pair;
-        const double2 d = L.jacobi ? ld2(L.dinv, j) : make_double2(0.0, 0.0);
-        pair_update(j, ld2(L.q, j), ld2(L.r, j), d, rz0, rr0);
     }
     if ((n & 1) && blockIdx.x == 0 && threadIdx.x == 0) {   // odd last entry
         const int64_t j = n - 1;
-        const double r = fma(-alpha, L.q[j], L.r[j]);
-        L.r[j] = r;
-        rr1 = fma(r, r, rr1);
-        if (L.jacobi) {
-            const double z = L.dinv[j] * r;
+        const double rv = fma(-alpha, L.q[j], L.r[j]);
+        L.r[j] = rv;
+        rrs[1] = fma(rv, rv, rrs[1]);
+        if (jac) {
+            const double z = L.dinv[j] * rv;
             L.z[j] = z;
-            rz1 = fma(r, z, rz1);
+            rzs[1] = fma(rv, z, rzs[1]);
         }
     }
-    const double rz = rz0 + rz1, rr = rr0 + rr1;
+    const double rz = rzs[0] + rzs[1], rr = rrs[0] + rrs[1];
     const double s_rz = block_sum_cg(rz);
     const double s_rr = block_sum_cg(rr);
     if (threadIdx.x == 0) {
@@ -342,51 +356,64 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
 // p = z + beta p, its rounded copies and the threshold rule when it is due; after the last
 // iteration only the x step.
 template <int T>
-__global__ void __launch_bounds__(kVecThreads) cg_pupdate_kernel(CgLaunch L)
+__global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_pupdate_kernel(CgLaunch L)
 {
     DevState *st = L.st;
-    const bool xs = st->xstep != 0, pdue = !st->done;
-    if (!xs && !pdue) return;
-    const double alpha = st->alpha, beta = st->beta;
     const int64_t n = L.n, npairs = (n + 1) / 2;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int lane = threadIdx.x & 31;
+    const double *zsrc = L.jacobi ? L.z : L.r;
+    // One pair per lane and pass; the next pass's p, x, z are loaded before this pass's
+    // arithmetic, and the first pass's before the solve state is read (none depends on it).
+    double2 p, x, z;
+    auto load = [&](int64_t base) {
+        const int64_t j = 2 * (base + lane);
+        p = x = z = make_double2(0.0, 0.0);
+        if (j + 1 < n) {
+            p = *reinterpret_cast<const double2 *>(L.p + j);
+            x = *reinterpret_cast<const double2 *>(L.x + j);
+            z = *reinterpret_cast<const double2 *>(zsrc + j);
+        }
+    };
+    int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+    load(base);
+    const bool xs = st->xstep != 0, pdue = !st->done;
+    if (!xs && !pdue) return;
+    const double alpha = st->alpha, beta = st->beta;
     const bool thr = pdue && (L.ctrl == EVOCG_CTRL_THRESHOLD) && (st->k % st->kstar == 0);
     const uint64_t lo_bits = (uint64_t)__double_as_longlong(st->eps_lo);
     const uint64_t hi_bits = (uint64_t)__double_as_longlong(st->eps_hi);
     const int64_t ncb = (n + T - 1) / T;
-    const double *zsrc = L.jacobi ? L.z : L.r;
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < npairs;
-         base += stride) {
+    for (; base < npairs; base += stride) {
+        double2 cp = p, cx = x;
+        const double2 cz = z;
+        load(base + stride);
         const int64_t pair = base + lane;
         uint64_t m = 0;
         if (pair < npairs) {
             const int64_t j = 2 * pair;
             if (j + 1 < n) {
-                double2 p = *reinterpret_cast<const double2 *>(L.p + j);
                 if (xs) {
-                    double2 x = *reinterpret_cast<const double2 *>(L.x + j);
-                    x.x = fma(alpha, p.x, x.x);
-                    x.y = fma(alpha, p.y, x.y);
-                    *reinterpret_cast<double2 *>(L.x + j) = x;
+                    cx.x = fma(alpha, cp.x, cx.x);
+                    cx.y = fma(alpha, cp.y, cx.y);
+                    *reinterpret_cast<double2 *>(L.x + j) = cx;
                 }
                 if (pdue) {
-                    const double2 z = *reinterpret_cast<const double2 *>(zsrc + j);
-                    p.x = fma(beta, p.x, z.x);
-                    p.y = fma(beta, p.y, z.y);
-                    *reinterpret_cast<double2 *>(L.p + j) = p;
-                    write_copies2(L, j, p.x, p.y);
-                    const uint64_t a0 = abs_bits(p.x), a1 = abs_bits(p.y);
+                    cp.x = fma(beta, cp.x, cz.x);
+                    cp.y = fma(beta, cp.y, cz.y);
+                    *reinterpret_cast<double2 *>(L.p + j) = cp;
+                    write_copies2(L, j, cp.x, cp.y);
+                    const uint64_t a0 = abs_bits(cp.x), a1 = abs_bits(cp.y);
                     m = a0 > a1 ? a0 : a1;
                 }
-            } else {
-                double p = L.p[j];
-                if (xs) L.x[j] = fma(alpha, p, L.x[j]);
+            } else {   // odd last entry
+                double pv = L.p[j];
+                if (xs) L.x[j] = fma(alpha, pv, L.x[j]);
                 if (pdue) {
-                    p = fma(beta, p, zsrc[j]);
-                    L.p[j] = p;
-                    write_copies(L, j, p);
-                    m = abs_bits(p);
+                    pv = fma(beta, pv, zsrc[j]);
+                    L.p[j] = pv;
+                    write_copies(L, j, pv);
+                    m = abs_bits(pv);
                 }
             }
         }
@@ -481,7 +508,7 @@ cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
     S.prec = (L.ctrl == EVOCG_CTRL_STATIC) ? L.prec : L.cbPrec;
     S.map_kind = (L.ctrl == EVOCG_CTRL_STATIC) ? L.map_kind : EVOCG_MAP_PER_COLBLOCK;
     S.force64 = force64;
-    S.dot = 1;             // per-warp p.q partials, summed by the update kernel
+    S.dot = 1;             // p.q partials (per warp or per block), summed by the update kernel
     S.pq = L.pq;
     S.gate = 1;
     S.partials = L.partials;
@@ -496,9 +523,9 @@ cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s)
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     switch (L.T) {
-    case 16: cg_pupdate_kernel<16><<<L.vec_grid, kVecThreads, 0, s>>>(L); break;
-    case 32: cg_pupdate_kernel<32><<<L.vec_grid, kVecThreads, 0, s>>>(L); break;
-    default: cg_pupdate_kernel<64><<<L.vec_grid, kVecThreads, 0, s>>>(L); break;
+    case 16: cg_pupdate_kernel<16><<<L.upd_grid, kVecThreads, 0, s>>>(L); break;
+    case 32: cg_pupdate_kernel<32><<<L.upd_grid, kVecThreads, 0, s>>>(L); break;
+    default: cg_pupdate_kernel<64><<<L.upd_grid, kVecThreads, 0, s>>>(L); break;
     }
     return cudaGetLastError();
 }

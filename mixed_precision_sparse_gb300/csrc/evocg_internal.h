@@ -12,9 +12,9 @@
 namespace evocg {
 
 constexpr int kMaxBlocks = 2048;      // upper bound of any grid here (partials buffers)
-constexpr int kMaxPq = 16384;         // per-warp p.q partials of one SpMV (grid x warps)
+constexpr int kMaxPq = 16384;         // p.q partials of one SpMV (grid x warps at most)
 constexpr int kVecThreads = 256;      // threads per block of the vector kernels
-constexpr int kUpdMinBlocks = 3;      // resident blocks per SM of the CG update kernel (its grid)
+constexpr int kUpdMinBlocks = 3;      // resident blocks per SM of the CG update and p-update kernels (their grid)
 constexpr int kSpmvThreads = 256;     // threads per block of the SpMV
 constexpr int kSpmvMinBlocks = 4;     // resident blocks per SM the SpMV registers are budgeted for
 constexpr int kMlpHiddenMax = 64;
@@ -110,7 +110,7 @@ struct SolveWS {
     double *b = nullptr, *x = nullptr, *r = nullptr, *p = nullptr, *q = nullptr, *z = nullptr;
     double *hist = nullptr;
     double *partials = nullptr;       // 2 * kMaxBlocks
-    double *pq = nullptr;             // kMaxPq per-warp p.q partials of the SpMV
+    double *pq = nullptr;             // kMaxPq p.q partials of the SpMV (per warp or per block)
     uint8_t *cbPrec = nullptr;        // controller decisions per column block
     uint8_t *logbuf = nullptr;        // device copy of a host decision log
     int64_t cap_log = 0;
@@ -235,7 +235,7 @@ struct SpmvLaunch {
     int map_kind;
     int force64;
     // p.q for CG (dot != 0): the sum over rows of x_i y_i, as spmv_dot_partials() partials in
-    // pq (one per warp, or one per block for the row-block kernel); the update kernel sums
+    // pq (one per warp, or one per block for the row-block and row-ELL kernels); the update kernel sums
     // them in order
     int dot;
     double *pq;
@@ -313,7 +313,7 @@ struct CgLaunch {
     float *x16f;
     double *hist;
     double *partials;
-    double *pq;            // the SpMV's per-warp p.q partials
+    double *pq;            // the SpMV's p.q partials (per warp or per block)
     uint8_t *cbPrec;       // controller output (map_kind 1 for the SpMV)
     const uint8_t *prec;   // static map
     int map_kind;
@@ -322,7 +322,7 @@ struct CgLaunch {
     double delta;
     DevState *st;
     int vec_grid, spmv_grid;
-    int upd_grid;          // grid of the update kernel (kUpdMinBlocks per SM)
+    int upd_grid;          // grid of the update and p-update kernels (kUpdMinBlocks per SM)
     uint8_t *map_log;      // device decision log (NULL: none), map_log_rows x ncb
     int64_t map_log_rows;
     cudaGraphConditionalHandle cond;
