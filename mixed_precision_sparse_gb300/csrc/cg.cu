@@ -45,6 +45,43 @@ __device__ __forceinline__ double block_sum_cg(double v)
     return s;
 }
 
+// Two block sums (blockDim.x == kVecThreads) with the same result bits as block_sum_cg but
+// far fewer FP64 warp instructions (each costs a sub-partition's FP64 unit 64 cycles however
+// few lanes it adds): the values go to shared memory, and warp 0 (for a) and warp 1 (for b)
+// replay every warp's shuffle tree there, level by level (level o: 8o sums, a warp's
+// position j < o plus position j + o), then add the eight warp totals in warp order.
+// The results are valid in every thread.
+__device__ __forceinline__ void tree_sum2(double a, double b, double &sa, double &sb)
+{
+    __shared__ double buf[2][kVecThreads];
+    __shared__ double res[2];
+    static_assert(kVecThreads == 256, "the tree below replays eight warps");
+    __syncthreads();   // earlier readers of res are done
+    buf[0][threadIdx.x] = a;
+    buf[1][threadIdx.x] = b;
+    __syncthreads();
+    const int wr = threadIdx.x >> 5, l = threadIdx.x & 31;
+    if (wr < 2) {
+        double *v = buf[wr];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            for (int i = l; i < 8 * o; i += 32) {
+                const int k = 32 * (i / o) + (i % o);
+                v[k] = v[k] + v[k + o];
+            }
+            __syncwarp();
+        }
+        if (l == 0) {
+            double t = 0.0;
+            for (int w = 0; w < kVecThreads / 32; ++w) t += v[32 * w];
+            res[wr] = t;
+        }
+    }
+    __syncthreads();
+    sa = res[0];
+    sb = res[1];
+}
+
 // Sum of gridDim.x partials in a fixed order; valid in thread 0 of the calling block.
 __device__ __forceinline__ double sum_partials(const double *part)
 {
@@ -55,7 +92,8 @@ __device__ __forceinline__ double sum_partials(const double *part)
 
 __device__ __forceinline__ uint64_t abs_bits(double v)
 {
-    return (uint64_t)__double_as_longlong(v) & 0x7FFFFFFFFFFFFFFFull;
+    const uint64_t u = (uint64_t)__double_as_longlong(v);
+    return ((uint64_t)abs_hi((uint32_t)(u >> 32)) << 32) | (uint32_t)u;
 }
 
 // Threshold rule of EvoCG §4.7 on segments of T entries held by T/2 consecutive lanes
@@ -259,7 +297,8 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
     {
         double v = 0.0;
         for (int i = threadIdx.x; i < npq; i += blockDim.x) v += __ldcg(L.pq + i);
-        const double sigma = block_sum_cg(v);
+        double sigma, unused;
+        tree_sum2(v, 0.0, sigma, unused);
         if (threadIdx.x == 0) {
             const bool ok = (sigma > 0.0) && isfinite(sigma);
             s_alpha = ok ? st->rho / sigma : 0.0;
@@ -318,16 +357,20 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(C
             rzs[1] = fma(rv, z, rzs[1]);
         }
     }
-    const double rz = rzs[0] + rzs[1], rr = rrs[0] + rrs[1];
-    const double s_rz = block_sum_cg(rz);
-    const double s_rr = block_sum_cg(rr);
+    double s_rz, s_rr;
+    tree_sum2(rzs[0] + rzs[1], rrs[0] + rrs[1], s_rz, s_rr);
     if (threadIdx.x == 0) {
         L.partials[blockIdx.x] = s_rz;
         L.partials[kMaxBlocks + blockIdx.x] = s_rr;
     }
     if (last_block_cg(st, TK_UPDATE)) {
-        const double RZ = sum_partials(L.partials);
-        const double RR = sum_partials(L.partials + kMaxBlocks);
+        double a = 0.0, b = 0.0;   // as sum_partials, both at once
+        for (int i = threadIdx.x; i < (int)gridDim.x; i += blockDim.x) {
+            a += __ldcg(L.partials + i);
+            b += __ldcg(L.partials + kMaxBlocks + i);
+        }
+        double RZ, RR;
+        tree_sum2(a, b, RZ, RR);
         if (threadIdx.x == 0) {
             st->tickets[TK_UPDATE] = 0;
             const int k = st->k + 1;
@@ -403,8 +446,10 @@ __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_pupdate_kernel(
                     cp.y = fma(beta, cp.y, cz.y);
                     *reinterpret_cast<double2 *>(L.p + j) = cp;
                     write_copies2(L, j, cp.x, cp.y);
-                    const uint64_t a0 = abs_bits(cp.x), a1 = abs_bits(cp.y);
-                    m = a0 > a1 ? a0 : a1;
+                    if (thr) {
+                        const uint64_t a0 = abs_bits(cp.x), a1 = abs_bits(cp.y);
+                        m = a0 > a1 ? a0 : a1;
+                    }
                 }
             } else {   // odd last entry
                 double pv = L.p[j];

@@ -69,13 +69,41 @@ __host__ __device__ __forceinline__ uint64_t f64_bits_from_f32(uint32_t u)
 }
 
 #ifdef __CUDACC__
+// |x|'s high word from x's, by a 32-bit AND the compiler keeps as one (a 64-bit mask of the
+// sign bit would be taken for an FP64 absolute value and run on the FP64 unit).
+__device__ __forceinline__ uint32_t abs_hi(uint32_t hi)
+{
+    uint32_t r;
+    asm("and.b32 %0, %1, 0x7fffffff;" : "=r"(r) : "r"(hi));
+    return r;
+}
+
+// The same rounding as rne_bits_from_f64, with a short path for results in the target's
+// normal range (FP64 exponents 897 .. 1150): the exponent and the top F fraction bits, rounded
+// to nearest even on the dropped bits (a carry moves into the exponent), rebiased from 1023
+// to 127. Zero, subnormal results, overflow, infinities and NaN take the general path.
+template <int F>
+__device__ __forceinline__ uint32_t rne_bits_dev(uint64_t u)
+{
+    const uint32_t hi = (uint32_t)(u >> 32), ahi = abs_hi(hi);
+    if ((ahi >> 20) - 897u <= 253u) {
+        constexpr int sh = 52 - F;
+        const uint64_t a = ((uint64_t)ahi << 32) | (uint32_t)u;
+        uint64_t q = a >> sh;
+        const uint64_t rem = a & ((1ull << sh) - 1ull), half = 1ull << (sh - 1);
+        q += (rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull;
+        return ((hi >> 31) << (F + 8)) | ((uint32_t)q - ((uint32_t)(1023 - 127) << F));
+    }
+    return rne_bits_from_f64<F>(u);
+}
+
 __device__ __forceinline__ float f32_from_f64_rn(double x)
 {
-    return __uint_as_float(rne_bits_from_f64<23>((uint64_t)__double_as_longlong(x)));
+    return __uint_as_float(rne_bits_dev<23>((uint64_t)__double_as_longlong(x)));
 }
 __device__ __forceinline__ uint16_t bf16_from_f64_rn(double x)
 {
-    return (uint16_t)rne_bits_from_f64<7>((uint64_t)__double_as_longlong(x));
+    return (uint16_t)rne_bits_dev<7>((uint64_t)__double_as_longlong(x));
 }
 __device__ __forceinline__ double f64_from_f32(float f)
 {
