@@ -110,17 +110,37 @@ def _workload(cfg):
     return W.workload(cfg)
 
 
-def _traffic_for(kernel_src_hash):
-    """Per-launch DRAM bytes of the SpMV from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def _traffic_for(kernel_src_hash, workload):
+    """Per-launch DRAM bytes of the SpMV from the committed ncu summary, if it was taken on
+    this workload and on the current kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", "spmv_traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    if d.get("kernel_src_sha256") != kernel_src_hash:
+    if d.get("kernel_src_sha256") != kernel_src_hash or d.get("workload", "").split(",")[0] != workload:
         return None
     return d.get("bytes_per_launch_full_size")
+
+
+def _spmv_kernel_label(G, dev):
+    """Which SpMV kernel the solve runs on this structure (the library's automatic choice):
+    the row-block kernel for tiles of 32, the panel kernel for 16, and for 64 the row-ELL
+    kernel when its plan exists (tiles holding about one entry per row), else the direct one."""
+    import torch
+
+    from mixed_precision_sparse_gb300 import evocg
+    if G.T == 32:
+        return "spmv_rowblock_kernel (warp per 32-row block, lane per row; single-entry tiles staged by cp.async)"
+    if G.T == 16:
+        return "spmv_panel_kernel (tiles of 16)"
+    x = torch.zeros(G.n, dtype=torch.float64, device=dev)
+    y = torch.empty_like(x)
+    try:
+        evocg.spmv_ex(G, x, y, evocg.SPMV_ROWELL)
+        return "spmv_rowell_kernel (row-ELL interior for tiles of 64 holding about one entry per row)"
+    except evocg.EvocgError:
+        return "spmv_kernel (direct, tiles of 64)"
 
 
 def _src_hash():
@@ -417,11 +437,11 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     spmv = spmv_measure(G, w, dev, stream, peak)
     src_hash = _src_hash()
-    traffic = _traffic_for(src_hash)
+    traffic = _traffic_for(src_hash, w.name)
     mixed = spmv["mixed_40_40_20"]
     roofline = {"bound": "hbm", "achieved": mixed["gbs"], "peak": peak, "unit": "GB/s",
                 "frac": mixed["frac_of_peak"], "traffic": traffic,
-                "kernel": "spmv_rowblock_kernel (row-block units staged by per-lane cp.async; mixed 40/40/20 map)",
+                "kernel": _spmv_kernel_label(G, dev) + "; mixed 40/40/20 map",
                 "peak_kind": peak_kind, "frac_of_8tbs": mixed["frac_of_8tbs"],
                 "bytes_per_launch": mixed["bytes"], "us_per_launch": mixed["us"],
                 "bytes_rule": "Tile-CSC algorithmic bytes: active value stream + 1 row-index "

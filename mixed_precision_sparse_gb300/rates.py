@@ -4,7 +4,7 @@
 
 Prints one JSON line per operation: FP64 FMA, FP32 FMA, the hardware FP64->FP32 and
 FP32->FP64 conversions, and the integer-pipe FP64->FP32 rounding the kernels use instead,
-each as operations per clock per SM (clock64 spans) and per second (CUDA events). The
+each as operations per second (CUDA events) and per clock per SM at the maximum SM clock. The
 conversion probes carry one 64-bit integer add and one FP32 add (or an integer OR and add)
 per conversion, so their figures are lower bounds on the conversion alone.
 """
@@ -49,7 +49,7 @@ def main(argv=None):
             it *= 4
         it = int(max(64, min(2_000_000, it * a.ms / max(ms, 1e-3))))
         ops, per_clk, ms = probe(lib, k, a.blocks_per_sm, it)
-        print(json.dumps({"op": name, "ops_per_clk_per_sm": round(per_clk, 3), "ops_per_s": ops,
+        print(json.dumps({"op": name, "ops_per_clk_per_sm_at_max_clock": round(per_clk, 3), "ops_per_s": ops,
                           "ms": round(ms, 3), "iters": it, "blocks_per_sm": a.blocks_per_sm,
                           "threads_per_block": 256, "chains_per_thread": 8}), flush=True)
     return 0

@@ -43,3 +43,15 @@ def test_no_gpu_is_reported_not_faked(lib):
     with pytest.raises(evocg.EvocgError) as e:
         evocg.tile_build(n, rp, ci, v, 16)
     assert e.value.code == evocg.EDEVICE
+
+
+def test_rate_probe_builds_and_exports():
+    """The arithmetic-rate probe (a measuring tool beside the library) builds for sm_103a and
+    exports its one entry point; with no GPU a call returns a CUDA error code, not rates."""
+    import ctypes
+    p = build.build_probe()
+    lib = ctypes.CDLL(p)
+    assert hasattr(lib, "evocg_rate_probe")
+    lib.evocg_rate_probe.restype = ctypes.c_int
+    d = [ctypes.c_double() for _ in range(3)]
+    assert lib.evocg_rate_probe(9, 4, 64, *[ctypes.byref(x) for x in d]) != 0   # unknown kind
