@@ -150,7 +150,15 @@ int upload_mlp(evocg_tiles *A, const evocg_ctrl *c, int *H1, int *H2)
         return fail(EVOCG_EINVAL, "MLP hidden widths must be in [1, 64]");
     if (!(c->delta >= 0.0)) return fail(EVOCG_EINVAL, "MLP delta must be >= 0");
     const int64_t T = A->T, h1 = c->hidden1, h2 = c->hidden2;
-    const int64_t words = h1 * T + h1 + h2 * h1 + h2 + 3 * h2 + 3;
+    const int64_t words = mlp_staged_words((int)T);   // the kernel's staged layout
+    if (words <= 0) return fail(EVOCG_EINVAL, "MLP controller needs tiles of 16, 32 or 64");
+    std::vector<float> staged;
+    try {
+        staged.resize((size_t)words);
+    } catch (const std::bad_alloc &) {
+        return fail(EVOCG_ENOMEM, "host allocation for the mlp weights");
+    }
+    mlp_stage_weights(c->weights, (int)T, (int)h1, (int)h2, staged.data());
     SolveWS &w = A->ws;
     if (w.cap_mlp < words) {
         release_graphs(w);  // the graphs hold the weight pointer
@@ -158,7 +166,7 @@ int upload_mlp(evocg_tiles *A, const evocg_ctrl *c, int *H1, int *H2)
         CK(dalloc(&w.mlpW, words), "cudaMalloc mlp weights");
         w.cap_mlp = words;
     }
-    CK(cudaMemcpy(w.mlpW, c->weights, sizeof(float) * (size_t)words, cudaMemcpyHostToDevice),
+    CK(cudaMemcpy(w.mlpW, staged.data(), sizeof(float) * (size_t)words, cudaMemcpyHostToDevice),
        "copy mlp weights");
     *H1 = (int)h1;
     *H2 = (int)h2;
@@ -419,6 +427,7 @@ extern "C" int evocg_tile_build(int64_t n, const int64_t *row_ptr, const int32_t
         else if (!std::strcmp(k, "rowell")) A->spmv_kind = SPMV_KIND_ROWELL;
     }
     A->vec_grid = sms * 4 > kMaxBlocks ? kMaxBlocks : sms * 4;
+    A->mlp_grid = mlp_grid_for(A->T, sms);
     *out = A;
     return EVOCG_OK;
 }

@@ -95,6 +95,7 @@ struct TilesView {
     const float *elV32;
     const uint16_t *elV16;
     int el_grid;
+    int mlp_grid;             // grid of the policy kernel: its resident blocks on every SM
 };
 
 // SpMV kernels: the row-block kernel (spmv_rowblock.cu; tiles of 32), the row-ELL kernel
@@ -170,6 +171,7 @@ struct evocg_tiles {
     uint16_t *elV16 = nullptr;
     int64_t el_slots = 0;
     int el_grid = 0;
+    int mlp_grid = 0;
     int *errw = nullptr;           // device error word (a lost stage wait)
     int spmv_kind = 0;             // default SpMV kernel (SPMV_KIND_*)
     uint8_t *tilePrec = nullptr;   // per-tile map
@@ -191,7 +193,7 @@ struct evocg_tiles {
                                 tileRowIdx, rowMask, tileWidth, colIdx, v64, v32, v16, colExp,
                                 errw, spmv_kind, pdesc, warpRec, panelRec, recPrec, nrec, panel_grid, panel_variant,
                                 rbMeta, rgDesc, sgCol, sgTile, sgV64, sgV32, sgV16, rb_grid,
-                                elBase, elCol, elPrec, elV64, elV32, elV16, el_grid};
+                                elBase, elCol, elPrec, elV64, elV32, elV16, el_grid, mlp_grid};
     }
 };
 
@@ -334,6 +336,12 @@ cudaError_t launch_cg_body(const CgLaunch &L, int force64, cudaStream_t s);
 cudaError_t launch_true_residual(const CgLaunch &L, cudaStream_t s);
 cudaError_t launch_ctrl_threshold(const TilesView &A, const double *p, double eps_lo,
                                   double eps_hi, uint8_t *cbPrec, cudaStream_t s);
+int mlp_grid_for(int T, int sms);   // resident policy-kernel blocks on every SM (0: none)
+// The policy weights in the layout the kernel stages (W1 and W2 transposed, zero-padded to
+// 64 outputs): mlp_staged_words(T) floats, written by mlp_stage_weights from the packed
+// layout of evocg_ctrl.weights.
+int64_t mlp_staged_words(int T);
+void mlp_stage_weights(const float *packed, int T, int H1, int H2, float *out);
 cudaError_t launch_ctrl_mlp(const TilesView &A, const double *p, const float *W, int H1,
                             int H2, double delta, uint8_t *cbPrec, float *logits,
                             const DevState *gate, cudaStream_t s);
