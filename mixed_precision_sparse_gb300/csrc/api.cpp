@@ -522,8 +522,12 @@ extern "C" int evocg_set_tile_precision(evocg_tiles_t A, const uint8_t *map, int
             for (int64_t t = 0; t < len; ++t) rp[(size_t)A->tileRec[(size_t)t]] = h[(size_t)t];
             CK(cudaMemcpyAsync(A->recPrec, rp.data(), rp.size(), cudaMemcpyHostToDevice, s), "upload map");
         }
-        if (map_kind == EVOCG_MAP_PER_TILE && A->elTile)   // the per-slot copy of the row-ELL plan
+        if (map_kind == EVOCG_MAP_PER_TILE && A->elTile) {   // the per-slot copy of the row-ELL plan,
+            // and its rows reordered by precision
             CK(launch_elprec(A->el_slots, A->elTile, A->tilePrec, A->elPrec, s), "per-slot map");
+            CK(launch_elsort(A->nrb, A->elBase, A->elCol, A->elTile, A->elV64, A->elV32, A->elV16,
+                             A->elPrec, s), "order row-ELL rows by precision");
+        }
         CK(cudaStreamSynchronize(s), "synchronise");
     }
     A->map_kind = map_kind;

@@ -285,6 +285,9 @@ bool rowblock_plan_ok(const HostTiles &H, const RowBlockPlan &P, std::string *wh
 cudaError_t launch_spmv_rowell(const SpmvLaunch &L, cudaStream_t s);
 int rowell_grid_for(int sms);
 cudaError_t launch_elprec(int64_t ns, const int32_t *tile, const uint8_t *tilePrec, uint8_t *out, cudaStream_t s);
+// Every row of the row-ELL blocks put in (precision, column) order (spmv_rowell.cu).
+cudaError_t launch_elsort(int64_t nrb, const int64_t *base, int32_t *col, int32_t *tile, double *v64,
+                          float *v32, uint16_t *v16, uint8_t *prec, cudaStream_t s);
 struct RowEllPlan {
     std::vector<int64_t> base;    // nrb + 1: first slot of every row block's ELL block
     std::vector<int32_t> col;     // absolute column (-1: pad), slot (k, r) at base + k*T + r
