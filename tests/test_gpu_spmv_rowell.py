@@ -77,3 +77,21 @@ def test_rowell_fp64_variants_in_a_solve():
     assert info["status"] == evocg.OK == ref["status"], info
     assert abs(info["iters"] - ref["iters"]) <= max(2, 0.03 * ref["iters"]), (info["iters"], ref["iters"])
     assert oracle.true_residual(P.A, b, x) <= 1e-8
+
+
+def test_rowell_row_order_depends_only_on_the_map():
+    """Setting a per-tile map puts every row's slots in (precision, column) order, whatever
+    order an earlier map left: the same map gives bit-identical products before and after
+    other maps (per tile and per column block), and the all-FP64 map restores column order
+    (its products equal the ones taken before any mixed map, bit for bit)."""
+    P = Pair(W.banded_spd(20000, 6, band=700), 64)
+    xh = np.random.default_rng(9).standard_normal(P.n)
+    x = torch.from_numpy(xh).cuda()
+    z = np.zeros(P.t.ntiles, np.uint8)
+    y64 = _run(P, x, z)
+    a, b = P.tile_map(11), P.tile_map(12, (0.2, 0.3, 0.5))
+    ya = _run(P, x, a)
+    _run(P, x, b)
+    _run(P, x, np.random.default_rng(3).integers(0, 3, P.t.nrb).astype(np.uint8), evocg.MAP_PER_COLBLOCK)
+    assert np.array_equal(_run(P, x, a).view(np.uint64), ya.view(np.uint64))
+    assert np.array_equal(_run(P, x, z).view(np.uint64), y64.view(np.uint64))
