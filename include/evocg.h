@@ -251,8 +251,12 @@ int evocg_rowell_plan_host(int64_t n, const int64_t *row_ptr, const int32_t *col
 /*
  * Set the precision map (EvoCG Eq. 9-10): codes EVOCG_FP64/FP32/BF16.
  *   map: host or device, len = ntiles (PER_TILE) or nrb (PER_COLBLOCK).
- * The SpMV and static-map solves read the map set last. Errors: EINVAL on a wrong length
- * or a code above 2 (the map is checked on the host; a device map is copied there).
+ * The SpMV and static-map solves read the map set last. With the row-ELL kernel (tiles of
+ * 64 holding about one entry per row) a PER_TILE map also reorders every row's entries by
+ * (precision, column) on the device, which changes the order of a row's sum but not its
+ * terms; the order is a function of the map alone (all-FP64: column order). Synchronises
+ * the stream. Errors: EINVAL on a wrong length or a code above 2 (the map is checked on the
+ * host; a device map is copied there).
  */
 int evocg_set_tile_precision(evocg_tiles_t A, const uint8_t *map, int64_t len,
                              int map_kind, void *stream);
