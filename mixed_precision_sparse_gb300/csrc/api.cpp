@@ -173,7 +173,9 @@ int upload_mlp(evocg_tiles *A, const evocg_ctrl *c, int *H1, int *H2)
     return EVOCG_OK;
 }
 
-int build_graph(CgLaunch L, int restart, cudaGraph_t *graph_out, cudaGraphExec_t *exec_out)
+// force64: the loop's SpMV runs its all-FP64 variant (the FP64 finish, or a static map whose
+// codes are all FP64: the same products without reading a precision code)
+int build_graph(CgLaunch L, int restart, int force64, cudaGraph_t *graph_out, cudaGraphExec_t *exec_out)
 {
     cudaStream_t cs = nullptr;
     CK(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking), "cudaStreamCreate (capture)");
@@ -230,7 +232,7 @@ int build_graph(CgLaunch L, int restart, cudaGraph_t *graph_out, cudaGraphExec_t
         cudaGraph_t body = np.conditional.phGraph_out[0];
         e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal);
         if (e == cudaSuccess) {
-            cudaError_t e1 = launch_cg_body(L, restart, cs);
+            cudaError_t e1 = launch_cg_body(L, force64, cs);
             cudaGraph_t bb = nullptr;
             cudaError_t e2 = cudaStreamEndCapture(cs, &bb);
             e = (e1 != cudaSuccess) ? e1 : e2;
@@ -256,7 +258,7 @@ int build_graph(CgLaunch L, int restart, cudaGraph_t *graph_out, cudaGraphExec_t
 // conditional nodes list every kernel of the solve this way.
 constexpr int kPlainBatch = 32;
 
-int run_plain(evocg_tiles *A, CgLaunch L, int restart, cudaStream_t s)
+int run_plain(evocg_tiles *A, CgLaunch L, int restart, int force64, cudaStream_t s)
 {
     SolveWS &w = A->ws;
     L.use_cond = 0;
@@ -274,7 +276,7 @@ int run_plain(evocg_tiles *A, CgLaunch L, int restart, cudaStream_t s)
         CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");
         CK(cudaStreamSynchronize(s), "synchronise");
         if (w.st_host->done) break;
-        for (int i = 0; i < kPlainBatch; ++i) CK(launch_cg_body(L, restart, s), "cg body");
+        for (int i = 0; i < kPlainBatch; ++i) CK(launch_cg_body(L, force64, s), "cg body");
     }
     return EVOCG_OK;
 }
@@ -531,6 +533,9 @@ extern "C" int evocg_set_tile_precision(evocg_tiles_t A, const uint8_t *map, int
         CK(cudaStreamSynchronize(s), "synchronise");
     }
     A->map_kind = map_kind;
+    A->map_all64 = 1;
+    for (int64_t i = 0; i < len; ++i)
+        if (h[(size_t)i] != EVOCG_FP64) { A->map_all64 = 0; break; }
     return EVOCG_OK;
 }
 
@@ -596,7 +601,8 @@ extern "C" int evocg_spmv_ex(evocg_tiles_t A, const double *x, double *y, int fl
     S.x64 = xd; S.x32 = A->x32; S.x16f = A->x16f; S.y = yd;
     S.prec = (A->map_kind == EVOCG_MAP_PER_TILE) ? A->tilePrec : A->cbPrec;
     S.map_kind = A->map_kind;
-    S.force64 = 0; S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
+    S.force64 = A->map_all64;   // an all-FP64 map: the same products without reading codes
+    S.dot = 0; S.st = nullptr; S.census = 0; S.grid = A->spmv_grid;
     S.direct = kdirect;
     S.kind = kkind;
     S.test_lost_wait = (flags & EVOCG_SPMV_TEST_LOST_WAIT) ? 1 : 0;
@@ -741,17 +747,20 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     L.map_log_rows = logging ? ctrl->map_log_rows : 0;
     L.cond = 0;
 
-    // graph cache: the key is every launch parameter (the handle aside)
+    // a static map whose codes are all FP64 runs the SpMV's all-FP64 variant (same products)
+    const int f64 = (kind == EVOCG_CTRL_STATIC && A->map_all64) ? 1 : 0;
+    // graph cache: the key is every launch parameter (the handle aside) and the variant
     uint64_t key = 1469598103934665603ull;
     {
         const unsigned char *pb = reinterpret_cast<const unsigned char *>(&L);
         for (size_t i = 0; i < sizeof(L); ++i) key = (key ^ pb[i]) * 1099511628211ull;
+        key = (key ^ (uint64_t)f64) * 1099511628211ull;
     }
     const bool use_graph = graphs_enabled();
     if (use_graph && (!w.exec || w.exec_key != key)) {
         if (w.exec) { cudaGraphExecDestroy(w.exec); w.exec = nullptr; }
         if (w.graph) { cudaGraphDestroy(w.graph); w.graph = nullptr; }
-        rc = build_graph(L, 0, &w.graph, &w.exec);
+        rc = build_graph(L, 0, f64, &w.graph, &w.exec);
         if (rc) return rc;
         w.exec_key = key;
     }
@@ -769,7 +778,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
     if (use_graph) {
         CK(cudaGraphLaunch(w.exec, s), "cudaGraphLaunch");
     } else {
-        rc = run_plain(A, L, 0, s);
+        rc = run_plain(A, L, 0, f64, s);
         if (rc) return rc;
     }
     CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");
@@ -794,7 +803,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
             if (use_graph && (!w.exec_rs || w.exec_rs_key != rkey)) {
                 if (w.exec_rs) { cudaGraphExecDestroy(w.exec_rs); w.exec_rs = nullptr; }
                 if (w.graph_rs) { cudaGraphDestroy(w.graph_rs); w.graph_rs = nullptr; }
-                rc = build_graph(R, 1, &w.graph_rs, &w.exec_rs);
+                rc = build_graph(R, 1, 1, &w.graph_rs, &w.exec_rs);
                 if (rc) return rc;
                 w.exec_rs_key = rkey;
             }
@@ -802,7 +811,7 @@ extern "C" int evocg_cg_solve(evocg_tiles_t A, const double *b, double *x, doubl
             if (use_graph) {
                 CK(cudaGraphLaunch(w.exec_rs, s), "cudaGraphLaunch (restart)");
             } else {
-                rc = run_plain(A, R, 1, s);
+                rc = run_plain(A, R, 1, 1, s);
                 if (rc) return rc;
             }
             CK(cudaMemcpyAsync(w.st_host, w.st, sizeof(DevState), cudaMemcpyDeviceToHost, s), "read state");

@@ -177,6 +177,7 @@ struct evocg_tiles {
     uint8_t *tilePrec = nullptr;   // per-tile map
     uint8_t *cbPrec = nullptr;     // per-column-block map
     int map_kind = EVOCG_MAP_PER_TILE;
+    int map_all64 = 1;   // every code of the map set last is FP64: the FP64 kernel variants run
     double *dinv = nullptr;        // 1 / a_ii (Jacobi)
     int diag_ok = 0;               // every diagonal entry present and > 0
     // SpMV scratch: rounded x copies and host staging
