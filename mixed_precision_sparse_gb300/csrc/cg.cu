@@ -254,11 +254,11 @@ __global__ void __launch_bounds__(kVecThreads) cg_init_kernel(CgLaunch L, int re
     }
 }
 
-// sigma = p.q from the SpMV's partials (one per warp or per block; summed in order, identically in every
-// block), alpha = rho / sigma; then r -= alpha q; z = D^-1 r; r.z and ||r||^2 (x += alpha p is
-// left to the p-update, which reads p anyway). The last block appends the history entry, tests
-// convergence and forms beta. A sigma that is not finite and positive stops the solve with
-// EVOCG_EBREAKDOWN.
+// sigma = p.q from the SpMV's partials (one per warp or per block, summed in order, identically
+// in every block), alpha = rho / sigma; then r -= alpha q; z = D^-1 r; r.z and ||r||^2 (x +=
+// alpha p is left to the p-update, which reads p anyway). The last block appends the history
+// entry, tests convergence and forms beta. A sigma that is not finite and positive stops the
+// solve with EVOCG_EBREAKDOWN.
 __global__ void __launch_bounds__(kVecThreads, kUpdMinBlocks) cg_update_kernel(CgLaunch L, int npq)
 {
     DevState *st = L.st;
