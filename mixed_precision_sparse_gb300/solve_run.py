@@ -6,8 +6,9 @@
 The workload's own settings (preconditioner, controller or static map, rtol, maxit) are used
 unless overridden: --maxit caps the iterations (a short run of the same per-iteration kernels,
 for profilers), --fp64 sets every tile to FP64 with no controller, --no-finish skips the FP64
-finish, --relative scales the threshold rule's cut points by ||b||_inf. Prints one JSON line: status, iterations, true residual, precision census, seconds
-(wall clock of the call, including the graph build on first use). With EVOCG_GRAPH=0 in the
+finish, --relative scales the threshold rule's cut points by ||b||_inf. Prints one JSON line:
+status, iterations, true residual, precision census, seconds (wall clock of the call,
+including the graph build on first use). With EVOCG_GRAPH=0 in the
 environment every kernel of the solve is a plain launch.
 """
 from __future__ import annotations
