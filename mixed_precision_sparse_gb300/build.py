@@ -53,8 +53,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     deps = _headers()
     common = ["-std=c++17", "-O3", "-I", INC, "-I", CSRC, "-Xcompiler", "-fPIC"]
-    # extra nvcc flags from EVOCG_NVCC_FLAGS (none by default, e.g. -lineinfo variants for a
-    # profiler); recorded in each object's stamp so that a change of flags rebuilds it
+    # extra nvcc flags from EVOCG_NVCC_FLAGS (none by default; e.g. -Xptxas=-v for register and
+    # spill counts); recorded in each object's stamp so that a change of flags rebuilds it
     extra = os.environ.get("EVOCG_NVCC_FLAGS", "").split()
     common += extra
     jobs = []
